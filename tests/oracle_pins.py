@@ -1,0 +1,390 @@
+"""Checks that pin the CPU oracle to things other than itself.
+
+Each `pin_*` function takes the oracle *module* and returns a list of failure
+messages (empty = the pin holds).  Taking the module lets the mutation tests
+plant a mistake in a private copy of the oracle and confirm some pin catches it.
+
+What the pins compare against:
+  * library routines in float64 (torch scaled_dot_product_attention, softmax,
+    logsumexp, amax; numpy unpackbits);
+  * brute force over every subset of block masses;
+  * exact closed-form selections (tests/golden/selection_cases.json);
+  * the pages' density example (tests/golden/union_density_example.json);
+  * invariances the pages state: all-blocks sparse is dense bitwise, block
+    masses from the LSE equal softmax block sums, the union equals the OR of
+    per-depth selections; and the page layout cannot matter.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+from typing import List
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from block_sparse_paged_split_gb300.workload import (MODE_DENSE, MODE_DISCOVER,
+                                                     MODE_DISCOVER_UNION, MODE_SPARSE,
+                                                     custom_workload)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def as_oracle_array(t: torch.Tensor) -> np.ndarray:
+    """torch CPU tensor -> the array form the oracle takes (bf16 as uint16 bits)."""
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.contiguous().numpy()
+
+
+def make_case(Hq, Hkv, D, dtype, lens, seed, pool_factor=2, n_planted=2):
+    lens = np.asarray(lens, np.int32)
+    w = custom_workload(R=len(lens), Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, depths=1,
+                        n_planted=n_planted, seq_lens=lens, pool_factor=pool_factor,
+                        seed=seed, depth_modes=[np.zeros(len(lens), np.int8)])
+    return w, w.depth_inputs(0, logical=True)
+
+
+def run(O, w, d, modes, support, eta=0.95, page_table=None, k_cache=None, v_cache=None):
+    return O.decode_layer(as_oracle_array(d["q"]),
+                          as_oracle_array(d["k_cache"] if k_cache is None else k_cache),
+                          as_oracle_array(d["v_cache"] if v_cache is None else v_cache),
+                          w.page_table if page_table is None else page_table,
+                          w.seq_lens, np.asarray(modes, np.int8), support, eta=eta,
+                          tile_tokens=w.tile_tokens)
+
+
+def empty_support(w) -> np.ndarray:
+    return np.zeros((w.num_rows, w.num_kv_heads, -(-w.max_blocks // 32)), np.uint32)
+
+
+def random_support(w, seed, density=0.4) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    W = -(-w.max_blocks // 32)
+    bits = rng.random((w.num_rows, w.num_kv_heads, W * 32)) < density
+    return np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(
+        w.num_rows, w.num_kv_heads, W).copy()
+
+
+def library_bits(words: np.ndarray, nb: int) -> np.ndarray:
+    """Mask bits decoded by numpy's unpackbits (little-endian words)."""
+    return np.unpackbits(np.ascontiguousarray(words, dtype="<u4").view(np.uint8),
+                         bitorder="little")[:nb].astype(bool)
+
+
+def _ref_row(d, r, g, h):
+    K = d["k_rows"][r][:, g, :].double()
+    V = d["v_rows"][r][:, g, :].double()
+    q = d["q"][r, h].double()
+    return q, K, V
+
+
+def _sdpa(q, K, V, scale, mask=None):
+    am = None if mask is None else torch.as_tensor(mask)[None, None, None, :]
+    return F.scaled_dot_product_attention(q[None, None, None, :], K[None, None], V[None, None],
+                                          attn_mask=am, scale=scale)[0, 0, 0]
+
+
+# ----------------------------------------------------------------------------------- pins
+def pin_dense_sdpa(O) -> List[str]:
+    """Dense output equals torch SDPA (float64), LSE equals torch.logsumexp of the
+    scaled scores; MHA and GQA, fp32 and bf16 storage, ragged lengths."""
+    fails = []
+    for (Hq, Hkv, D, dt, lens, seed) in [(2, 2, 64, "f32", [70, 33, 96, 1, 0], 11),
+                                         (4, 2, 128, "bf16", [100, 31, 64], 12)]:
+        w, d = make_case(Hq, Hkv, D, dt, lens, seed)
+        res = run(O, w, d, [MODE_DENSE] * len(lens), empty_support(w))
+        scale = 1.0 / math.sqrt(D)
+        G = Hq // Hkv
+        for r, L in enumerate(lens):
+            for h in range(Hq):
+                if L == 0:
+                    if not (np.all(res["out"][r, h] == 0) and res["lse"][r, h] == -math.inf):
+                        fails.append(f"padding row {r} head {h} not zero/-inf")
+                    continue
+                q, K, V = _ref_row(d, r, h // G, h)
+                o = _sdpa(q, K, V, scale).numpy()
+                lse = torch.logsumexp(scale * torch.mv(K, q), 0).item()
+                if not np.allclose(res["out"][r, h], o, rtol=1e-10, atol=1e-12):
+                    fails.append(f"dense out differs r={r} h={h}")
+                if abs(res["lse"][r, h] - lse) > 1e-10:
+                    fails.append(f"dense lse differs r={r} h={h}")
+    return fails
+
+
+def pin_sparse_masked_sdpa(O) -> List[str]:
+    """Sparse output equals SDPA under the boolean tile mask [WISE PR, Tests:
+    sparse output matches masked attention]; an empty support gives 0/-inf."""
+    fails = []
+    for (Hq, Hkv, D, dt, lens, seed) in [(2, 2, 64, "f32", [200, 65, 130, 31], 21),
+                                         (4, 2, 128, "bf16", [250, 96], 22)]:
+        w, d = make_case(Hq, Hkv, D, dt, lens, seed)
+        sup = random_support(w, seed)
+        sup[0, 0, :] = 0  # one (row, head) with nothing selected
+        res = run(O, w, d, [MODE_SPARSE] * len(lens), sup)
+        scale = 1.0 / math.sqrt(D)
+        G = Hq // Hkv
+        for r, L in enumerate(lens):
+            nb = -(-L // w.tile_tokens)
+            for h in range(Hq):
+                g = h // G
+                blocks = library_bits(sup[r, g], nb)
+                mask = np.repeat(blocks, w.tile_tokens)[:L]
+                if not mask.any():
+                    if not (np.all(res["out"][r, h] == 0) and res["lse"][r, h] == -math.inf):
+                        fails.append(f"empty support r={r} h={h} not zero/-inf")
+                    continue
+                q, K, V = _ref_row(d, r, g, h)
+                o = _sdpa(q, K, V, scale, mask).numpy()
+                s = scale * torch.mv(K, q)
+                lse = torch.logsumexp(s[torch.from_numpy(mask)], 0).item()
+                if not np.allclose(res["out"][r, h], o, rtol=1e-10, atol=1e-12):
+                    fails.append(f"sparse out differs r={r} h={h}")
+                if abs(res["lse"][r, h] - lse) > 1e-10:
+                    fails.append(f"sparse lse differs r={r} h={h}")
+    return fails
+
+
+def pin_all_blocks_sparse_is_dense(O) -> List[str]:
+    """Every block selected: sparse equals dense bitwise [WISE PR, Tests:
+    compaction with every block selected is bitwise dense]."""
+    w, d = make_case(4, 2, 128, "bf16", [130, 64, 33], 31)
+    full = np.full_like(empty_support(w), 0xFFFFFFFF)
+    dense = run(O, w, d, [MODE_DENSE] * 3, empty_support(w))
+    sparse = run(O, w, d, [MODE_SPARSE] * 3, full)
+    if not (np.array_equal(dense["out"], sparse["out"]) and np.array_equal(dense["lse"], sparse["lse"])):
+        return ["all-blocks sparse differs from dense"]
+    return []
+
+
+def pin_paging_invariance(O) -> List[str]:
+    """Moving pages around the pool (and adding NaN-filled pages no row
+    references) leaves every output bitwise unchanged."""
+    w, d = make_case(2, 2, 64, "f32", [90, 17, 48], 41, pool_factor=1)
+    base = run(O, w, d, [MODE_DENSE, MODE_DISCOVER, MODE_DENSE], empty_support(w))
+    rng = np.random.default_rng(5)
+    n = w.num_pages
+    new_n = 3 * n
+    where = rng.permutation(new_n)[:n]          # old page p -> new page where[p]
+    kc = torch.full((new_n,) + tuple(d["k_cache"].shape[1:]), float("nan"), dtype=d["k_cache"].dtype)
+    vc = kc.clone()
+    kc[torch.from_numpy(where)] = d["k_cache"]
+    vc[torch.from_numpy(where)] = d["v_cache"]
+    pt = np.where(w.page_table >= 0, where[np.maximum(w.page_table, 0)], -1).astype(np.int32)
+    moved = run(O, w, d, [MODE_DENSE, MODE_DISCOVER, MODE_DENSE], empty_support(w),
+                page_table=pt, k_cache=kc, v_cache=vc)
+    fails = []
+    for key in ("out", "lse", "support"):
+        if not np.array_equal(base[key], moved[key]):
+            fails.append(f"page layout changed {key}")
+    return fails
+
+
+def pin_block_masses(O) -> List[str]:
+    """Per-tile stats and block masses against library softmax/logsumexp:
+    m_b = amax over the tile; p_b = sum of the tile's softmax probabilities;
+    sum_b p_b = 1; logsumexp_b(m_b + log l_b) = LSE; and the LSE-derived mass
+    l_b * exp(m_b - LSE) equals p_b [WISE PR, Tests: LSE-derived block mass
+    matches softmax block sums]."""
+    fails = []
+    w, d = make_case(4, 2, 64, "f32", [200, 47, 32, 1], 51)
+    res = run(O, w, d, [MODE_DISCOVER] * 4, empty_support(w))
+    scale = 1.0 / math.sqrt(w.head_dim)
+    B = w.tile_tokens
+    for (r, h), dg in res["diag"].items():
+        L = int(w.seq_lens[r])
+        q, K, _ = _ref_row(d, r, h // w.group, h)
+        s = scale * torch.mv(K, q)
+        prob = torch.softmax(s, 0)
+        nb = -(-L // B)
+        for b in range(nb):
+            blk = slice(b * B, min((b + 1) * B, L))
+            if abs(dg["p"][b] - prob[blk].sum().item()) > 1e-12:
+                fails.append(f"p_b != softmax block sum r={r} h={h} b={b}")
+            if abs(dg["m_b"][b] - torch.amax(s[blk]).item()) > 1e-12:
+                fails.append(f"m_b != amax r={r} h={h} b={b}")
+            lse_mass = dg["l_b"][b] * math.exp(dg["m_b"][b] - res["lse"][r, h])
+            if abs(lse_mass - dg["p"][b]) > 1e-12:
+                fails.append(f"LSE-derived mass differs r={r} h={h} b={b}")
+        if abs(dg["p"].sum() - 1.0) > 1e-12:
+            fails.append(f"masses do not sum to 1 r={r} h={h}")
+        blk_lse = torch.logsumexp(torch.tensor(dg["m_b"] + np.log(dg["l_b"])), 0).item()
+        if abs(blk_lse - res["lse"][r, h]) > 1e-10:
+            fails.append(f"logsumexp of tile stats != lse r={r} h={h}")
+    return fails
+
+
+def _brute_force_k(p: np.ndarray, eta: float):
+    n = p.shape[0]
+    for k in range(1, n + 1):
+        best = max(sum(p[list(c)]) for c in itertools.combinations(range(n), k))
+        if best >= eta:
+            return k, best
+    return n, p.sum()
+
+
+def pin_selection_bruteforce(O) -> List[str]:
+    """Over every subset: k* is the least size of any block set whose mass
+    reaches eta, and the chosen set has the largest mass of that size."""
+    fails = []
+    rng = np.random.default_rng(61)
+    for trial in range(150):
+        n = int(rng.integers(1, 11))
+        p = rng.dirichlet(np.full(n, rng.uniform(0.2, 3.0))).astype(np.float32).astype(np.float64)
+        eta = float(rng.uniform(0.05, 0.999))
+        C = np.cumsum(np.sort(p)[::-1])
+        if np.any(np.abs(C - eta) < 1e-9):
+            continue
+        k, best = _brute_force_k(p, eta)
+        got = O.select_blocks(p, eta)
+        if got["k"] != k or int(got["sel"].sum()) != k:
+            fails.append(f"trial {trial}: k*={got['k']} brute force {k}")
+        elif abs(p[got["sel"]].sum() - best) > 1e-12:
+            fails.append(f"trial {trial}: chosen mass {p[got['sel']].sum()} < best {best}")
+    return fails
+
+
+def pin_selection_golden(O) -> List[str]:
+    with open(os.path.join(GOLDEN, "selection_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    fails = []
+    for c in cases:
+        got = O.select_blocks(np.array(c["p"], np.float64), c["eta"])
+        if sorted(np.nonzero(got["sel"])[0].tolist()) != c["selected"]:
+            fails.append(f"golden p={c['p']} eta={c['eta']}: got {np.nonzero(got['sel'])[0].tolist()}")
+    return fails
+
+
+def pin_selection_limits(O) -> List[str]:
+    """eta = 1 takes every block; a tiny eta takes exactly the arg-max block
+    (lowest index among equal maxima); a larger eta never takes fewer blocks."""
+    fails = []
+    rng = np.random.default_rng(71)
+    for trial in range(100):
+        n = int(rng.integers(1, 40))
+        p = rng.dirichlet(np.ones(n)).astype(np.float32).astype(np.float64)
+        if not O.select_blocks(p, 1.0)["sel"].all():
+            fails.append("eta=1 did not select every block")
+        tiny = O.select_blocks(p, 1e-9)["sel"]
+        if np.nonzero(tiny)[0].tolist() != [int(np.argmax(p))]:
+            fails.append("tiny eta did not select exactly the arg-max")
+        prev = np.zeros(n, bool)
+        for eta in np.linspace(0.05, 0.99, 12):
+            sel = O.select_blocks(p, float(eta))["sel"]
+            if np.any(prev & ~sel):
+                fails.append("selection not monotone in eta")
+                break
+            prev = sel
+    return fails
+
+
+def pin_union(O) -> List[str]:
+    """Discover at depth 0, then union-discover at depth 1, equals the OR of the
+    two depths' own selections [WISE PR, Tests: the fused selection matches
+    the union across discovery depths]."""
+    fails = []
+    w = custom_workload(R=3, Hq=2, Hkv=2, D=64, dtype="f32", depths=2, n_planted=2,
+                        seq_lens=np.array([256, 100, 64], np.int32), pool_factor=1, seed=81,
+                        depth_modes=[np.zeros(3, np.int8)] * 2)
+    d0, d1 = w.depth_inputs(0, logical=True), w.depth_inputs(1, logical=True)
+    z = empty_support(w)
+    s0 = run(O, w, d0, [MODE_DISCOVER] * 3, z)["support"]
+    s1 = run(O, w, d1, [MODE_DISCOVER] * 3, z)["support"]
+    u = run(O, w, d1, [MODE_DISCOVER_UNION] * 3, s0)["support"]
+    if not np.array_equal(u, s0 | s1):
+        fails.append("union-discover != OR of per-depth selections")
+    if not np.array_equal(O.support_union(s0, s1), s0 | s1):
+        fails.append("support_union != bitwise OR")
+    # The union mask really contains both selections (no overwrite).
+    for r in range(3):
+        for g in range(2):
+            nb = -(-int(w.seq_lens[r]) // 32)
+            a, b, c = (library_bits(x[r, g], nb) for x in (s0, s1, u))
+            if not np.array_equal(c, a | b):
+                fails.append(f"union bits differ r={r} g={g}")
+    return fails
+
+
+def _two_block_input(hot_block: int):
+    """One row, one head, D=64, 64 tokens (two causal blocks): every key of the
+    hot block equals q, every other key is zero, so the hot block carries all
+    but e^-8 of the mass."""
+    D, L, P = 64, 64, 16
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = 8.0
+    k = np.zeros((L // P, P, 1, D), np.float32)
+    v = np.random.default_rng(hot_block).standard_normal((L // P, P, 1, D)).astype(np.float32)
+    for j in range(hot_block * 32, hot_block * 32 + 32):
+        k[j // P, j % P, 0, 0] = 8.0
+    return q, k, v, np.arange(L // P, dtype=np.int32)[None, :], np.array([L], np.int32)
+
+
+def pin_density_example(O) -> List[str]:
+    """The pages' worked example: two disjoint one-block selections over two
+    causal blocks give a reused-union density of 1.0 (per-selection 0.5)."""
+    with open(os.path.join(GOLDEN, "union_density_example.json")) as f:
+        gold = json.load(f)
+    fails = []
+    sup = np.zeros((1, 1, 1), np.uint32)
+    sels = []
+    for depth, hot in enumerate((0, 1)):
+        q, k, v, pt, lens = _two_block_input(hot)
+        mode = MODE_DISCOVER if depth == 0 else MODE_DISCOVER_UNION
+        res = O.decode_layer(q, k, v, pt, lens, np.array([mode], np.int8), sup, eta=0.95)
+        sels.append(np.nonzero(res["diag"][(0, 0)]["sel"])[0].tolist())
+        sup = res["support"]
+    if sels != gold["depth_selections"]:
+        fails.append(f"per-depth selections {sels}")
+    if np.nonzero(library_bits(sup[0, 0], 2))[0].tolist() != gold["union_blocks"]:
+        fails.append("union blocks differ")
+    dens = O.union_density(sup, np.array([64]), 32)
+    if dens != gold["union_density"]:
+        fails.append(f"union density {dens}")
+    per_sel = np.mean([len(s) for s in sels]) / gold["causal_blocks"]
+    if per_sel != gold["per_selection_density"]:
+        fails.append(f"per-selection density {per_sel}")
+    return fails
+
+
+def pin_compaction(O) -> List[str]:
+    """Tile lists decoded with numpy.unpackbits, and work items: 1..T tiles each,
+    the fewest items possible, concatenating back to the strictly ascending
+    list; dense and discover rows list every block."""
+    fails = []
+    rng = np.random.default_rng(91)
+    for trial in range(20):
+        R, H = int(rng.integers(1, 5)), int(rng.integers(1, 4))
+        lens = rng.integers(0, 300, size=R).astype(np.int32)
+        W = max(1, -(-int(-(-lens.max() // 32)) // 32)) + int(rng.integers(0, 2))
+        bits = rng.random((R, H, W * 32)) < rng.uniform(0, 1)
+        sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, H, W).copy()
+        modes = rng.choice([MODE_DENSE, MODE_DISCOVER, MODE_DISCOVER_UNION, MODE_SPARSE], size=R).astype(np.int8)
+        T = int(rng.choice([1, 3, 8]))
+        res = O.compact_tiles(sup, modes, lens, 32, T)
+        items = res["items"]
+        for r in range(R):
+            nb = -(-int(lens[r]) // 32)
+            for g in range(H):
+                want = (np.nonzero(library_bits(sup[r, g], nb))[0] if modes[r] == MODE_SPARSE
+                        else np.arange(nb))
+                lst = res["lists"][r][g]
+                if not np.array_equal(lst, want):
+                    fails.append(f"trial {trial} list r={r} g={g}")
+                mine = items[(items[:, 0] == r) & (items[:, 1] == g)]
+                if mine.shape[0] != -(-want.shape[0] // T):
+                    fails.append(f"trial {trial} item count r={r} g={g}")
+                if mine.shape[0] and (mine[:, 3].min() < 1 or mine[:, 3].max() > T):
+                    fails.append(f"trial {trial} item size r={r} g={g}")
+                cat = np.concatenate([lst[a:a + c] for (_, _, a, c) in mine]) if mine.shape[0] else np.zeros(0)
+                if not np.array_equal(cat, want) or np.any(np.diff(cat) <= 0):
+                    fails.append(f"trial {trial} items do not cover list r={r} g={g}")
+    return fails
+
+
+ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_all_blocks_sparse_is_dense,
+            pin_paging_invariance, pin_block_masses, pin_selection_bruteforce,
+            pin_selection_golden, pin_selection_limits, pin_union, pin_density_example,
+            pin_compaction]
