@@ -1,0 +1,18 @@
+"""WISE working-set paged decode attention for GB300 (sm_103a).
+
+The compute lives in libwise.so (hand-written CUDA; C ABI in include/wise.h);
+`block_sparse_paged_split_gb300.wise` is its Python binding.  Importing the
+package does not load the library; the first call does, and raises if the
+library has not been built.
+"""
+from .wise import (MODE_DENSE, MODE_DISCOVER, MODE_DISCOVER_UNION, MODE_SPARSE, DTYPE_BF16,
+                   DTYPE_F32, WiseError, alloc_workspace, make_shape, mask_words,
+                   wise_compact_tiles, wise_decode, wise_decode_finish, wise_decode_partial,
+                   wise_support_union, wise_validate, wise_workspace_bytes,
+                   wise_workspace_layout, workspace_views)
+
+__all__ = ["MODE_DENSE", "MODE_DISCOVER", "MODE_DISCOVER_UNION", "MODE_SPARSE", "DTYPE_BF16",
+           "DTYPE_F32", "WiseError", "alloc_workspace", "make_shape", "mask_words",
+           "wise_compact_tiles", "wise_decode", "wise_decode_finish", "wise_decode_partial",
+           "wise_support_union", "wise_validate", "wise_workspace_bytes",
+           "wise_workspace_layout", "workspace_views"]

@@ -1,0 +1,192 @@
+// Device helpers shared by the WISE kernels: inline PTX for mbarriers and TMA
+// bulk-tensor copies (sm_90+ forms, compiled for sm_103a), bounded waits, and
+// warp-level reductions.  Nothing here depends on torch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wise.h"
+
+namespace wise {
+
+constexpr int kTile = 32;             // block / tile size B in tokens
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Wall-clock limit of every mbarrier wait (nanoseconds of %globaltimer); a
+// wait that runs out sets WISE_DEVERR_WAIT_TIMEOUT instead of hanging.
+constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;
+
+// Per-call constants every kernel needs.
+struct KParams {
+  int R, Hq, Hkv, G, D, P, max_pages, num_pages, max_blocks, W, T;
+  int cap_tokens;    // min(max_blocks * 32, max_pages * P)
+  float scale_log2;  // softmax scale * log2(e): scores are kept in log2 units
+  float eta;
+};
+
+// Device view of the caller's workspace (offsets from wise_workspace_layout).
+struct WsView {
+  int32_t* status;
+  int32_t* num_items;
+  int4* head_info;     // [R*Hkv]: first item, item count, tile count, 0
+  int32_t* tile_list;  // [R*Hkv, max_blocks]
+  int4* items;         // [max_items]: row, kv head, first tile, tile count
+  float2* partial_ml;  // [max_items, G]
+  float* partial_acc;  // [max_items, G, D]
+  float2* tile_stats;  // [R*Hq, max_blocks]
+  int32_t max_items;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ----------------------------------------------------------------------- TMA
+// 3-D tiled bulk-tensor load global -> shared, completing on an mbarrier.
+// Coordinates are innermost first: (element within the row, KV head, token).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------ math
+// 2^x via the SFU instruction (ex2.approx.ftz: ~2 ulp, 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void flag_error(int32_t* status, int bit) { atomicOr(status, bit); }
+
+// Element-type traits: how a lane loads its DPL = D/32 consecutive elements of
+// one K or V row from shared memory and widens them to float.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+  template <int DPL>
+  static __device__ __forceinline__ void load(const uint8_t* row, int lane, float (&x)[DPL]) {
+    if constexpr (DPL == 4) {
+      uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
+      x[0] = lo(w.x); x[1] = hi(w.x); x[2] = lo(w.y); x[3] = hi(w.y);
+    } else {
+      uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
+      x[0] = lo(w); x[1] = hi(w);
+    }
+  }
+  template <int DPL>
+  static __device__ __forceinline__ void load_global(const __nv_bfloat16* p, float (&x)[DPL]) {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) x[i] = __bfloat162float(p[i]);
+  }
+  template <int DPL>
+  static __device__ __forceinline__ void store_global(__nv_bfloat16* p, const float (&x)[DPL]) {
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2)
+      *reinterpret_cast<__nv_bfloat162*>(p + i) = __floats2bfloat162_rn(x[i], x[i + 1]);
+  }
+};
+
+template <>
+struct Elem<float> {
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  template <int DPL>
+  static __device__ __forceinline__ void load(const uint8_t* row, int lane, float (&x)[DPL]) {
+    if constexpr (DPL == 4) {
+      float4 v = *reinterpret_cast<const float4*>(row + lane * 16);
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+      float2 v = *reinterpret_cast<const float2*>(row + lane * 8);
+      x[0] = v.x; x[1] = v.y;
+    }
+  }
+  template <int DPL>
+  static __device__ __forceinline__ void load_global(const float* p, float (&x)[DPL]) {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) x[i] = p[i];
+  }
+  template <int DPL>
+  static __device__ __forceinline__ void store_global(float* p, const float (&x)[DPL]) {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) p[i] = x[i];
+  }
+};
+
+}  // namespace wise

@@ -1,0 +1,229 @@
+"""Python binding of libwise.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+include/wise.h for the operation, layouts and error behaviour), takes torch
+CUDA tensors, passes their device pointers and the current torch stream, and
+raises WiseError on a non-OK status.  There is no fallback: if the library is
+not built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Dict, Optional
+
+import torch
+
+from .build import LIBRARY
+
+MODE_DENSE = 0
+MODE_DISCOVER = 1
+MODE_DISCOVER_UNION = 2
+MODE_SPARSE = 3
+
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+DEVERR_SEQ_LEN_CLAMPED = 1
+DEVERR_WAIT_TIMEOUT = 2
+
+BAD_MODE = 1
+BAD_SEQ_LEN = 2
+BAD_PAGE = 4
+EMPTY_SPARSE_SUPPORT = 8
+
+_STATUS = {0: "WISE_OK", 1: "WISE_ERR_INVALID_ARG", 2: "WISE_ERR_UNSUPPORTED",
+           3: "WISE_ERR_WORKSPACE", 4: "WISE_ERR_CUDA"}
+
+
+class WiseError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class wise_shape(ctypes.Structure):
+    _fields_ = [("num_rows", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+                ("max_pages_per_row", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32), ("tiles_per_item", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eta", ctypes.c_float)]
+
+
+class wise_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status_word", "num_items", "head_info", "tile_list", "items", "partial_ml",
+        "partial_acc", "tile_stats", "max_items", "total_bytes")]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libwise.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(f"{LIBRARY} is not built; run "
+                               "`python -m block_sparse_paged_split_gb300.build`")
+        lib = ctypes.CDLL(LIBRARY)
+        P, S, I64, SZ = ctypes.c_void_p, ctypes.POINTER(wise_shape), ctypes.c_int64, ctypes.c_size_t
+        sigs = {
+            "wise_workspace_bytes": [S, ctypes.POINTER(ctypes.c_size_t)],
+            "wise_workspace_layout": [S, ctypes.POINTER(wise_layout)],
+            "wise_compact_tiles": [S, P, P, P, P, SZ, P],
+            "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
+            "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
+            "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "wise_support_union": [P, P, I64, P],
+            "wise_validate": [S, P, P, P, P, P, P],
+        }
+        for name, args in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.wise_status_string.argtypes = [ctypes.c_int]
+        lib.wise_status_string.restype = ctypes.c_char_p
+        lib.wise_last_error.argtypes = []
+        lib.wise_last_error.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise WiseError(status, library().wise_last_error().decode())
+
+
+def make_shape(*, num_rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+               page_size: int, max_pages_per_row: int, num_pages: int,
+               max_blocks: Optional[int] = None, dtype: int = DTYPE_BF16, eta: float = 0.95,
+               scale: float = 0.0, tiles_per_item: int = 0, tile_tokens: int = 32) -> wise_shape:
+    if max_blocks is None:
+        max_blocks = -(-max_pages_per_row * page_size // tile_tokens)
+    return wise_shape(num_rows, num_q_heads, num_kv_heads, head_dim, page_size, tile_tokens,
+                      max_pages_per_row, num_pages, max_blocks, tiles_per_item, dtype, scale, eta)
+
+
+def mask_words(shape: wise_shape) -> int:
+    return -(-shape.max_blocks // 32)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _elem(shape: wise_shape) -> torch.dtype:
+    return torch.bfloat16 if shape.dtype == DTYPE_BF16 else torch.float32
+
+
+def wise_workspace_bytes(shape: wise_shape) -> int:
+    n = ctypes.c_size_t()
+    _check(library().wise_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
+def wise_workspace_layout(shape: wise_shape) -> Dict[str, int]:
+    lay = wise_layout()
+    _check(library().wise_workspace_layout(ctypes.byref(shape), ctypes.byref(lay)))
+    return {name: getattr(lay, name) for name, _ in wise_layout._fields_}
+
+
+def alloc_workspace(shape: wise_shape, device=None) -> torch.Tensor:
+    """A workspace of the right size (torch allocations are 256-byte aligned)."""
+    return torch.empty(wise_workspace_bytes(shape), dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def wise_compact_tiles(shape, modes, seq_lens, support, workspace, stream=None) -> None:
+    _check(library().wise_compact_tiles(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(support, torch.int32, "support"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
+def wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                        stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_partial(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
+def wise_decode_finish(shape, modes, seq_lens, workspace, support, out, lse, stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_finish(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(support, torch.int32, "support"), _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"),
+        _stream(stream)))
+
+
+def wise_decode(shape, q, k_cache, v_cache, page_table, seq_lens, modes, support, out, lse,
+                workspace, stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(support, torch.int32, "support"),
+        _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def wise_support_union(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    if dst.numel() != src.numel():
+        raise ValueError("dst and src must have the same number of words")
+    _check(library().wise_support_union(_ptr(dst, torch.int32, "dst"), _ptr(src, torch.int32, "src"),
+                                        dst.numel(), _stream(stream)))
+
+
+def wise_validate(shape, page_table, seq_lens, modes, support, err_word, stream=None) -> None:
+    _check(library().wise_validate(
+        ctypes.byref(shape), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(modes, torch.int8, "modes"),
+        _ptr(support, torch.int32, "support"), _ptr(err_word, torch.int32, "err_word"),
+        _stream(stream)))
+
+
+def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, torch.Tensor]:
+    """Typed views of the workspace regions (for inspecting intermediates)."""
+    lay = wise_workspace_layout(shape)
+    R, Hq, Hkv, D = shape.num_rows, shape.num_q_heads, shape.num_kv_heads, shape.head_dim
+    G = Hq // Hkv
+    mi = lay["max_items"]
+
+    def region(off, count, dt):
+        nbytes = count * torch.tensor([], dtype=dt).element_size()
+        return workspace[off:off + nbytes].view(dt)
+
+    return {
+        "status": region(lay["status_word"], 1, torch.int32),
+        "num_items": region(lay["num_items"], 1, torch.int32),
+        "head_info": region(lay["head_info"], R * Hkv * 4, torch.int32).view(R, Hkv, 4),
+        "tile_list": region(lay["tile_list"], R * Hkv * shape.max_blocks, torch.int32).view(R, Hkv, shape.max_blocks),
+        "items": region(lay["items"], mi * 4, torch.int32).view(mi, 4),
+        "partial_ml": region(lay["partial_ml"], mi * G * 2, torch.float32).view(mi, G, 2),
+        "partial_acc": region(lay["partial_acc"], mi * G * D, torch.float32).view(mi, G, D),
+        "tile_stats": region(lay["tile_stats"], R * Hq * shape.max_blocks * 2, torch.float32).view(R, Hq, shape.max_blocks, 2),
+    }
+
+
+LOG2E = 1.0 / math.log(2.0)

@@ -1,0 +1,224 @@
+/*
+ * wise.h - C ABI of the WISE working-set paged decode attention library
+ * (libwise.so, CUDA kernels for sm_103a).
+ *
+ * The operation (vllm-rlt pull request "WISE working-set decode", PR #143,
+ * sections "Summary" and "What changes"): one decode call attends, for every
+ * row of a batch and every query head, over that row's paged K/V cache.  Each
+ * row runs in one of three modes:
+ *   dense     ordinary paged decode attention over all of the row's tokens;
+ *   discover  dense, and it also records every 32-token tile's max and
+ *             exp-sum; the finish step turns them into per-block softmax
+ *             masses and applies the eta selection (B = 32, eta = 0.95 by
+ *             default) into a [row, KV head, block] support bitmask;
+ *             DISCOVER overwrites the mask, DISCOVER_UNION ORs the new choice
+ *             into it (review comment "[P2] Distinguish discovery density
+ *             from reused union density");
+ *   sparse    attends only the row's selected tiles, compacted first so the
+ *             inner loop has no branch; the softmax is renormalised over the
+ *             selected tokens ("Tests": sparse output matches masked
+ *             attention).
+ * The split-KV structure (a partial pass over work items of about eight
+ * tiles, then a finish pass that merges the splits by log-sum-exp) follows
+ * the same section: one long dense row must not set the latency of a launch
+ * whose other rows are sparse.
+ *
+ * One call of the path, on one CUDA stream:
+ *     wise_compact_tiles -> wise_decode_partial -> wise_decode_finish
+ * (wise_decode runs all three).  wise_support_union ORs masks kept per depth.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller owns every buffer, including the workspace.  The library never
+ *     allocates device memory, never synchronises the stream and never
+ *     blocks; all work is enqueued on `stream` (NULL = legacy default stream).
+ *   - Arguments the host can check (null pointers, alignment, shape limits,
+ *     workspace size) are checked before anything is enqueued; on failure the
+ *     call returns a status and enqueues nothing.  A failed launch returns
+ *     WISE_ERR_CUDA.  wise_last_error() gives a one-line reason for the
+ *     calling thread's last non-OK status.
+ *   - Device data is never trusted to be in range and never traps: a page id
+ *     outside [0, num_pages) reads zeros, a seq_len above the row's capacity
+ *     is clamped to it and flagged in the workspace status word; use
+ *     wise_validate to check a batch explicitly.
+ *
+ * Layouts (row-major, no padding):
+ *   q, out       [num_rows, num_q_heads, head_dim], dtype of the shape
+ *   k_cache,
+ *   v_cache      [num_pages, page_size, num_kv_heads, head_dim] (paged, the
+ *                token-major layout of FlashAttention's paged KV cache)
+ *   page_table   int32 [num_rows, max_pages_per_row]; token j of row r lives
+ *                in page page_table[r][j / page_size], slot j % page_size
+ *   seq_lens     int32 [num_rows]; 0 marks a padding row
+ *   modes        int8  [num_rows], WISE_MODE_*
+ *   support      uint32 [num_rows, num_kv_heads, W], W = ceil(max_blocks/32);
+ *                block b of a (row, KV head) is bit (b % 32) of word b / 32.
+ *                Block b covers tokens [32 b, 32 b + 32) of the row.
+ *   lse          float32 [num_rows, num_q_heads]: natural log of the softmax
+ *                normaliser sum_j exp(scale * q . k_j) over attended tokens.
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).  For grouped
+ * query heads each query head selects blocks with its own eta rule and the
+ * KV head's mask is the OR over its group, so sparse rows attend the group's
+ * union.  Padding rows (seq_len 0) get out = 0 and lse = -inf and leave the
+ * mask untouched; a sparse row whose mask selects nothing gets the same.
+ */
+#ifndef WISE_H_
+#define WISE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *wise_stream_t;
+
+typedef enum {
+  WISE_OK = 0,
+  WISE_ERR_INVALID_ARG = 1, /* null pointer, misalignment, bad shape field */
+  WISE_ERR_UNSUPPORTED = 2, /* valid but not built (e.g. head_dim 96)      */
+  WISE_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small  */
+  WISE_ERR_CUDA = 4         /* a CUDA runtime call or launch failed        */
+} wise_status;
+
+enum {
+  WISE_MODE_DENSE = 0,
+  WISE_MODE_DISCOVER = 1,
+  WISE_MODE_DISCOVER_UNION = 2,
+  WISE_MODE_SPARSE = 3
+};
+
+enum { WISE_DTYPE_BF16 = 0, WISE_DTYPE_F32 = 1 };
+
+/* Bits of the workspace status word (set by the kernels, read by the caller
+ * from the workspace after the stream has run; see wise_workspace_layout). */
+enum {
+  WISE_DEVERR_SEQ_LEN_CLAMPED = 1, /* a seq_len exceeded the row's capacity */
+  WISE_DEVERR_WAIT_TIMEOUT = 2     /* a bounded wait gave up (no hang)      */
+};
+
+/* Bits of the word written by wise_validate. */
+enum {
+  WISE_BAD_MODE = 1,           /* mode outside 0..3                          */
+  WISE_BAD_SEQ_LEN = 2,        /* seq_len < 0 or above the row's capacity    */
+  WISE_BAD_PAGE = 4,           /* a page id the row uses is outside the pool */
+  WISE_EMPTY_SPARSE_SUPPORT = 8 /* a sparse (row, KV head) selects nothing   */
+};
+
+typedef struct {
+  int32_t num_rows;          /* R >= 0 (0: every call is a no-op)              */
+  int32_t num_q_heads;       /* Hq >= 1                                         */
+  int32_t num_kv_heads;      /* Hkv >= 1, Hq % Hkv == 0, Hq/Hkv in {1,2,4,8}    */
+  int32_t head_dim;          /* D in {64, 128}                                  */
+  int32_t page_size;         /* tokens per page: 8, 16 or 32                    */
+  int32_t tile_tokens;       /* block size B; must be 32                        */
+  int32_t max_pages_per_row; /* page_table row stride, >= 1                     */
+  int32_t num_pages;         /* pages in the K/V pools, >= 1                    */
+  int32_t max_blocks;        /* mask capacity per (row, KV head), 1..1024;
+                                a row's capacity is min(max_blocks * 32,
+                                max_pages_per_row * page_size) tokens          */
+  int32_t tiles_per_item;    /* tiles per split work item, 1..64; 0 means 8     */
+  int32_t dtype;             /* WISE_DTYPE_* of q, k_cache, v_cache and out     */
+  float scale;               /* softmax scale; 0 means 1/sqrt(head_dim)         */
+  float eta;                 /* selection threshold, > 0; >= 1 selects all      */
+} wise_shape;
+
+/* Offsets (bytes from the workspace base) of the workspace regions, for
+ * callers that inspect intermediate results.  All offsets are 256-aligned. */
+typedef struct {
+  size_t status_word;   /* int32: WISE_DEVERR_* bits, cleared by compaction   */
+  size_t num_items;     /* int32: work items written by compaction            */
+  size_t head_info;     /* int32x4 [R*Hkv]: first item, items, tiles, 0        */
+  size_t tile_list;     /* int32 [R*Hkv, max_blocks]: sparse rows' tiles, asc */
+  size_t items;         /* int32x4 [max_items]: row, KV head, first, tiles     */
+  size_t partial_ml;    /* float32x2 [max_items, G]: running max (log2 units)
+                           and exp-sum of each item and query head             */
+  size_t partial_acc;   /* float32 [max_items, G, D]: unnormalised outputs     */
+  size_t tile_stats;    /* float32x2 [R*Hq, max_blocks]: per tile max (log2
+                           units of the scaled score) and exp-sum (discover)  */
+  size_t max_items;     /* capacity of the item arrays                         */
+  size_t total_bytes;   /* = wise_workspace_bytes                              */
+} wise_layout;
+
+/* Bytes of device workspace one call sequence needs for this shape.  Host
+ * only; enqueues nothing.  `bytes` is a host pointer. */
+wise_status wise_workspace_bytes(const wise_shape *shape, size_t *bytes);
+
+/* Region offsets for this shape (host only). `layout` is a host pointer. */
+wise_status wise_workspace_layout(const wise_shape *shape,
+                                  wise_layout *layout);
+
+/* Compaction [WISE PR, "What changes": sparse rows are compacted first so
+ * the loop has no branch; programs cover about eight tiles].  For each
+ * (row, KV head): the tile list (ascending selected blocks below the row's
+ * block count for sparse rows; implicitly 0..n_b-1 for the other modes), cut
+ * in order into work items of at most tiles_per_item tiles.  Reads modes,
+ * seq_lens and (sparse rows only) support; writes the workspace (items, head
+ * info, tile lists) and clears its status word.  The workspace must be
+ * 256-byte aligned and at least wise_workspace_bytes long. */
+wise_status wise_compact_tiles(const wise_shape *shape, const int8_t *modes,
+                               const int32_t *seq_lens, const uint32_t *support,
+                               void *workspace, size_t workspace_bytes,
+                               wise_stream_t stream);
+
+/* Split partial pass [WISE PR, "What changes": split-KV paged decode with
+ * per-row modes].  For every work item written by wise_compact_tiles and
+ * every query head of its KV head: online softmax over the item's tiles,
+ * writing the unnormalised output, running max and exp-sum to the
+ * workspace; discover and discover-union rows also write each tile's max and
+ * exp-sum.  q, k_cache and v_cache must be 16-byte aligned. */
+wise_status wise_decode_partial(const wise_shape *shape, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const int32_t *page_table, const int32_t *seq_lens,
+                                const int8_t *modes, void *workspace,
+                                size_t workspace_bytes, wise_stream_t stream);
+
+/* Finish [WISE PR, "What changes": a finish kernel merges the splits and runs
+ * the selection for discovery rows].  Merges each (row, query head)'s splits
+ * by log-sum-exp into out and lse; for discover rows computes the block
+ * masses p_b = exp-sum_b * exp(max_b - lse), orders them by mass descending
+ * (ties: lower block index), keeps the shortest prefix whose cumulative mass
+ * reaches eta, ORs the selections of the KV head's query-head group and
+ * writes (DISCOVER) or ORs (DISCOVER_UNION) it into support, clearing bits at
+ * or past the row's block count.  Sparse and dense rows leave support alone.
+ * out must be 16-byte aligned; support may be NULL if no row discovers. */
+wise_status wise_decode_finish(const wise_shape *shape, const int8_t *modes,
+                               const int32_t *seq_lens, void *workspace,
+                               size_t workspace_bytes, uint32_t *support,
+                               void *out, float *lse, wise_stream_t stream);
+
+/* compact + partial + finish, in that order, on one stream. */
+wise_status wise_decode(const wise_shape *shape, const void *q,
+                        const void *k_cache, const void *v_cache,
+                        const int32_t *page_table, const int32_t *seq_lens,
+                        const int8_t *modes, uint32_t *support, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes,
+                        wise_stream_t stream);
+
+/* dst[i] |= src[i] for i < n_words [review "[P2] Distinguish discovery density
+ * from reused union density": the reused support is the union of the
+ * discovery depths' choices].  For callers that keep one mask per depth. */
+wise_status wise_support_union(uint32_t *dst, const uint32_t *src,
+                               int64_t n_words, wise_stream_t stream);
+
+/* Checks a batch's device data and ORs WISE_BAD_* / WISE_EMPTY_SPARSE_SUPPORT
+ * bits into *err_word (device int32; the caller zeroes it first).  support
+ * may be NULL when no row is sparse.  Never traps; reading only. */
+wise_status wise_validate(const wise_shape *shape, const int32_t *page_table,
+                          const int32_t *seq_lens, const int8_t *modes,
+                          const uint32_t *support, int32_t *err_word,
+                          wise_stream_t stream);
+
+/* Static name of a status code. */
+const char *wise_status_string(wise_status status);
+
+/* One-line reason for the calling thread's last non-OK status ("" if none). */
+const char *wise_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WISE_H_ */

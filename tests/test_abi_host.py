@@ -1,0 +1,113 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and its host-side checks reject bad arguments before
+anything is enqueued (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_paged_split_gb300 as W
+from block_sparse_paged_split_gb300 import wise
+from block_sparse_paged_split_gb300.build import INCLUDE, build_library
+
+HEADER = os.path.join(INCLUDE, "wise.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return wise.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:wise_status|const char \*)\s*(wise_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_path(lib):
+    names = declared_functions()
+    for required in ("wise_compact_tiles", "wise_decode_partial", "wise_decode_finish",
+                     "wise_support_union", "wise_workspace_bytes", "wise_validate", "wise_decode"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _shape(**kw):
+    base = dict(num_rows=4, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                max_pages_per_row=64, num_pages=256)
+    base.update(kw)
+    return W.make_shape(**base)
+
+
+def test_workspace_layout_is_aligned_and_sized(lib):
+    s = _shape()
+    lay = W.wise_workspace_layout(s)
+    assert lay["total_bytes"] == W.wise_workspace_bytes(s)
+    offs = [lay[k] for k in ("head_info", "tile_list", "items", "partial_ml", "partial_acc", "tile_stats")]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    # max items: every (row, KV head) split into ceil(max_blocks / 8) items
+    assert lay["max_items"] == 4 * 2 * -(-s.max_blocks // 8)
+    assert lay["partial_acc"] - lay["partial_ml"] >= lay["max_items"] * 4 * 8
+    # zero rows: header only
+    assert W.wise_workspace_bytes(_shape(num_rows=0)) == 256
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, 2), ("num_kv_heads", 3, 1), ("num_q_heads", 24, 2), ("page_size", 12, 2),
+    ("tile_tokens", 64, 2), ("max_blocks", 2048, 2), ("max_blocks", 0, 2), ("dtype", 7, 1),
+    ("eta", 0.0, 1), ("eta", float("nan"), 1), ("scale", -1.0, 1), ("num_rows", -1, 1),
+    ("num_pages", 0, 1), ("tiles_per_item", 65, 1)])
+def test_shape_checks(lib, field, value, status):
+    s = _shape()
+    setattr(s, field, value)
+    with pytest.raises(W.WiseError) as e:
+        W.wise_workspace_bytes(s)
+    assert e.value.status == status
+    assert lib.wise_last_error().decode()
+
+
+def test_host_checks_before_any_launch(lib):
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    P = ctypes.c_void_p
+    # NULL workspace
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, None, n, None)
+    assert st == 3
+    # misaligned workspace
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(4096 + 8), n, None)
+    assert st == 3
+    # workspace too small
+    st = lib.wise_decode_partial(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
+                                 P(4096), n - 1, None)
+    assert st == 3 and b"too small" in lib.wise_last_error()
+    # NULL required pointers
+    st = lib.wise_decode_partial(ctypes.byref(s), None, P(16), P(16), P(16), P(16), P(16),
+                                 P(4096), n, None)
+    assert st == 1
+    # misaligned q
+    st = lib.wise_decode_partial(ctypes.byref(s), P(18), P(16), P(16), P(16), P(16), P(16),
+                                 P(4096), n, None)
+    assert st == 1
+    st = lib.wise_decode_finish(ctypes.byref(s), P(16), P(16), P(4096), n, None, P(24), P(16), None)
+    assert st == 1  # out must be 16-byte aligned
+    st = lib.wise_support_union(None, P(16), 5, None)
+    assert st == 1
+    assert lib.wise_support_union(None, None, 0, None) == 0   # nothing to do
+    assert lib.wise_support_union(P(16), P(16), -1, None) == 1
+    st = lib.wise_validate(ctypes.byref(s), P(16), P(16), P(16), None, None, None)
+    assert st == 1
+    assert lib.wise_status_string(4) == b"WISE_ERR_CUDA"
+
+
+def test_zero_rows_is_a_no_op(lib):
+    s = _shape(num_rows=0)
+    n = W.wise_workspace_bytes(s)
+    P = ctypes.c_void_p
+    assert lib.wise_decode_partial(ctypes.byref(s), None, None, None, None, None, None,
+                                   P(4096), n, None) == 0
+    assert lib.wise_decode_finish(ctypes.byref(s), None, None, P(4096), n, None, None, None, None) == 0

@@ -1,0 +1,259 @@
+"""GPU parity against the CPU oracle at sizes the oracle finishes in seconds:
+several tiles per row, ragged tails, padding rows, NaN-filled pool pages and
+slots no row owns.  Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_paged_split_gb300 as W
+from block_sparse_paged_split_gb300.workload import custom_workload, make_workload
+from oracle import wise_oracle as O
+from tests.gpu_harness import (Batch, compare_masks, compare_outputs, dev_support, gpu_call,
+                               np_support, oracle_call, shape_for, words)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = np.array([1, 31, 32, 33, 300, 517, 0, 1024], np.int32)
+
+
+def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=3, n_planted=3):
+    R = len(lens)
+    return custom_workload("parity", R=R, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, depths=3,
+                           n_planted=n_planted, seq_lens=lens, pool_factor=2, seed=seed,
+                           depth_modes=[np.zeros(R, np.int8)] * 3)
+
+
+CASES = [(4, 4, 128, "bf16"), (4, 4, 64, "bf16"), (8, 2, 128, "bf16"), (4, 1, 64, "bf16"),
+         (2, 2, 64, "f32"), (4, 2, 128, "f32")]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
+def test_modes_match_oracle(Hq, Hkv, D, dtype):
+    w = _wl(Hq, Hkv, D, dtype)
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, Hkv, words(w)), np.uint32)
+    # dense
+    m = np.full(R, W.MODE_DENSE, np.int8)
+    g, o = gpu_call(b, 0, m, zero), oracle_call(b, 0, m, zero)
+    assert not compare_outputs(w, g, o)
+    assert np.array_equal(g["support"], zero)  # dense leaves the mask alone
+    # discover at depth 0 (overwrites a garbage mask), union-discover at depth 1
+    junk = np.random.default_rng(1).integers(0, 2**32, size=zero.shape, dtype=np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, junk), oracle_call(b, 0, m, junk)
+    assert not compare_outputs(w, g, o)
+    cm = compare_masks(w, g["support"], o, m)
+    assert not cm["fails"] and cm["checked"] >= cm["excluded"], cm
+    s0 = o["support"]
+    m = np.full(R, W.MODE_DISCOVER_UNION, np.int8)
+    g, o = gpu_call(b, 1, m, s0), oracle_call(b, 1, m, s0)
+    assert not compare_outputs(w, g, o)
+    cm = compare_masks(w, g["support"], o, m)
+    assert not cm["fails"], cm
+    # sparse on the oracle's union mask (the same mask on both sides)
+    s1 = o["support"]
+    m = np.full(R, W.MODE_SPARSE, np.int8)
+    g, o = gpu_call(b, 2, m, s1), oracle_call(b, 2, m, s1)
+    assert not compare_outputs(w, g, o)
+    assert np.array_equal(g["support"], s1)  # sparse leaves the mask alone
+
+
+def test_tile_stats_match_oracle():
+    """Discover rows' per-tile max and exp-sum (the workspace intermediates)."""
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, 4, words(w)), np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, zero), oracle_call(b, 0, m, zero)
+    ts = g["ws"]["tile_stats"].numpy()
+    for (r, h), dg in o["diag"].items():
+        nb = dg["m_b"].shape[0]
+        m_gpu = ts[r, h, :nb, 0] / W.wise.LOG2E
+        assert np.max(np.abs(m_gpu - dg["m_b"])) < 1e-4
+        assert np.max(np.abs(ts[r, h, :nb, 1] / dg["l_b"] - 1)) < 1e-4
+
+
+def test_tiny_schedule_f32():
+    """The 4-row fp32 D=64 workload: rows [dense, discover, sparse, sparse] over
+    two depths; sparse rows use a support from a prior discovery of the same
+    inputs (depth 0 discover, depth 1 union)."""
+    w = make_workload("tiny")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, w.num_kv_heads, words(w)), np.uint32)
+    d0 = np.full(R, W.MODE_DISCOVER, np.int8)
+    prior = oracle_call(b, 0, d0, zero)["support"]
+    prior = oracle_call(b, 1, np.full(R, W.MODE_DISCOVER_UNION, np.int8), prior)["support"]
+    sup = prior.copy()
+    sup[w.depth_modes[0] == W.MODE_DISCOVER] = 0
+    for depth in range(2):
+        m = w.depth_modes[depth]
+        g, o = gpu_call(b, depth, m, sup), oracle_call(b, depth, m, sup)
+        assert not compare_outputs(w, g, o)
+        assert not compare_masks(w, g["support"], o, m)["fails"]
+        sup = o["support"]
+
+
+def test_compaction_matches_oracle():
+    """Tile lists, per-head item counts and work items: bit-exact."""
+    rng = np.random.default_rng(5)
+    for T in (1, 3, 8):
+        lens = rng.integers(0, 700, size=9).astype(np.int32)
+        w = _wl(4, 2, 64, "bf16", lens=lens, seed=9)
+        R = w.num_rows
+        bits = rng.random((R, 2, words(w) * 32)) < 0.3
+        sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 2, -1).copy()
+        modes = rng.choice([0, 1, 2, 3], size=R).astype(np.int8)
+        shape = shape_for(w, tiles_per_item=T)
+        ws = W.alloc_workspace(shape)
+        W.wise_compact_tiles(shape, torch.from_numpy(modes).cuda(), torch.from_numpy(lens).cuda(),
+                             dev_support(sup), ws)
+        torch.cuda.synchronize()
+        v = {k: t.cpu().numpy() for k, t in W.workspace_views(shape, ws).items()}
+        ref = O.compact_tiles(sup, modes, lens, 32, T)
+        n = int(v["num_items"][0])
+        assert n == ref["items"].shape[0]
+        assert np.array_equal(v["items"][:n], ref["items"])
+        for r in range(R):
+            for g in range(2):
+                lst = ref["lists"][r][g]
+                assert v["head_info"][r, g, 2] == lst.shape[0]
+                assert v["head_info"][r, g, 1] == -(-lst.shape[0] // T)
+                if modes[r] == W.MODE_SPARSE:
+                    assert np.array_equal(v["tile_list"][r, g, :lst.shape[0]], lst)
+        assert int(v["status"][0]) == 0
+
+
+def test_all_selected_sparse_is_dense_bitwise():
+    """[WISE PR, Tests]: with every block selected, sparse is bitwise dense."""
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    full = np.full((R, 4, words(w)), 0xFFFFFFFF, np.uint32)
+    gd = gpu_call(b, 0, np.full(R, W.MODE_DENSE, np.int8), full)
+    gs = gpu_call(b, 0, np.full(R, W.MODE_SPARSE, np.int8), full)
+    gx = gpu_call(b, 0, np.full(R, W.MODE_DISCOVER, np.int8), full.copy())
+    assert torch.equal(gd["out_raw"], gs["out_raw"]) and np.array_equal(gd["lse"], gs["lse"])
+    assert torch.equal(gd["out_raw"], gx["out_raw"]) and np.array_equal(gd["lse"], gx["lse"])
+
+
+def test_mixed_launch_equals_uniform_launches_bitwise():
+    """One mixed-mode launch equals the uniform launches row for row, bitwise."""
+    w = _wl(8, 2, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    rng = np.random.default_rng(11)
+    bits = rng.random((R, 2, words(w) * 32)) < 0.4
+    sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 2, -1).copy()
+    mixed = np.array([0, 3, 1, 2, 3, 0, 1, 3], np.int8)
+    gm = gpu_call(b, 0, mixed, sup)
+    for mode in (0, 1, 2, 3):
+        gu = gpu_call(b, 0, np.full(R, mode, np.int8), sup)
+        rows = np.nonzero(mixed == mode)[0]
+        assert torch.equal(gm["out_raw"][rows], gu["out_raw"][rows])
+        assert np.array_equal(gm["lse"][rows], gu["lse"][rows])
+        assert np.array_equal(gm["support"][rows], gu["support"][rows])
+
+
+def test_split_size_invariance():
+    """Changing the work-item size only reorders fp32 sums."""
+    w = _wl(4, 4, 128, "f32")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, 4, words(w)), np.uint32)
+    m = np.full(R, W.MODE_DENSE, np.int8)
+    ref = gpu_call(b, 0, m, zero, tiles_per_item=8)
+    for T in (1, 3, 64):
+        g = gpu_call(b, 0, m, zero, tiles_per_item=T)
+        assert np.max(np.abs(g["out"] - ref["out"])) < 1e-5
+        fin = np.isfinite(ref["lse"])
+        assert np.max(np.abs(g["lse"][fin] - ref["lse"][fin])) < 1e-5
+
+
+def test_one_call_entry_point_matches_stepwise():
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, 4, words(w)), np.uint32)
+    m = np.array([1, 1, 3, 0, 2, 1, 3, 1], np.int8)
+    a = gpu_call(b, 0, m, zero, stepwise=True)
+    c = gpu_call(b, 0, m, zero, stepwise=False)
+    assert torch.equal(a["out_raw"], c["out_raw"]) and np.array_equal(a["support"], c["support"])
+
+
+def test_padding_rows_and_empty_sparse_support():
+    w = _wl(4, 4, 128, "bf16", lens=np.array([0, 64, 0, 100], np.int32))
+    b = Batch(w)
+    sup = np.zeros((4, 4, words(w)), np.uint32)
+    sup[0] = 0xFFFFFFFF  # padding row: mask must stay untouched even when discovering
+    sup[3, 1] = 0         # sparse row 3 head 1 selects nothing
+    sup[3, [0, 2, 3]] = 0b101
+    m = np.array([W.MODE_DISCOVER, W.MODE_SPARSE, W.MODE_DENSE, W.MODE_SPARSE], np.int8)
+    g, o = gpu_call(b, 0, m, sup), oracle_call(b, 0, m, sup)
+    assert not compare_outputs(w, g, o)
+    assert np.all(g["out"][[0, 2]] == 0) and np.all(np.isneginf(g["lse"][[0, 2]]))
+    assert np.all(g["out"][3, 1] == 0) and np.isneginf(g["lse"][3, 1])
+    assert np.array_equal(g["support"][0], sup[0])
+
+
+def test_support_union_kernel():
+    rng = np.random.default_rng(2)
+    for n in (1, 7, 4096 + 3):
+        a = rng.integers(0, 2**32, size=n, dtype=np.uint32)
+        c = rng.integers(0, 2**32, size=n, dtype=np.uint32)
+        da, dc = dev_support(a), dev_support(c)
+        W.wise_support_union(da, dc)
+        torch.cuda.synchronize()
+        assert np.array_equal(np_support(da), a | c)
+    # the union of two discovery depths equals union-discover mode
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, 4, words(w)), np.uint32)
+    s0 = gpu_call(b, 0, np.full(R, 1, np.int8), zero)["support"]
+    s1 = gpu_call(b, 1, np.full(R, 1, np.int8), zero)["support"]
+    su = gpu_call(b, 1, np.full(R, 2, np.int8), s0)["support"]
+    d0 = dev_support(s0)
+    W.wise_support_union(d0, dev_support(s1))
+    torch.cuda.synchronize()
+    assert np.array_equal(np_support(d0), su)
+
+
+def test_validate_reports_bad_batches():
+    w = _wl(4, 4, 64, "bf16", lens=np.array([64, 100, 40, 33], np.int32))
+    shape = shape_for(w)
+    pt = w.page_table.copy()
+    pt[1, 2] = w.num_pages + 5          # a page outside the pool
+    lens = w.seq_lens.copy()
+    lens[2] = 10**6                     # above the row capacity
+    modes = np.array([0, 0, 0, 3], np.int8)
+    sup = np.zeros((4, 4, words(w)), np.uint32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    W.wise_validate(shape, torch.from_numpy(pt).cuda(), torch.from_numpy(lens).cuda(),
+                    torch.from_numpy(modes).cuda(), dev_support(sup), err)
+    modes_bad = modes.copy()
+    modes_bad[0] = 9
+    W.wise_validate(shape, torch.from_numpy(w.page_table).cuda(), torch.from_numpy(w.seq_lens).cuda(),
+                    torch.from_numpy(modes_bad).cuda(), dev_support(sup), err)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & W.wise.BAD_PAGE and e & W.wise.BAD_SEQ_LEN and e & W.wise.EMPTY_SPARSE_SUPPORT
+    assert e & W.wise.BAD_MODE
+
+
+def test_seq_len_above_capacity_is_clamped_and_flagged():
+    w = _wl(4, 4, 64, "bf16", lens=np.array([64, 100, 40, 33], np.int32))
+    b = Batch(w)
+    shape = shape_for(w)
+    lens = w.seq_lens.copy()
+    cap = min(w.max_blocks * 32, w.max_pages_per_row * w.page_size)
+    lens[0] = cap + 1000
+    ws = W.alloc_workspace(shape)
+    modes = torch.zeros(4, dtype=torch.int8, device="cuda")
+    W.wise_compact_tiles(shape, modes, torch.from_numpy(lens).cuda(), None, ws)
+    torch.cuda.synchronize()
+    v = W.workspace_views(shape, ws)
+    assert int(v["status"].item()) & W.wise.DEVERR_SEQ_LEN_CLAMPED
+    assert int(v["head_info"][0, 0, 2].item()) == -(-cap // 32)
