@@ -127,7 +127,8 @@ def compare_outputs(w, g, o, rows=None) -> list:
         r, h, _ = np.unravel_index(np.argmax(err), err.shape)
         fails.append(f"out max err {err.max():.3g} > {tol} at row {r} head {h}")
     both_inf = np.isneginf(gl) & np.isneginf(o["lse"])
-    lerr = np.where(both_inf, 0.0, np.abs(gl - o["lse"]))
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(gl - o["lse"]))
     if not np.all(np.isfinite(lerr)) or lerr.max() > LSE_TOL:
         fails.append(f"lse max err {np.nanmax(lerr):.3g} > {LSE_TOL}")
     return fails
