@@ -110,8 +110,15 @@ def oracle_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
     if rows is not None:
         rows = np.asarray(rows)
         q, pt, sl, md, sup = q[rows], pt[rows], sl[rows], md[rows], sup[rows]
-    return O.decode_layer(q, as_oracle_array(c["k_cache"]), as_oracle_array(c["v_cache"]), pt, sl,
-                          md, sup, eta=w.eta if eta is None else eta, tile_tokens=w.tile_tokens)
+    e = w.eta if eta is None else eta
+    res = O.decode_layer(q, as_oracle_array(c["k_cache"]), as_oracle_array(c["v_cache"]), pt, sl,
+                         md, sup, eta=e, tile_tokens=w.tile_tokens)
+    res["eta"] = e
+    return res
+
+
+def o_eta(o, w) -> float:
+    return float(o.get("eta", w.eta))
 
 
 def compare_outputs(w, g, o, rows=None) -> list:
@@ -132,6 +139,29 @@ def compare_outputs(w, g, o, rows=None) -> list:
     if not np.all(np.isfinite(lerr)) or lerr.max() > LSE_TOL:
         fails.append(f"lse max err {np.nanmax(lerr):.3g} > {LSE_TOL}")
     return fails
+
+
+def mask_bounds(dg: dict, eta: float, nb: int):
+    """Blocks any valid fp32 evaluation must keep, and blocks it may keep, for
+    one query head whose decision is near a tie: a block is certain when the
+    mass before it is below eta - MARGIN and it outweighs the first dropped
+    block by more than GAP; it is possible when the mass before it is below
+    eta + MARGIN or it is within GAP of the last kept block."""
+    if eta >= 1.0:
+        allb = np.ones(nb, bool)
+        return allb, allb
+    p32 = dg["p"].astype(np.float32).astype(np.float64)
+    order = dg["order"]
+    ps = p32[order]
+    before = np.cumsum(ps) - ps
+    k = dg["k"]
+    p_next = ps[k] if k < nb else -np.inf
+    p_last = ps[k - 1]
+    must = np.zeros(nb, bool)
+    may = np.zeros(nb, bool)
+    must[order] = (before < eta - MARGIN) & (ps > p_next + GAP)
+    may[order] = (before < eta + MARGIN) | (ps >= p_last - GAP)
+    return must, may
 
 
 def compare_masks(w, g_support, o, modes, rows=None) -> Dict[str, object]:
@@ -159,8 +189,14 @@ def compare_masks(w, g_support, o, modes, rows=None) -> Dict[str, object]:
                     fails.append(f"mask differs row {r} kv head {g}")
             else:
                 excluded += 1
-                if gb.sum() == 0:
-                    fails.append(f"empty ambiguous mask row {r} kv head {g}")
+                must = np.zeros(nb, bool)
+                may = np.zeros(nb, bool)
+                for dg in diags:
+                    a, c = mask_bounds(dg, o_eta(o, w), nb)
+                    must |= a
+                    may |= c
+                if np.any(must & ~gb) or np.any(gb & ~may):
+                    fails.append(f"ambiguous mask outside its bounds row {r} kv head {g}")
             # never any bit at or past the block count
             if np.any(np.unpackbits(sup_g[r, g].view(np.uint8), bitorder="little")[nb:32 * sup_g.shape[2]]):
                 fails.append(f"bits past the row end row {r} kv head {g}")
