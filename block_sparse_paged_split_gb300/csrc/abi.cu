@@ -192,6 +192,14 @@ wise_status tensor_map(const wise_shape* s, const void* base, CUtensorMap* out) 
 
 }  // namespace
 
+wise_status record_error(wise_status status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
 // ---------------------------------------------------------------- devices
 int sm_count() {
   static std::mutex mu;

@@ -31,4 +31,7 @@ cudaError_t launch_validate(const KParams& kp, const int32_t* page_table,
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// Records a printf-style reason for wise_last_error() and returns `status`.
+wise_status record_error(wise_status status, const char* fmt, ...);
+
 }  // namespace wise

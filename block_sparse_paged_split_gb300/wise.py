@@ -77,6 +77,7 @@ def library() -> ctypes.CDLL:
             "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
             "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "wise_decode_noalloc": [S, P, P, P, P, P, P, P, P, P, P],
             "wise_support_union": [P, P, I64, P],
             "wise_validate": [S, P, P, P, P, P, P],
         }
@@ -186,6 +187,19 @@ def wise_decode(shape, q, k_cache, v_cache, page_table, seq_lens, modes, support
         _ptr(modes, torch.int8, "modes"), _ptr(support, torch.int32, "support"),
         _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def wise_decode_noalloc(shape, q, k_cache, v_cache, page_table, seq_lens, modes, support, out,
+                        lse, stream=None) -> None:
+    """wise_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library's static 16 MiB device scratch is
+    used instead (see include/wise.h for its limits and sharing rules)."""
+    e = _elem(shape)
+    _check(library().wise_decode_noalloc(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(support, torch.int32, "support"),
+        _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
 
 
 def wise_support_union(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:

@@ -211,6 +211,25 @@ wise_status wise_validate(const wise_shape *shape, const int32_t *page_table,
                           const uint32_t *support, int32_t *err_word,
                           wise_stream_t stream);
 
+/* The same call as wise_decode, for callers that cannot allocate device
+ * memory (no counterpart in the paper; it exists for integration only).
+ * Instead of a caller-provided workspace it uses a 16 MiB scratch array that
+ * lives in the library's static device memory, held by every GPU that loads
+ * the library until the process exits.  A shape whose workspace
+ * (wise_workspace_bytes) exceeds 16 MiB is rejected with WISE_ERR_WORKSPACE
+ * and nothing is enqueued.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current),
+ * which may load device code: make that first call before any stream
+ * capture.  No call allocates or frees device memory.  All calls on a device
+ * share the one array and it keeps the last call's contents (nothing in it
+ * needs to start at zero); calls whose GPU work overlaps (different streams
+ * without ordering) race on it. */
+wise_status wise_decode_noalloc(const wise_shape *shape, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const int32_t *page_table, const int32_t *seq_lens,
+                                const int8_t *modes, uint32_t *support, void *out,
+                                float *lse, wise_stream_t stream);
+
 /* Static name of a status code. */
 const char *wise_status_string(wise_status status);
 
