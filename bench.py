@@ -44,12 +44,14 @@ UNIT = "rows/s"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--rows", type=int, default=None,
                    help="fewer rows of the same workload (small profiling case)")
+    p.add_argument("--tiles-per-item", type=int, default=0,
+                   help="split work-item size (0: the library default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
@@ -163,7 +165,7 @@ class ClockSampler:
 class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
-    def __init__(self, w, rank_seed_offset: int = 0):
+    def __init__(self, w, tiles_per_item: int = 0):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -178,7 +180,7 @@ class Pipeline:
                                   page_size=w.page_size, max_pages_per_row=w.max_pages_per_row,
                                   num_pages=w.num_pages, max_blocks=w.max_blocks,
                                   dtype=W.DTYPE_BF16 if w.dtype == "bf16" else W.DTYPE_F32,
-                                  eta=w.eta)
+                                  eta=w.eta, tiles_per_item=tiles_per_item)
         dev = torch.device("cuda")
         self.host = [w.depth_inputs(t) for t in range(w.num_depths)]
         self.depth = [{k: v.to(dev) for k, v in d.items()} for d in self.host]
@@ -204,7 +206,7 @@ class Pipeline:
             m = modes_t.data_ptr()
             c = []
             if compact:
-                c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, ws, nws, st)))
+                c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, pt, ws, nws, st)))
             c.append(("partial", lib.wise_decode_partial,
                       (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                        pt, sl, m, ws, nws, st)))
@@ -220,6 +222,28 @@ class Pipeline:
             reuse = t > 0 and mode == W.MODE_SPARSE and int(w.depth_modes[t - 1][0]) == W.MODE_SPARSE
             self.wise_step.append((t, mode_name[mode], calls(self.modes[t], t, compact=not reuse)))
         self.dense_step = [(t, "dense", calls(self.dense_modes, t)) for t in range(w.num_depths)]
+
+    def graph(self, step):
+        """The step captured once as a CUDA graph (its launches bound to the
+        capture stream)."""
+        torch = self.torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        rebound = []
+        for t, mode, calls in step:
+            rb = []
+            for kind, fn, args in calls:
+                rb.append((kind, fn, tuple(side.cuda_stream if i == len(args) - 1 else a
+                                           for i, a in enumerate(args))))
+            rebound.append((t, mode, rb))
+        with torch.cuda.stream(side):
+            self.run(rebound)  # one eager pass on the side stream before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            self.run(rebound)
+        torch.cuda.synchronize()
+        return g
 
     def run(self, step, events=None):
         for t, mode, calls in step:
@@ -278,6 +302,22 @@ def timed_region(pipe, step, K, dist, with_events=True):
     if dist:
         dist.barrier()
     return start.elapsed_time(end), events
+
+
+def graph_region(pipe, graph, K, dist):
+    import torch
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(K):
+        graph.replay()
+    e.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    return s.elapsed_time(e)
 
 
 def e2e_region(pipe, K):
@@ -352,7 +392,7 @@ def main_ours(args):
     # Weak scaling: every rank decodes its own batch (rows are independent).
     w = make_workload(args.workload, num_rows=args.rows,
                       seed=None if rank == 0 else 100000 + rank)
-    pipe = Pipeline(w)
+    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -368,18 +408,31 @@ def main_ours(args):
         kv[(t, mode)] = pipe.kv_bytes("dense", t) + pipe.small_bytes()
     density = kv[(2, "sparse")] / kv[(2, "dense")] if (2, "sparse") in kv else None
 
+    # The step and the dense baseline step, each captured once as a CUDA graph.
+    graph = pipe.graph(pipe.wise_step)
+    graph_dense = pipe.graph(pipe.dense_step)
+    for _ in range(3):
+        graph.replay()
+        graph_dense.replay()
+    torch.cuda.synchronize()
+
     clock = ClockSampler(local)
     wall0 = time.time()
-    ms, events = timed_region(pipe, pipe.wise_step, args.steps, dist)
+    # Headline: K steps replayed from the graph, CUDA events around them.
+    ms = graph_region(pipe, graph, args.steps, dist)
+    ms_dense_graph = graph_region(pipe, graph_dense, args.steps, dist)
+    # Per-launch view: the same K steps launched eagerly with CUDA events
+    # around every launch (per-mode times and the roofline of the partial pass).
+    ms_eager, events = timed_region(pipe, pipe.wise_step, args.steps, dist)
     ms_dense, events_dense = timed_region(pipe, pipe.dense_step, args.steps, dist)
     clocks = clock.stop()
     wall = time.time() - wall0
 
     # Max over ranks.
-    t = torch.tensor([ms, ms_dense], dtype=torch.float64, device="cuda")
+    t = torch.tensor([ms, ms_dense_graph, ms_eager, ms_dense], dtype=torch.float64, device="cuda")
     if dist:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, ms_dense = float(t[0]), float(t[1])
+    ms, ms_dense_graph, ms_eager, ms_dense = (float(x) for x in t)
 
     def summarize(evts):
         per = {}
@@ -395,8 +448,10 @@ def main_ours(args):
     part_bytes = sum(kv[(tt, m)] for (tt, m, k) in per if k == "partial")
     part_ms = sum(v for (tt, m, k), v in per.items() if k == "partial")
     achieved = part_bytes / (part_ms * 1e-3) / 1e9
-    launches = pipe.launches_per_step(pipe.wise_step) * args.steps + \
-        pipe.launches_per_step(pipe.dense_step) * args.steps
+    # Kernels launched in the timed regions: the graph replays and the eager
+    # passes, each over K WISE steps and K dense steps.
+    launches = 2 * (pipe.launches_per_step(pipe.wise_step) +
+                    pipe.launches_per_step(pipe.dense_step)) * args.steps
 
     R = w.num_rows
     modes = {}
@@ -416,7 +471,9 @@ def main_ours(args):
                       "rows_per_s": round(R / (dense_call * 1e-3), 1),
                       "partial_gbs": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9, 1),
                       "partial_frac_of_measured_hbm": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9 / peak, 3),
-                      "step_ms": round(ms_dense / args.steps, 4)}
+                      "step_ms_eager": round(ms_dense / args.steps, 4),
+                      "step_ms_graph": round(ms_dense_graph / args.steps, 4)}
+
 
     e2e_ms, h2d, d2h = e2e_region(pipe, args.steps)
     rows_per_step = R * w.num_depths
@@ -433,7 +490,9 @@ def main_ours(args):
                                f"page {w.page_size}, B=32, eta={w.eta}, 4 depths",
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": "inputs larger than L2: 2.1 GB of K/V per step (129 MB L2)",
-                   "timing": "eager launches, CUDA events on the launching stream around every launch",
+                   "timing": "value: CUDA-graph replay of the step, CUDA events around the K "
+                             "replays; modes and roofline: eager launches with CUDA events "
+                             "around every launch on the launching stream",
                    "union_density": round(density, 4) if density else None},
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -442,12 +501,16 @@ def main_ours(args):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "eager": {"ms_per_step": round(ms_eager / args.steps, 4),
+                  "rows_per_s": round(world * rows_per_step * args.steps / (ms_eager * 1e-3), 1),
+                  "note": "every launch bracketed by CUDA events"},
+        "speedup_vs_dense": round(ms_dense_graph / ms, 3),
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed": round(wall, 2),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=8, reps=2)
+        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, reps=36)
     if rank == 0:
         print(json.dumps(result))
     if dist:

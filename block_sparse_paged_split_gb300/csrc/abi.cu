@@ -45,8 +45,8 @@ wise_status check_shape(const wise_shape* s) {
     return fail(WISE_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
   if (s->head_dim != 64 && s->head_dim != 128)
     return fail(WISE_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", s->head_dim);
-  if (s->page_size != 8 && s->page_size != 16 && s->page_size != 32)
-    return fail(WISE_ERR_UNSUPPORTED, "page_size must be 8, 16 or 32 (got %d)", s->page_size);
+  if (s->page_size != 16 && s->page_size != 32)
+    return fail(WISE_ERR_UNSUPPORTED, "page_size must be 16 or 32 (got %d)", s->page_size);
   if (s->tile_tokens != kTile)
     return fail(WISE_ERR_UNSUPPORTED, "tile_tokens must be 32 (got %d)", s->tile_tokens);
   if (s->max_pages_per_row < 1 || s->num_pages < 1)
@@ -55,8 +55,9 @@ wise_status check_shape(const wise_shape* s) {
     return fail(WISE_ERR_UNSUPPORTED, "num_pages * page_size too large");
   if (s->max_blocks < 1 || s->max_blocks > 1024)
     return fail(WISE_ERR_UNSUPPORTED, "max_blocks must be in [1, 1024] (got %d)", s->max_blocks);
-  if (s->tiles_per_item < 0 || s->tiles_per_item > 64)
-    return fail(WISE_ERR_INVALID_ARG, "tiles_per_item must be in [0, 64]");
+  if (s->tiles_per_item < 0 || s->tiles_per_item > 16 ||
+      (s->tiles_per_item & (s->tiles_per_item - 1)) != 0)
+    return fail(WISE_ERR_INVALID_ARG, "tiles_per_item must be 0, 1, 2, 4, 8 or 16");
   if (s->dtype != WISE_DTYPE_BF16 && s->dtype != WISE_DTYPE_F32)
     return fail(WISE_ERR_INVALID_ARG, "unknown dtype %d", s->dtype);
   if (!std::isfinite(s->scale) || s->scale < 0.f)
@@ -82,6 +83,7 @@ KParams make_params(const wise_shape* s) {
   kp.max_blocks = s->max_blocks;
   kp.W = (s->max_blocks + 31) / 32;
   kp.T = s->tiles_per_item ? s->tiles_per_item : 8;
+  kp.S_max = (s->max_blocks + kp.T - 1) / kp.T;
   const int64_t cap_a = (int64_t)s->max_blocks * kTile;
   const int64_t cap_b = (int64_t)s->max_pages_per_row * s->page_size;
   kp.cap_tokens = (int)(cap_a < cap_b ? cap_a : cap_b);
@@ -98,9 +100,10 @@ void compute_layout(const wise_shape* s, wise_layout* l) {
   size_t off = 0;
   l->status_word = 0;
   l->num_items = 4;
+  l->queue = 8;
   off = 256;
   l->head_info = off;   off = up256(off + pairs * sizeof(int4));
-  l->tile_list = off;   off = up256(off + pairs * kp.max_blocks * sizeof(int32_t));
+  l->tile_list = off;   off = up256(off + pairs * kp.max_blocks * sizeof(int4));
   l->items = off;       off = up256(off + max_items * sizeof(int4));
   l->partial_ml = off;  off = up256(off + max_items * kp.G * sizeof(float2));
   l->partial_acc = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
@@ -119,8 +122,10 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v)
   uint8_t* b = static_cast<uint8_t*>(ws);
   v->status = reinterpret_cast<int32_t*>(b + l.status_word);
   v->num_items = reinterpret_cast<int32_t*>(b + l.num_items);
+  v->queue = reinterpret_cast<int32_t*>(b + l.queue);
+  v->queue_done = reinterpret_cast<int32_t*>(b + l.queue + 4);
   v->head_info = reinterpret_cast<int4*>(b + l.head_info);
-  v->tile_list = reinterpret_cast<int32_t*>(b + l.tile_list);
+  v->tile_list = reinterpret_cast<int4*>(b + l.tile_list);
   v->items = reinterpret_cast<int4*>(b + l.items);
   v->partial_ml = reinterpret_cast<float2*>(b + l.partial_ml);
   v->partial_acc = reinterpret_cast<float*>(b + l.partial_acc);
@@ -254,15 +259,16 @@ wise_status wise_workspace_layout(const wise_shape* shape, wise_layout* layout) 
 
 wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
                                const int32_t* seq_lens, const uint32_t* support,
-                               void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+                               const int32_t* page_table, void* workspace,
+                               size_t workspace_bytes, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
-  if (shape->num_rows > 0 && (!modes || !seq_lens))
-    return fail(WISE_ERR_INVALID_ARG, "modes and seq_lens must not be NULL");
+  if (shape->num_rows > 0 && (!modes || !seq_lens || !page_table))
+    return fail(WISE_ERR_INVALID_ARG, "modes, seq_lens and page_table must not be NULL");
   if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
-  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, support, ws,
+  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, support, page_table, ws,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "compact launch");
 }
@@ -312,7 +318,7 @@ wise_status wise_decode(const wise_shape* shape, const void* q, const void* k_ca
                         const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
                         const int8_t* modes, uint32_t* support, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, wise_stream_t stream) {
-  wise_status st = wise_compact_tiles(shape, modes, seq_lens, support, workspace,
+  wise_status st = wise_compact_tiles(shape, modes, seq_lens, support, page_table, workspace,
                                       workspace_bytes, stream);
   if (st != WISE_OK) return st;
   st = wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,

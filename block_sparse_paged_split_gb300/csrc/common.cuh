@@ -24,6 +24,7 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;
 // Per-call constants every kernel needs.
 struct KParams {
   int R, Hq, Hkv, G, D, P, max_pages, num_pages, max_blocks, W, T;
+  int S_max;         // splits per (row, KV head) at most: ceil(max_blocks / T)
   int cap_tokens;    // min(max_blocks * 32, max_pages * P)
   float scale_log2;  // softmax scale * log2(e): scores are kept in log2 units
   float eta;
@@ -33,16 +34,24 @@ struct KParams {
 struct WsView {
   int32_t* status;
   int32_t* num_items;
+  int32_t* queue;      // next schedule slot; zeroed by compaction and again by
+                       // the last CTA of every partial launch
+  int32_t* queue_done; // CTAs of the running partial launch past the queue
   int4* head_info;     // [R*Hkv]: first item, item count, tile count, 0
-  int32_t* tile_list;  // [R*Hkv, max_blocks]
-  int4* items;         // [max_items]: row, kv head, first tile, tile count
-  float2* partial_ml;  // [max_items, G]
+  int4* tile_list;     // [R*Hkv, max_blocks]: block, first page, second page (or 0), 0
+  int4* items;         // [max_items] in schedule order: rg, first, tiles | flags, L
+  float2* partial_ml;  // [max_items, G], split s of rg in slot rg * S_max + s
   float* partial_acc;  // [max_items, G, D]
   float2* tile_stats;  // [R*Hq, max_blocks]
   int32_t max_items;
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
+
+// Work item record, third field: tile count (bits 0-7), block range index
+// (bits 8-23) and mode flags (bits 24, 25).
+constexpr int kItemSparse = 1 << 24;
+constexpr int kItemDiscover = 1 << 25;
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -130,6 +139,19 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ void flag_error(int32_t* status, int bit) { atomicOr(status, bit); }
+
+// Programmatic dependent launch: wait until the previous kernel in the stream
+// has completed and its writes are visible (a no-op when the kernel was not
+// launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream start launching (its CTAs then wait in
+// grid_dependency_wait until this grid has completed).
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Element-type traits: how a lane loads its DPL = D/32 consecutive elements of
 // one K or V row from shared memory and widens them to float.

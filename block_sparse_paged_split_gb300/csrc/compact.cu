@@ -43,71 +43,160 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
   return base + incl - v;
 }
 
+// Work items are block ranges: item (rg, s) holds the tiles of (row, KV head)
+// rg that lie in blocks [s*T, s*T + T) -- all of them for dense and discover
+// rows, the selected ones for sparse rows (skipped when none is).  A row's
+// split therefore depends only on its own length, mode and mask, and a
+// sparse row with every block selected splits exactly like a dense row.
+// Item (rg, s) writes its partial output to slot rg * S_max + s.
+//
+// Compaction writes the items already in schedule order, which is the order
+// the partial pass hands them out (through an atomic counter): tile count
+// descending, so the last warps do not finish long items alone.  Each record
+// is self-contained: x = rg, y = first index in the tile list (sparse) or
+// first block (otherwise), z = tiles | flags | s << 8, w = row length.
+//
+// Phase A, a thread per (row, KV head): item and tile counts and a
+// histogram of item sizes (warp-aggregated shared-memory atomics).
+// Phase B, the same thread: its item records at their schedule slots,
+// empty-range markers for sparse rows, and its tile list.
+__device__ __forceinline__ int range_count(bool sparse, const uint32_t* words, int s, int T,
+                                           int nb) {
+  const int lo = s * T;
+  if (lo >= nb) return 0;
+  const int n = min(T, nb - lo);
+  if (!sparse) return n;
+  if (!words) return 0;
+  // T is at most 16 and a power of two here, so a range never straddles words.
+  const uint32_t w = words[lo >> 5] >> (lo & 31);
+  return __popc(w & ((1u << n) - 1u));
+}
+
 __global__ void __launch_bounds__(kCompactThreads)
     compact_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                   const uint32_t* __restrict__ support, const WsView ws, const KParams kp) {
+                   const uint32_t* __restrict__ support, const int32_t* __restrict__ page_table,
+                   const WsView ws, const KParams kp) {
+  grid_dependency_wait();
+  grid_dependents_launch();  // the partial pass may start its prologue now
   __shared__ int warp_tot[32];
-  if (threadIdx.x == 0) *ws.status = 0;
+  __shared__ int size_slot[17];  // items per size (1..T), then the next schedule slot
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    *ws.status = 0;
+    *ws.queue = 0;
+    *ws.queue_done = 0;
+  }
+  for (int i = threadIdx.x; i <= 16; i += blockDim.x) size_slot[i] = 0;
   __syncthreads();
   const int npair = kp.R * kp.Hkv;
-  int carry = 0;
+  const int T = kp.T;
+  const int S = kp.S_max;
+
+  // Phase A: counts and the size histogram.
+  int carry_items = 0;
   for (int base = 0; base < npair; base += kCompactThreads) {
     const int idx = base + threadIdx.x;
-    int count = 0, nitems = 0, r = 0, g = 0, nb = 0;
+    const bool valid = idx < npair;
+    int nb = 0, nitems = 0, count = 0;
     bool sparse = false;
-    if (idx < npair) {
-      r = idx / kp.Hkv;
-      g = idx - r * kp.Hkv;
+    const uint32_t* words = nullptr;
+    if (valid) {
+      const int r = idx / kp.Hkv;
       const int raw = seq_lens[r];
       const int L = clamp_len(raw, kp.cap_tokens);
-      if (raw > kp.cap_tokens && g == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
+      if (raw > kp.cap_tokens && idx % kp.Hkv == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
       nb = (L + kTile - 1) / kTile;
       sparse = modes[r] == WISE_MODE_SPARSE;
-      if (sparse) {
-        if (support != nullptr) {
-          const uint32_t* words = support + (size_t)idx * kp.W;
-          for (int w = 0; w * 32 < nb; ++w) {
-            const int lo = w * 32;
-            const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u;
-            count += __popc(words[w] & valid);
-          }
-        }
-      } else {
-        count = nb;
-      }
-      nitems = (count + kp.T - 1) / kp.T;
+      words = (sparse && support) ? support + (size_t)idx * kp.W : nullptr;
     }
-    int total = 0;
-    const int first = carry + block_exclusive_scan(nitems, warp_tot, &total);
-    if (idx < npair) {
-      ws.head_info[idx] = make_int4(first, nitems, count, 0);
-      for (int s = 0; s < nitems; ++s) {
-        const int t0 = s * kp.T;
-        ws.items[first + s] = make_int4(r, g, t0, min(kp.T, count - t0));
-      }
-      if (sparse && count > 0) {
-        const uint32_t* words = support + (size_t)idx * kp.W;
-        int32_t* list = ws.tile_list + (size_t)idx * kp.max_blocks;
-        int k = 0;
-        for (int w = 0; w * 32 < nb; ++w) {
-          const int lo = w * 32;
-          uint32_t bits = words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u);
-          while (bits) {
-            list[k++] = lo + __ffs(bits) - 1;
-            bits &= bits - 1;
-          }
-        }
-      }
+    for (int s = 0; s < S; ++s) {
+      const int n = valid ? range_count(sparse, words, s, T, nb) : 0;
+      count += n;
+      nitems += n > 0;
+      const unsigned same = __match_any_sync(kFull, n);
+      if (n > 0 && lane == __ffs(same) - 1) atomicAdd(&size_slot[n], __popc(same));
     }
-    carry += total;
+    if (valid) ws.head_info[idx] = make_int4(idx * S, (nb + T - 1) / T, count, nitems);
+    int tot = 0;
+    block_exclusive_scan(nitems, warp_tot, &tot);
+    carry_items += tot;
   }
-  if (threadIdx.x == 0) *ws.num_items = carry;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *ws.num_items = carry_items;
+    int run = 0;
+    for (int sz = T; sz >= 1; --sz) {
+      const int n = size_slot[sz];
+      size_slot[sz] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+
+  // Phase B: item records at their schedule slots, empty-range markers,
+  // tile lists.
+  for (int base = 0; base < npair; base += kCompactThreads) {
+    const int idx = base + threadIdx.x;
+    const bool valid = idx < npair;
+    int r = 0, nb = 0, L = 0, flags = 0;
+    bool sparse = false;
+    const uint32_t* words = nullptr;
+    if (valid) {
+      r = idx / kp.Hkv;
+      L = clamp_len(seq_lens[r], kp.cap_tokens);
+      nb = (L + kTile - 1) / kTile;
+      const int mode = modes[r];
+      sparse = mode == WISE_MODE_SPARSE;
+      words = (sparse && support) ? support + (size_t)idx * kp.W : nullptr;
+      flags = (sparse ? kItemSparse : 0) |
+              (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION ? kItemDiscover : 0);
+    }
+    int first = 0;  // index into this pair's tile list (sparse rows)
+    for (int s = 0; s < S; ++s) {
+      const int n = valid ? range_count(sparse, words, s, T, nb) : 0;
+      const unsigned same = __match_any_sync(kFull, n);
+      const int leader = __ffs(same) - 1;
+      int slot = 0;
+      if (n > 0 && lane == leader) slot = atomicAdd(&size_slot[n], __popc(same));
+      slot = __shfl_sync(kFull, slot, leader);
+      if (n > 0) {
+        ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
+            make_int4(idx, sparse ? first : s * T, n | flags | (s << 8), L);
+      } else if (sparse && s * T < nb) {
+        // An empty range of a sparse row: mark its partial slot so the
+        // finish pass skips it.
+        for (int h = 0; h < kp.G; ++h)
+          ws.partial_ml[((size_t)idx * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
+      }
+      first += n;
+    }
+    if (sparse && words) {
+      // Each selected tile with its page ids, so the partial pass needs one
+      // load per tile (pages past the row's length are never read: 0).
+      const int32_t* pt = page_table + (size_t)r * kp.max_pages;
+      const int ppt = kTile / kp.P;  // pages per tile: 2 or 1
+      int4* list = ws.tile_list + (size_t)idx * kp.max_blocks;
+      int k = 0;
+      for (int w = 0; w * 32 < nb; ++w) {
+        const int lo = w * 32;
+        uint32_t bits = words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u);
+        while (bits) {
+          const int b = lo + __ffs(bits) - 1;
+          const int pg = b * ppt;
+          const bool two = ppt == 2 && b * kTile + kp.P < L;
+          list[k++] = make_int4(b, pt[pg], two ? pt[pg + 1] : 0, 0);
+          bits &= bits - 1;
+        }
+      }
+    }
+  }
 }
 
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const WsView& ws, cudaStream_t stream) {
-  compact_kernel<<<1, kCompactThreads, 0, stream>>>(modes, seq_lens, support, ws, kp);
-  return cudaGetLastError();
+                           const uint32_t* support, const int32_t* page_table, const WsView& ws,
+                           cudaStream_t stream) {
+  return launch_pdl(compact_kernel, dim3(1), dim3(kCompactThreads), 0, stream, modes, seq_lens,
+                    support, page_table, ws, kp);
 }
 
 // ------------------------------------------------------------------ union

@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(256)
                   const WsView ws, const KParams kp, uint32_t* __restrict__ support,
                   T* __restrict__ out, float* __restrict__ lse) {
   __shared__ uint32_t smask[32];
+  grid_dependency_wait();    // the partial pass's results
+  grid_dependents_launch();  // the next call's compaction may start launching
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256)
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 
   const int4 hi = ws.head_info[rg];
-  if (L == 0 || hi.y == 0) {  // padding row, or a sparse row selecting nothing
+  if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
     if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
     else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
@@ -142,11 +144,15 @@ __global__ void __launch_bounds__(256)
 
   const float2* ml = ws.partial_ml;
   float M = -INFINITY;
+  // hi.x = first partial slot of this (row, KV head) (rg * S_max); its hi.y
+  // block ranges occupy the next slots (an empty range of a sparse row
+  // holds (-inf, 0) and is skipped).
   for (int i = 0; i < hi.y; ++i) M = fmaxf(M, ml[(size_t)(hi.x + i) * G + warp].x);
   float lam = 0.f;
   for (int i = 0; i < hi.y; ++i) {
     const size_t idx = (size_t)(hi.x + i) * G + warp;
     const float2 t = ml[idx];
+    if (!(t.y > 0.f)) continue;
     const float w = exp2f(t.x - M);
     lam = fmaf(t.y, w, lam);
     const float* a = ws.partial_acc + idx * D + lane * dpl;
@@ -198,12 +204,10 @@ cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,
   const int grid = kp.R * kp.Hkv;
   const int threads = 32 * kp.G;
   if (dtype == WISE_DTYPE_BF16)
-    finish_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
-        modes, seq_lens, ws, kp, support, static_cast<__nv_bfloat16*>(out), lse);
-  else
-    finish_kernel<float><<<grid, threads, 0, stream>>>(modes, seq_lens, ws, kp, support,
-                                                       static_cast<float*>(out), lse);
-  return cudaGetLastError();
+    return launch_pdl(finish_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, stream, modes,
+                      seq_lens, ws, kp, support, static_cast<__nv_bfloat16*>(out), lse);
+  return launch_pdl(finish_kernel<float>, dim3(grid), dim3(threads), 0, stream, modes, seq_lens,
+                    ws, kp, support, static_cast<float*>(out), lse);
 }
 
 }  // namespace wise

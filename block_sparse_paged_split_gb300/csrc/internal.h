@@ -1,6 +1,8 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace wise {
@@ -8,7 +10,8 @@ namespace wise {
 // Launchers (host).  Each enqueues one kernel on `stream` and returns the
 // launch status; none allocates or synchronises.
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const WsView& ws, cudaStream_t stream);
+                           const uint32_t* support, const int32_t* page_table, const WsView& ws,
+                           cudaStream_t stream);
 
 cudaError_t launch_partial_bf16(const KParams& kp, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const void* q, const int32_t* page_table, const int32_t* seq_lens,
@@ -27,6 +30,26 @@ cudaError_t launch_union(uint32_t* dst, const uint32_t* src, int64_t n_words,
 cudaError_t launch_validate(const KParams& kp, const int32_t* page_table,
                             const int32_t* seq_lens, const int8_t* modes,
                             const uint32_t* support, int32_t* err_word, cudaStream_t stream);
+
+// Launches `kern` as a programmatic dependent of the previous kernel in the
+// stream: its CTAs may start while that kernel finishes, and every kernel of
+// this library calls grid_dependency_wait() before it reads anything an
+// earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();

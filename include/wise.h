@@ -112,14 +112,16 @@ typedef struct {
   int32_t num_q_heads;       /* Hq >= 1                                         */
   int32_t num_kv_heads;      /* Hkv >= 1, Hq % Hkv == 0, Hq/Hkv in {1,2,4,8}    */
   int32_t head_dim;          /* D in {64, 128}                                  */
-  int32_t page_size;         /* tokens per page: 8, 16 or 32                    */
+  int32_t page_size;         /* tokens per page: 16 or 32                       */
   int32_t tile_tokens;       /* block size B; must be 32                        */
   int32_t max_pages_per_row; /* page_table row stride, >= 1                     */
   int32_t num_pages;         /* pages in the K/V pools, >= 1                    */
   int32_t max_blocks;        /* mask capacity per (row, KV head), 1..1024;
                                 a row's capacity is min(max_blocks * 32,
                                 max_pages_per_row * page_size) tokens          */
-  int32_t tiles_per_item;    /* tiles per split work item, 1..64; 0 means 8     */
+  int32_t tiles_per_item;    /* blocks per split range T: 1, 2, 4, 8 or 16;
+                                0 means 8.  Work item s of a (row, KV head)
+                                holds its tiles in blocks [s*T, s*T + T)   */
   int32_t dtype;             /* WISE_DTYPE_* of q, k_cache, v_cache and out     */
   float scale;               /* softmax scale; 0 means 1/sqrt(head_dim)         */
   float eta;                 /* selection threshold, > 0; >= 1 selects all      */
@@ -130,11 +132,23 @@ typedef struct {
 typedef struct {
   size_t status_word;   /* int32: WISE_DEVERR_* bits, cleared by compaction   */
   size_t num_items;     /* int32: work items written by compaction            */
-  size_t head_info;     /* int32x4 [R*Hkv]: first item, items, tiles, 0        */
-  size_t tile_list;     /* int32 [R*Hkv, max_blocks]: sparse rows' tiles, asc */
-  size_t items;         /* int32x4 [max_items]: row, KV head, first, tiles     */
+  size_t queue;         /* int32 x2: next schedule slot and finished CTAs of
+                           the partial pass (both back to 0 after each pass) */
+  size_t head_info;     /* int32x4 [R*Hkv]: first partial slot (rg * S),
+                           block ranges, tiles, non-empty items                */
+  size_t tile_list;     /* int32x4 [R*Hkv, max_blocks]: sparse rows' tiles in
+                           ascending order: block, page of its first
+                           page_size tokens, page of the next (or 0), 0      */
+  size_t items;         /* int32x4 [max_items], in schedule order (tile count
+                           descending): row*Hkv + KV head, first tile-list
+                           index (sparse) or first block, tile count |
+                           range s << 8 | sparse << 24 | discover << 25,
+                           sequence length                                     */
   size_t partial_ml;    /* float32x2 [max_items, G]: running max (log2 units)
-                           and exp-sum of each item and query head             */
+                           and exp-sum per item and query head; range s of
+                           (row, KV head) rg lives in slot rg * S + s, with
+                           S = ceil(max_blocks / tiles_per_item); an empty
+                           range of a sparse row holds (-inf, 0)              */
   size_t partial_acc;   /* float32 [max_items, G, D]: unnormalised outputs     */
   size_t tile_stats;    /* float32x2 [R*Hq, max_blocks]: per tile max (log2
                            units of the scaled score) and exp-sum (discover)  */
@@ -153,15 +167,16 @@ wise_status wise_workspace_layout(const wise_shape *shape,
 /* Compaction [WISE PR, "What changes": sparse rows are compacted first so
  * the loop has no branch; programs cover about eight tiles].  For each
  * (row, KV head): the tile list (ascending selected blocks below the row's
- * block count for sparse rows; implicitly 0..n_b-1 for the other modes), cut
- * in order into work items of at most tiles_per_item tiles.  Reads modes,
- * seq_lens and (sparse rows only) support; writes the workspace (items, head
- * info, tile lists) and clears its status word.  The workspace must be
- * 256-byte aligned and at least wise_workspace_bytes long. */
+ * block count for sparse rows, each with its page ids; implicitly 0..n_b-1
+ * for the other modes), cut in order into work items of at most
+ * tiles_per_item tiles.  Reads modes, seq_lens and, for sparse rows, support
+ * and page_table; writes the workspace (items, head info, tile lists) and
+ * clears its status word.  The workspace must be 256-byte aligned and at
+ * least wise_workspace_bytes long. */
 wise_status wise_compact_tiles(const wise_shape *shape, const int8_t *modes,
                                const int32_t *seq_lens, const uint32_t *support,
-                               void *workspace, size_t workspace_bytes,
-                               wise_stream_t stream);
+                               const int32_t *page_table, void *workspace,
+                               size_t workspace_bytes, wise_stream_t stream);
 
 /* Split partial pass [WISE PR, "What changes": split-KV paged decode with
  * per-row modes].  For every work item written by wise_compact_tiles and

@@ -200,15 +200,17 @@ def union_density(support: np.ndarray, seq_lens: np.ndarray, B: int) -> float:
 # --------------------------------------------------------------------------- compaction
 def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray, B: int,
                   tiles_per_item: int) -> Dict[str, object]:
-    """Tile lists and the balanced work list [WISE PR, "What changes": sparse
-    rows attend only their selected tiles, compacted first so the loop has no
+    """Tile lists and the work list [WISE PR, "What changes": sparse rows
+    attend only their selected tiles, compacted first so the loop has no
     branch; programs cover about eight tiles each].
 
     Per (row, KV head): the list is the ascending selected blocks b < n_b for
-    sparse rows and 0..n_b-1 otherwise.  Each list is cut in order into items
-    of at most `tiles_per_item` tiles; items are ordered by (row, head, split).
-    """
+    sparse rows and 0..n_b-1 otherwise.  Work item s of the pair holds the
+    list's tiles whose blocks lie in [s*T, s*T + T) (T = tiles_per_item); a
+    range with no tile has no item.  Items are ordered by (row, head, s) and
+    given as (row, head, s, first index in the list, tile count)."""
     R, Hkv, _ = support.shape
+    T = tiles_per_item
     lists: List[List[np.ndarray]] = []
     items = []
     for r in range(R):
@@ -220,10 +222,12 @@ def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray, 
             else:
                 lst = np.arange(nb, dtype=np.int32)
             per.append(lst)
-            for first in range(0, lst.shape[0], tiles_per_item):
-                items.append((r, g, first, min(tiles_per_item, lst.shape[0] - first)))
+            for s in range(-(-nb // T)):
+                in_range = np.nonzero((lst >= s * T) & (lst < (s + 1) * T))[0]
+                if in_range.size:
+                    items.append((r, g, s, int(in_range[0]), int(in_range.size)))
         lists.append(per)
-    return {"lists": lists, "items": np.array(items, dtype=np.int32).reshape(-1, 4)}
+    return {"lists": lists, "items": np.array(items, dtype=np.int32).reshape(-1, 5)}
 
 
 # --------------------------------------------------------------------------- one call

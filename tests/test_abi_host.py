@@ -50,7 +50,8 @@ def test_workspace_layout_is_aligned_and_sized(lib):
     assert lay["total_bytes"] == W.wise_workspace_bytes(s)
     offs = [lay[k] for k in ("head_info", "tile_list", "items", "partial_ml", "partial_acc", "tile_stats")]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
-    # max items: every (row, KV head) split into ceil(max_blocks / 8) items
+    # max items: every (row, KV head) split into ceil(max_blocks / 8) block
+    # ranges (the default range is 8 blocks)
     assert lay["max_items"] == 4 * 2 * -(-s.max_blocks // 8)
     assert lay["partial_acc"] - lay["partial_ml"] >= lay["max_items"] * 4 * 8
     # zero rows: header only
@@ -59,9 +60,10 @@ def test_workspace_layout_is_aligned_and_sized(lib):
 
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 96, 2), ("num_kv_heads", 3, 1), ("num_q_heads", 24, 2), ("page_size", 12, 2),
+    ("page_size", 8, 2),
     ("tile_tokens", 64, 2), ("max_blocks", 2048, 2), ("max_blocks", 0, 2), ("dtype", 7, 1),
     ("eta", 0.0, 1), ("eta", float("nan"), 1), ("scale", -1.0, 1), ("num_rows", -1, 1),
-    ("num_pages", 0, 1), ("tiles_per_item", 65, 1)])
+    ("num_pages", 0, 1), ("tiles_per_item", 17, 1), ("tiles_per_item", 3, 1)])
 def test_shape_checks(lib, field, value, status):
     s = _shape()
     setattr(s, field, value)
@@ -76,11 +78,14 @@ def test_host_checks_before_any_launch(lib):
     n = W.wise_workspace_bytes(s)
     P = ctypes.c_void_p
     # NULL workspace
-    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, None, n, None)
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(16), None, n, None)
     assert st == 3
     # misaligned workspace
-    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(4096 + 8), n, None)
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(16), P(4096 + 8), n, None)
     assert st == 3
+    # NULL page table
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, None, P(4096), n, None)
+    assert st == 1
     # workspace too small
     st = lib.wise_decode_partial(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
                                  P(4096), n - 1, None)

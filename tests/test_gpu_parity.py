@@ -49,7 +49,7 @@ def test_modes_match_oracle(Hq, Hkv, D, dtype):
     m = np.full(R, W.MODE_DISCOVER_UNION, np.int8)
     g, o = gpu_call(b, 1, m, s0), oracle_call(b, 1, m, s0)
     assert not compare_outputs(w, g, o)
-    cm = compare_masks(w, g["support"], o, m)
+    cm = compare_masks(w, g["support"], o, m, support_in=s0)
     assert not cm["fails"], cm
     # sparse on the oracle's union mask (the same mask on both sides)
     s1 = o["support"]
@@ -92,14 +92,14 @@ def test_tiny_schedule_f32():
         m = w.depth_modes[depth]
         g, o = gpu_call(b, depth, m, sup), oracle_call(b, depth, m, sup)
         assert not compare_outputs(w, g, o)
-        assert not compare_masks(w, g["support"], o, m)["fails"]
+        assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
         sup = o["support"]
 
 
 def test_compaction_matches_oracle():
-    """Tile lists, per-head item counts and work items: bit-exact."""
+    """Tile lists (with page ids), per-head counts and work items: bit-exact."""
     rng = np.random.default_rng(5)
-    for T in (1, 3, 8):
+    for T in (1, 2, 4, 8):
         lens = rng.integers(0, 700, size=9).astype(np.int32)
         w = _wl(4, 2, 64, "bf16", lens=lens, seed=9)
         R = w.num_rows
@@ -109,20 +109,48 @@ def test_compaction_matches_oracle():
         shape = shape_for(w, tiles_per_item=T)
         ws = W.alloc_workspace(shape)
         W.wise_compact_tiles(shape, torch.from_numpy(modes).cuda(), torch.from_numpy(lens).cuda(),
-                             dev_support(sup), ws)
+                             dev_support(sup), torch.from_numpy(w.page_table).cuda(), ws)
         torch.cuda.synchronize()
         v = {k: t.cpu().numpy() for k, t in W.workspace_views(shape, ws).items()}
         ref = O.compact_tiles(sup, modes, lens, 32, T)
         n = int(v["num_items"][0])
         assert n == ref["items"].shape[0]
-        assert np.array_equal(v["items"][:n], ref["items"])
+        rec = v["items"][:n]
+        # Records are in schedule order: the tile counts never increase.
+        sizes = rec[:, 2] & 0xFF
+        assert np.all(np.diff(sizes) <= 0)
+        ranges = (rec[:, 2] >> 8) & 0xFFFF
+        # In canonical (row, KV head, range) order they are the oracle's items.
+        order = np.lexsort((ranges, rec[:, 0]))
+        canon, crange = rec[order], ranges[order]
+        mine = np.stack([canon[:, 0] // 2, canon[:, 0] % 2, crange, canon[:, 1], canon[:, 2] & 0xFF], 1)
+        assert np.array_equal(mine, ref["items"])
+        for row in canon:
+            r = row[0] // 2
+            assert bool(row[2] & (1 << 24)) == (modes[r] == W.MODE_SPARSE)
+            assert bool(row[2] & (1 << 25)) == (modes[r] in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION))
+            assert row[3] == lens[r]
+        assert int(v["queue"][0]) == 0
+        S_max = -(-shape.max_blocks // T)
         for r in range(R):
+            nb = -(-int(lens[r]) // 32)
             for g in range(2):
                 lst = ref["lists"][r][g]
-                assert v["head_info"][r, g, 2] == lst.shape[0]
-                assert v["head_info"][r, g, 1] == -(-lst.shape[0] // T)
+                hi = v["head_info"][r, g]
+                assert hi[0] == (r * 2 + g) * S_max
+                assert hi[1] == -(-nb // T) and hi[2] == lst.shape[0]
                 if modes[r] == W.MODE_SPARSE:
-                    assert np.array_equal(v["tile_list"][r, g, :lst.shape[0]], lst)
+                    tl = v["tile_list"][r, g, :lst.shape[0]]
+                    assert np.array_equal(tl[:, 0], lst)
+                    # each tile carries the pages of its valid tokens (0 past the row)
+                    for (b_, p0, p1, _z) in tl:
+                        assert p0 == w.page_table[r, 2 * b_]
+                        assert p1 == (w.page_table[r, 2 * b_ + 1] if 32 * b_ + 16 < lens[r] else 0)
+                    # empty ranges are marked so the finish pass skips them
+                    ml = v["partial_ml"][hi[0]:hi[0] + hi[1]]
+                    for s_ in range(hi[1]):
+                        if not np.any(lst // T == s_):
+                            assert np.all(np.isneginf(ml[s_, :, 0])) and np.all(ml[s_, :, 1] == 0)
         assert int(v["status"][0]) == 0
 
 
@@ -165,11 +193,42 @@ def test_split_size_invariance():
     zero = np.zeros((R, 4, words(w)), np.uint32)
     m = np.full(R, W.MODE_DENSE, np.int8)
     ref = gpu_call(b, 0, m, zero, tiles_per_item=8)
-    for T in (1, 3, 64):
+    for T in (1, 2, 16):
         g = gpu_call(b, 0, m, zero, tiles_per_item=T)
         assert np.max(np.abs(g["out"] - ref["out"])) < 1e-5
         fin = np.isfinite(ref["lse"])
         assert np.max(np.abs(g["lse"][fin] - ref["lse"][fin])) < 1e-5
+
+
+def test_partial_reuses_a_compaction():
+    """Two partial + finish passes over one compaction (the next depth reusing
+    the same mask) give the same results as separate compactions."""
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    rng = np.random.default_rng(4)
+    bits = rng.random((R, 4, words(w) * 32)) < 0.3
+    sup = dev_support(np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 4, -1))
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    modes = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
+    W.wise_compact_tiles(shape, modes, b.seq_lens, sup, b.page_table, ws)
+    outs = []
+    for depth in (0, 1, 1):
+        d = b.dev(depth)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, 4), dtype=torch.float32, device="cuda")
+        W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
+                              modes, ws)
+        W.wise_decode_finish(shape, modes, b.seq_lens, ws, sup, out, lse)
+        outs.append((out.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert int(W.workspace_views(shape, ws)["queue"].item()) == 0
+    sup_np = np_support(sup)
+    for depth, (out, lse) in zip((0, 1, 1), outs):
+        ref = gpu_call(b, depth, np.full(R, W.MODE_SPARSE, np.int8), sup_np)
+        assert torch.equal(out.cpu(), ref["out_raw"])
+        assert np.array_equal(lse.cpu().numpy(), ref["lse"])
 
 
 def test_one_call_entry_point_matches_stepwise():
@@ -252,7 +311,8 @@ def test_seq_len_above_capacity_is_clamped_and_flagged():
     lens[0] = cap + 1000
     ws = W.alloc_workspace(shape)
     modes = torch.zeros(4, dtype=torch.int8, device="cuda")
-    W.wise_compact_tiles(shape, modes, torch.from_numpy(lens).cuda(), None, ws)
+    W.wise_compact_tiles(shape, modes, torch.from_numpy(lens).cuda(), None,
+                         torch.from_numpy(w.page_table).cuda(), ws)
     torch.cuda.synchronize()
     v = W.workspace_views(shape, ws)
     assert int(v["status"].item()) & W.wise.DEVERR_SEQ_LEN_CLAMPED

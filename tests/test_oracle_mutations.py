@@ -138,10 +138,22 @@ def m_compaction_split_off_by_one(O):
     O.compact_tiles = compact_tiles
 
 
+def m_compaction_first_index_shifted(O):
+    orig = O.compact_tiles
+
+    def compact_tiles(support, modes, seq_lens, B, T):
+        res = orig(support, modes, seq_lens, B, T)
+        items = res["items"].copy()
+        items[:, 3] = np.maximum(items[:, 3] - 1, 0)
+        return {**res, "items": items}
+    O.compact_tiles = compact_tiles
+
+
 MUTANTS = [m_scale_squared, m_slot_off_by_one, m_page_order_reversed, m_wrong_kv_head, m_unnormalised_output,
            m_tile_sum_without_max, m_masses_drop_partial_block, m_ties_to_higher_index,
            m_strict_cutoff, m_one_extra_block, m_union_overwrites, m_mask_ignored,
-           m_mask_bit_order_reversed, m_compaction_split_off_by_one]
+           m_mask_bit_order_reversed, m_compaction_split_off_by_one,
+           m_compaction_first_index_shifted]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
