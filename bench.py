@@ -54,6 +54,10 @@ def parse():
                    help="split work-item size (0: the library default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    p.add_argument("--record-traffic", default=None, metavar="RAW_CSV",
+                   help="store the DRAM bytes of the partial-kernel launches in an ncu "
+                        "'--page raw --csv' export (one WISE step of --rows rows) with the "
+                        "kernel's source hash, and exit")
     return p.parse_args()
 
 
@@ -109,6 +113,61 @@ def run_oracle_sample(workload: str, rows: int, reps: int) -> dict:
             "kind": "oracle",
             "sample": f"{rows} rows of {workload} (same recipe), {reps}x the 4-depth schedule, "
                       f"numpy float64, BLAS pinned to 1 thread; {out['seconds']:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- traffic
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_kernel_traffic.json")
+KERNEL_SOURCES = ("partial_kernel.cuh", "partial_bf16.cu", "common.cuh", "internal.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_paged_split_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def record_traffic(raw_csv: str, rows: int, workload: str) -> None:
+    """Per-launch dram__bytes_read.sum + dram__bytes_write.sum of the
+    partial-kernel launches in an ncu raw CSV, in launch order (the four
+    depths of one step), saved with the kernel's source hash."""
+    import csv
+    with open(raw_csv) as f:
+        table = list(csv.reader(f))
+    head = table[0]
+    col = {n: i for i, n in enumerate(head)}
+    units = table[1]
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    launches = []
+    for row in table[2:]:
+        if "partial_kernel" not in row[col["Kernel Name"]]:
+            continue
+        total = 0.0
+        for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            total += float(row[col[m]].replace(",", "")) * scale[units[col[m]]]
+        launches.append(total)
+    out = {"kernel_source_sha256": kernel_source_hash(), "workload": workload,
+           "captured_rows": rows, "per_launch_bytes": launches,
+           "note": "one WISE step (depths 0-3) of the captured rows; scaled to the bench's "
+                   "rows by rows/captured_rows (traffic grows in proportion to rows)"}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out))
+
+
+def recorded_traffic(rows: int):
+    """Average per-launch DRAM bytes of the partial pass, or None when no
+    capture exists for the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256") != kernel_source_hash() or not rec.get("per_launch_bytes"):
+        return None
+    per = rec["per_launch_bytes"][:4]
+    return sum(per) / len(per) * rows / rec["captured_rows"]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -206,7 +265,7 @@ class Pipeline:
             m = modes_t.data_ptr()
             c = []
             if compact:
-                c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, pt, ws, nws, st)))
+                c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, ws, nws, st)))
             c.append(("partial", lib.wise_decode_partial,
                       (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                        pt, sl, m, ws, nws, st)))
@@ -216,12 +275,26 @@ class Pipeline:
 
         mode_name = {W.MODE_DENSE: "dense", W.MODE_DISCOVER: "discover",
                      W.MODE_DISCOVER_UNION: "discover_union", W.MODE_SPARSE: "sparse"}
+        def depth_name(m):
+            u = set(int(x) for x in m)
+            return mode_name[u.pop()] if len(u) == 1 else "mixed"
+
+        def all_sparse(m):
+            return all(int(x) == W.MODE_SPARSE for x in m)
+
         self.wise_step = []
         for t in range(w.num_depths):
-            mode = int(w.depth_modes[t][0])
-            reuse = t > 0 and mode == W.MODE_SPARSE and int(w.depth_modes[t - 1][0]) == W.MODE_SPARSE
-            self.wise_step.append((t, mode_name[mode], calls(self.modes[t], t, compact=not reuse)))
+            reuse = t > 0 and all_sparse(w.depth_modes[t]) and all_sparse(w.depth_modes[t - 1])
+            self.wise_step.append((t, depth_name(w.depth_modes[t]),
+                                   calls(self.modes[t], t, compact=not reuse)))
         self.dense_step = [(t, "dense", calls(self.dense_modes, t)) for t in range(w.num_depths)]
+        # Sparse rows of a depth that no earlier depth discovers (a mixed
+        # batch) use the support of a prior discovery of the same inputs.
+        if any(int(x) == W.MODE_SPARSE for x in w.depth_modes[0]):
+            disc = torch.full((w.num_rows,), W.MODE_DISCOVER, dtype=torch.int8, device=dev)
+            for kind, fn, args in calls(disc, 0):
+                fn(*args)
+            torch.cuda.synchronize()
 
     def graph(self, step):
         """The step captured once as a CUDA graph (its launches bound to the
@@ -262,17 +335,19 @@ class Pipeline:
     def launches_per_step(self, step) -> int:
         return sum(len(calls) for _, _, calls in step)
 
-    def kv_bytes(self, mode: str, t: int) -> int:
-        """Algorithmic K+V bytes one partial launch must read at depth t."""
-        np, w = self.np, self.w
-        per_token = w.num_kv_heads * w.head_dim * (2 if w.dtype == "bf16" else 4) * 2
-        if mode != "sparse":
-            return int(w.seq_lens.sum()) * per_token
+    def kv_bytes(self, modes) -> int:
+        """Algorithmic K+V bytes one partial launch must read for these row
+        modes: every token of dense and discover rows, the selected tiles'
+        tokens of sparse rows (from the current mask)."""
+        np, w, W = self.np, self.w, self.W
+        per_head_token = w.head_dim * (2 if w.dtype == "bf16" else 4) * 2
         sup = self.support.cpu().numpy().view(np.uint32)
-        per_head_token = per_token // w.num_kv_heads
         total = 0
         for r in range(w.num_rows):
             L = int(w.seq_lens[r])
+            if int(modes[r]) != W.MODE_SPARSE:
+                total += L * w.num_kv_heads * per_head_token
+                continue
             nb = -(-L // 32)
             bits = np.unpackbits(sup[r].view(np.uint8).reshape(w.num_kv_heads, -1), axis=1,
                                  bitorder="little")[:, :nb]
@@ -403,10 +478,12 @@ def main_ours(args):
     # every step: the inputs do not change).
     kv = {}
     for t, mode, _ in pipe.wise_step:
-        kv[(t, mode)] = pipe.kv_bytes(mode, t) + pipe.small_bytes()
+        kv[(t, mode)] = pipe.kv_bytes(w.depth_modes[t]) + pipe.small_bytes()
     for t, mode, _ in pipe.dense_step:
-        kv[(t, mode)] = pipe.kv_bytes("dense", t) + pipe.small_bytes()
-    density = kv[(2, "sparse")] / kv[(2, "dense")] if (2, "sparse") in kv else None
+        kv[(t, mode)] = pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) + pipe.small_bytes()
+    sparse_depths = [t for t, mode, _ in pipe.wise_step if mode == "sparse"]
+    density = (pipe.kv_bytes(w.depth_modes[sparse_depths[0]]) /
+               pipe.kv_bytes(np.zeros(w.num_rows, np.int8))) if sparse_depths else None
 
     # The step and the dense baseline step, each captured once as a CUDA graph.
     graph = pipe.graph(pipe.wise_step)
@@ -471,6 +548,7 @@ def main_ours(args):
                       "rows_per_s": round(R / (dense_call * 1e-3), 1),
                       "partial_gbs": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9, 1),
                       "partial_frac_of_measured_hbm": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9 / peak, 3),
+                      "algorithmic_bytes": kv[(0, "dense")],
                       "step_ms_eager": round(ms_dense / args.steps, 4),
                       "step_ms_graph": round(ms_dense_graph / args.steps, 4)}
 
@@ -489,14 +567,19 @@ def main_ours(args):
                                f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, D={w.head_dim}, "
                                f"page {w.page_size}, B=32, eta={w.eta}, 4 depths",
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
-                   "l2": "inputs larger than L2: 2.1 GB of K/V per step (129 MB L2)",
+                   "l2": f"inputs larger than L2: "
+                         f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "
+                         f"of K/V per step (129 MB L2)",
                    "timing": "value: CUDA-graph replay of the step, CUDA events around the K "
                              "replays; modes and roofline: eager launches with CUDA events "
                              "around every launch on the launching stream",
                    "union_density": round(density, 4) if density else None},
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": (round(traffic) if (traffic := recorded_traffic(R)) else None),
+                     "algorithmic_bytes_per_launch": round(
+                         part_bytes / sum(1 for k in per if k[2] == "partial")),
                      "kernel": "partial_kernel (split-KV partial pass, all four depths)",
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -546,6 +629,8 @@ if __name__ == "__main__":
     a = parse()
     if a.oracle_sample is not None:
         oracle_sample_main(a.oracle_sample)
+    elif a.record_traffic is not None:
+        record_traffic(a.record_traffic, a.rows or 64, a.workload)
     elif a.impl == "reference":
         main_reference(a)
     else:

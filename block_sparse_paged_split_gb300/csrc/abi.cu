@@ -103,7 +103,6 @@ void compute_layout(const wise_shape* s, wise_layout* l) {
   l->queue = 8;
   off = 256;
   l->head_info = off;   off = up256(off + pairs * sizeof(int4));
-  l->tile_list = off;   off = up256(off + pairs * kp.max_blocks * sizeof(int4));
   l->items = off;       off = up256(off + max_items * sizeof(int4));
   l->partial_ml = off;  off = up256(off + max_items * kp.G * sizeof(float2));
   l->partial_acc = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
@@ -125,7 +124,6 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v)
   v->queue = reinterpret_cast<int32_t*>(b + l.queue);
   v->queue_done = reinterpret_cast<int32_t*>(b + l.queue + 4);
   v->head_info = reinterpret_cast<int4*>(b + l.head_info);
-  v->tile_list = reinterpret_cast<int4*>(b + l.tile_list);
   v->items = reinterpret_cast<int4*>(b + l.items);
   v->partial_ml = reinterpret_cast<float2*>(b + l.partial_ml);
   v->partial_acc = reinterpret_cast<float*>(b + l.partial_acc);
@@ -137,13 +135,20 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v)
 // ------------------------------------------------------------ tensor maps
 struct MapKey {
   const void* ptr;
-  int device, num_pages, page_size, kv_heads, head_dim, dtype;
+  int device, num_pages, page_size, kv_heads, head_dim, dtype, swizzled;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && device == o.device && num_pages == o.num_pages &&
            page_size == o.page_size && kv_heads == o.kv_heads && head_dim == o.head_dim &&
-           dtype == o.dtype;
+           dtype == o.dtype && swizzled == o.swizzled;
   }
 };
+
+// The tensor-core path (bf16 with grouped query heads) loads half rows of 64
+// elements with the 128-byte shared-memory swizzle; the FMA path loads whole
+// rows unswizzled.
+bool uses_tensor_cores(const wise_shape* s) {
+  return s->dtype == WISE_DTYPE_BF16 && s->num_q_heads > s->num_kv_heads;
+}
 
 constexpr int kMapCache = 32;
 std::mutex g_map_mu;
@@ -156,7 +161,9 @@ wise_status tensor_map(const wise_shape* s, const void* base, CUtensorMap* out) 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  const MapKey key{base, dev, s->num_pages, s->page_size, s->num_kv_heads, s->head_dim, s->dtype};
+  const int swizzled = uses_tensor_cores(s) ? 1 : 0;
+  const MapKey key{base, dev, s->num_pages, s->page_size, s->num_kv_heads, s->head_dim, s->dtype,
+                   swizzled};
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (int i = 0; i < g_map_used; ++i)
     if (g_map_keys[i] == key) {
@@ -178,14 +185,16 @@ wise_status tensor_map(const wise_shape* s, const void* base, CUtensorMap* out) 
                               (cuuint64_t)s->num_pages * s->page_size};
   const cuuint64_t strides[2] = {(cuuint64_t)s->head_dim * es,
                                  (cuuint64_t)s->num_kv_heads * s->head_dim * es};
-  const cuuint32_t box[3] = {(cuuint32_t)s->head_dim, 1u, (cuuint32_t)s->page_size};
+  const cuuint32_t box[3] = {(cuuint32_t)(swizzled ? 64 : s->head_dim), 1u,
+                             (cuuint32_t)s->page_size};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMap m;
   CUresult r = g_encode(&m,
                         s->dtype == WISE_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                         3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(WISE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   const int slot = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
@@ -259,16 +268,15 @@ wise_status wise_workspace_layout(const wise_shape* shape, wise_layout* layout) 
 
 wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
                                const int32_t* seq_lens, const uint32_t* support,
-                               const int32_t* page_table, void* workspace,
-                               size_t workspace_bytes, wise_stream_t stream) {
+                               void* workspace, size_t workspace_bytes, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
-  if (shape->num_rows > 0 && (!modes || !seq_lens || !page_table))
-    return fail(WISE_ERR_INVALID_ARG, "modes, seq_lens and page_table must not be NULL");
+  if (shape->num_rows > 0 && (!modes || !seq_lens))
+    return fail(WISE_ERR_INVALID_ARG, "modes and seq_lens must not be NULL");
   if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
-  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, support, page_table, ws,
+  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, support, ws,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "compact launch");
 }
@@ -318,7 +326,7 @@ wise_status wise_decode(const wise_shape* shape, const void* q, const void* k_ca
                         const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
                         const int8_t* modes, uint32_t* support, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, wise_stream_t stream) {
-  wise_status st = wise_compact_tiles(shape, modes, seq_lens, support, page_table, workspace,
+  wise_status st = wise_compact_tiles(shape, modes, seq_lens, support, workspace,
                                       workspace_bytes, stream);
   if (st != WISE_OK) return st;
   st = wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,

@@ -38,8 +38,7 @@ struct WsView {
                        // the last CTA of every partial launch
   int32_t* queue_done; // CTAs of the running partial launch past the queue
   int4* head_info;     // [R*Hkv]: first item, item count, tile count, 0
-  int4* tile_list;     // [R*Hkv, max_blocks]: block, first page, second page (or 0), 0
-  int4* items;         // [max_items] in schedule order: rg, first, tiles | flags, L
+  int4* items;         // [max_items] in schedule order: rg, range, bitmap | count << 16, L | flags
   float2* partial_ml;  // [max_items, G], split s of rg in slot rg * S_max + s
   float* partial_acc;  // [max_items, G, D]
   float2* tile_stats;  // [R*Hq, max_blocks]
@@ -48,10 +47,10 @@ struct WsView {
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
-// Work item record, third field: tile count (bits 0-7), block range index
-// (bits 8-23) and mode flags (bits 24, 25).
+// Work item record, fourth field: row length (bits 0-23) and mode flags.
 constexpr int kItemSparse = 1 << 24;
 constexpr int kItemDiscover = 1 << 25;
+constexpr int kItemLenMask = (1 << 24) - 1;
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -14,118 +14,109 @@ namespace wise {
 
 constexpr int kCompactThreads = 1024;
 
-// Block-wide exclusive scan of one int per thread; returns the block total
-// through *total.  Uses `warp_tot` (32 ints of shared memory).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int nw = blockDim.x >> 5;
-    int t = lane < nw ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < nw) warp_tot[lane] = t;
-  }
-  __syncthreads();
-  const int base = wid ? warp_tot[wid - 1] : 0;
-  *total = warp_tot[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return base + incl - v;
-}
-
 // Work items are block ranges: item (rg, s) holds the tiles of (row, KV head)
 // rg that lie in blocks [s*T, s*T + T) -- all of them for dense and discover
-// rows, the selected ones for sparse rows (skipped when none is).  A row's
+// rows, the selected ones for sparse rows (no item when none is).  A row's
 // split therefore depends only on its own length, mode and mask, and a
 // sparse row with every block selected splits exactly like a dense row.
 // Item (rg, s) writes its partial output to slot rg * S_max + s.
 //
+// An item record carries its compacted tiles as a bitmap over its range:
+// x = rg, y = s, z = tile bitmap (bit i: block s*T + i) | tile count << 16,
+// w = row length | sparse << 24 | discover << 25.  The partial pass walks the
+// set bits in order (the k-th tile is the k-th set bit), so its inner loop
+// has no branch and needs no list in memory.
+//
 // Compaction writes the items already in schedule order, which is the order
 // the partial pass hands them out (through an atomic counter): tile count
-// descending, so the last warps do not finish long items alone.  Each record
-// is self-contained: x = rg, y = first index in the tile list (sparse) or
-// first block (otherwise), z = tiles | flags | s << 8, w = row length.
+// descending, so the last warps do not finish long items alone.
 //
-// Phase A, a thread per (row, KV head): item and tile counts and a
-// histogram of item sizes (warp-aggregated shared-memory atomics).
-// Phase B, the same thread: its item records at their schedule slots,
-// empty-range markers for sparse rows, and its tile list.
-__device__ __forceinline__ int range_count(bool sparse, const uint32_t* words, int s, int T,
-                                           int nb) {
+// Work is flattened to one unit per (row, KV head, range): phase A counts
+// each unit's tiles and builds a histogram of item sizes (warp-aggregated
+// shared-memory atomics); phase B writes each item at its schedule slot and
+// marks the partial slots of a sparse row's empty ranges; a thread per
+// (row, KV head) writes its head info.
+__device__ __forceinline__ uint32_t range_bitmap(bool sparse, const uint32_t* words, int s, int T,
+                                                 int nb) {
   const int lo = s * T;
-  if (lo >= nb) return 0;
+  if (lo >= nb) return 0u;
   const int n = min(T, nb - lo);
-  if (!sparse) return n;
-  if (!words) return 0;
-  // T is at most 16 and a power of two here, so a range never straddles words.
-  const uint32_t w = words[lo >> 5] >> (lo & 31);
-  return __popc(w & ((1u << n) - 1u));
+  const uint32_t full = n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+  if (!sparse) return full;
+  if (!words) return 0u;
+  // T is a power of two up to 16, so a range never straddles mask words.
+  return (words[lo >> 5] >> (lo & 31)) & full;
+}
+
+struct UnitInfo {
+  uint32_t bits;
+  int L, flags;
+  bool sparse;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(int pair, int s, const int8_t* __restrict__ modes,
+                                              const int32_t* __restrict__ seq_lens,
+                                              const uint32_t* __restrict__ support,
+                                              const KParams& kp) {
+  UnitInfo u;
+  const int r = pair / kp.Hkv;
+  const int mode = modes[r];
+  u.L = clamp_len(seq_lens[r], kp.cap_tokens);
+  u.sparse = mode == WISE_MODE_SPARSE;
+  u.flags = (u.sparse ? kItemSparse : 0) |
+            (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION ? kItemDiscover : 0);
+  const uint32_t* words = (u.sparse && support) ? support + (size_t)pair * kp.W : nullptr;
+  u.bits = range_bitmap(u.sparse, words, s, kp.T, (u.L + kTile - 1) / kTile);
+  return u;
 }
 
 __global__ void __launch_bounds__(kCompactThreads)
     compact_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                   const uint32_t* __restrict__ support, const int32_t* __restrict__ page_table,
-                   const WsView ws, const KParams kp) {
+                   const uint32_t* __restrict__ support, const WsView ws, const KParams kp) {
   grid_dependency_wait();
   grid_dependents_launch();  // the partial pass may start its prologue now
-  __shared__ int warp_tot[32];
   __shared__ int size_slot[17];  // items per size (1..T), then the next schedule slot
+  __shared__ int total_items;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     *ws.status = 0;
     *ws.queue = 0;
     *ws.queue_done = 0;
+    total_items = 0;
   }
   for (int i = threadIdx.x; i <= 16; i += blockDim.x) size_slot[i] = 0;
   __syncthreads();
   const int npair = kp.R * kp.Hkv;
-  const int T = kp.T;
   const int S = kp.S_max;
+  const int nunits = npair * S;
 
-  // Phase A: counts and the size histogram.
-  int carry_items = 0;
-  for (int base = 0; base < npair; base += kCompactThreads) {
-    const int idx = base + threadIdx.x;
-    const bool valid = idx < npair;
-    int nb = 0, nitems = 0, count = 0;
-    bool sparse = false;
-    const uint32_t* words = nullptr;
-    if (valid) {
-      const int r = idx / kp.Hkv;
-      const int raw = seq_lens[r];
-      const int L = clamp_len(raw, kp.cap_tokens);
-      if (raw > kp.cap_tokens && idx % kp.Hkv == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
-      nb = (L + kTile - 1) / kTile;
-      sparse = modes[r] == WISE_MODE_SPARSE;
-      words = (sparse && support) ? support + (size_t)idx * kp.W : nullptr;
+  // A thread's units are u = threadIdx.x + i * kCompactThreads; up to
+  // kCached of them stay in registers between the two phases (more are
+  // looked up again in phase B).
+  constexpr int kCached = 8;
+  const int rounds = (nunits + kCompactThreads - 1) / kCompactThreads;
+  UnitInfo cache[kCached];
+
+  // Phase A: item sizes.
+  for (int i = 0; i < rounds; ++i) {
+    const int u = i * kCompactThreads + threadIdx.x;
+    UnitInfo ui{0u, 0, 0, false};
+    if (u < nunits) ui = unit_info(u / S, u % S, modes, seq_lens, support, kp);
+#pragma unroll
+    for (int c = 0; c < kCached; ++c)
+      if (c == i) cache[c] = ui;
+    const int n = __popc(ui.bits);
+    const unsigned same = __match_any_sync(kFull, n);
+    if (n > 0 && lane == __ffs(same) - 1) {
+      atomicAdd(&size_slot[n], __popc(same));
+      atomicAdd(&total_items, __popc(same));
     }
-    for (int s = 0; s < S; ++s) {
-      const int n = valid ? range_count(sparse, words, s, T, nb) : 0;
-      count += n;
-      nitems += n > 0;
-      const unsigned same = __match_any_sync(kFull, n);
-      if (n > 0 && lane == __ffs(same) - 1) atomicAdd(&size_slot[n], __popc(same));
-    }
-    if (valid) ws.head_info[idx] = make_int4(idx * S, (nb + T - 1) / T, count, nitems);
-    int tot = 0;
-    block_exclusive_scan(nitems, warp_tot, &tot);
-    carry_items += tot;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    *ws.num_items = carry_items;
+    *ws.num_items = total_items;
     int run = 0;
-    for (int sz = T; sz >= 1; --sz) {
+    for (int sz = kp.T; sz >= 1; --sz) {
       const int n = size_slot[sz];
       size_slot[sz] = run;
       run += n;
@@ -133,70 +124,64 @@ __global__ void __launch_bounds__(kCompactThreads)
   }
   __syncthreads();
 
-  // Phase B: item records at their schedule slots, empty-range markers,
-  // tile lists.
-  for (int base = 0; base < npair; base += kCompactThreads) {
-    const int idx = base + threadIdx.x;
-    const bool valid = idx < npair;
-    int r = 0, nb = 0, L = 0, flags = 0;
-    bool sparse = false;
-    const uint32_t* words = nullptr;
-    if (valid) {
-      r = idx / kp.Hkv;
-      L = clamp_len(seq_lens[r], kp.cap_tokens);
-      nb = (L + kTile - 1) / kTile;
-      const int mode = modes[r];
-      sparse = mode == WISE_MODE_SPARSE;
-      words = (sparse && support) ? support + (size_t)idx * kp.W : nullptr;
-      flags = (sparse ? kItemSparse : 0) |
-              (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION ? kItemDiscover : 0);
+  // Phase B: item records at their schedule slots; empty-range markers.
+  for (int i = 0; i < rounds; ++i) {
+    const int u = i * kCompactThreads + threadIdx.x;
+    const int pair = u / S, s = u % S;
+    UnitInfo ui{0u, 0, 0, false};
+    if (i < kCached) {
+#pragma unroll
+      for (int c = 0; c < kCached; ++c)
+        if (c == i) ui = cache[c];
+    } else if (u < nunits) {
+      ui = unit_info(pair, s, modes, seq_lens, support, kp);
     }
-    int first = 0;  // index into this pair's tile list (sparse rows)
-    for (int s = 0; s < S; ++s) {
-      const int n = valid ? range_count(sparse, words, s, T, nb) : 0;
-      const unsigned same = __match_any_sync(kFull, n);
-      const int leader = __ffs(same) - 1;
-      int slot = 0;
-      if (n > 0 && lane == leader) slot = atomicAdd(&size_slot[n], __popc(same));
-      slot = __shfl_sync(kFull, slot, leader);
-      if (n > 0) {
-        ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
-            make_int4(idx, sparse ? first : s * T, n | flags | (s << 8), L);
-      } else if (sparse && s * T < nb) {
-        // An empty range of a sparse row: mark its partial slot so the
-        // finish pass skips it.
-        for (int h = 0; h < kp.G; ++h)
-          ws.partial_ml[((size_t)idx * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
-      }
-      first += n;
+    const int n = __popc(ui.bits);
+    const unsigned same = __match_any_sync(kFull, n);
+    const int leader = __ffs(same) - 1;
+    int slot = 0;
+    if (n > 0 && lane == leader) slot = atomicAdd(&size_slot[n], __popc(same));
+    slot = __shfl_sync(kFull, slot, leader);
+    if (n > 0) {
+      ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
+          make_int4(pair, s, (int)(ui.bits | ((uint32_t)n << 16)), ui.L | ui.flags);
+    } else if (u < nunits && ui.sparse && s * kp.T < (ui.L + kTile - 1) / kTile) {
+      // An empty range of a sparse row: mark its partial slot so the finish
+      // pass skips it.
+      for (int h = 0; h < kp.G; ++h)
+        ws.partial_ml[((size_t)pair * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
     }
-    if (sparse && words) {
-      // Each selected tile with its page ids, so the partial pass needs one
-      // load per tile (pages past the row's length are never read: 0).
-      const int32_t* pt = page_table + (size_t)r * kp.max_pages;
-      const int ppt = kTile / kp.P;  // pages per tile: 2 or 1
-      int4* list = ws.tile_list + (size_t)idx * kp.max_blocks;
-      int k = 0;
-      for (int w = 0; w * 32 < nb; ++w) {
+  }
+
+  // Head info: first partial slot, block ranges, tiles, items.
+  for (int pair = threadIdx.x; pair < npair; pair += kCompactThreads) {
+    const int r = pair / kp.Hkv;
+    const int raw = seq_lens[r];
+    const int L = clamp_len(raw, kp.cap_tokens);
+    if (raw > kp.cap_tokens && pair % kp.Hkv == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
+    const int nb = (L + kTile - 1) / kTile;
+    const int nr = (nb + kp.T - 1) / kp.T;
+    int count = nb, nitems = nr;
+    if (modes[r] == WISE_MODE_SPARSE) {
+      count = 0;
+      nitems = 0;
+      const uint32_t* words = support ? support + (size_t)pair * kp.W : nullptr;
+      for (int w = 0; words && w * 32 < nb; ++w) {
         const int lo = w * 32;
-        uint32_t bits = words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u);
-        while (bits) {
-          const int b = lo + __ffs(bits) - 1;
-          const int pg = b * ppt;
-          const bool two = ppt == 2 && b * kTile + kp.P < L;
-          list[k++] = make_int4(b, pt[pg], two ? pt[pg + 1] : 0, 0);
-          bits &= bits - 1;
-        }
+        const uint32_t bits = words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u);
+        count += __popc(bits);
+        for (int g = 0; g < 32; g += kp.T)
+          nitems += ((bits >> g) & (kp.T >= 32 ? 0xffffffffu : (1u << kp.T) - 1u)) != 0u;
       }
     }
+    ws.head_info[pair] = make_int4(pair * S, nr, count, nitems);
   }
 }
 
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const int32_t* page_table, const WsView& ws,
-                           cudaStream_t stream) {
+                           const uint32_t* support, const WsView& ws, cudaStream_t stream) {
   return launch_pdl(compact_kernel, dim3(1), dim3(kCompactThreads), 0, stream, modes, seq_lens,
-                    support, page_table, ws, kp);
+                    support, ws, kp);
 }
 
 // ------------------------------------------------------------------ union

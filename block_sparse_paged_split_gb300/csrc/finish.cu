@@ -1,26 +1,249 @@
 // Finish pass of WISE paged decode attention.
 //
 // [WISE PR, "What changes"]: a finish kernel merges the splits and runs the
-// selection for discovery rows.  One CTA per (row, KV head), one warp per
-// query head of the group.
+// selection for discovery rows.  One CTA per (row, KV head).  Rows of up to
+// 64 blocks use one warp per query head (finish_short_kernel); longer rows
+// give each query head WPH = 4 warps (its "group" of threads, synchronised
+// by a named barrier of its own).
 //
 //   merge    M = max_i m_i, Lambda = sum_i l_i 2^(m_i - M),
 //            out = sum_i acc_i 2^(m_i - M) / Lambda, lse = (M + log2 Lambda) ln 2
-//            (m_i in log2 units of the scaled score).
-//   select   for discover rows: p_b = l_b 2^(m_b - lse2) per block; the warp
-//            sorts 64-bit keys (~bits(p_b) << 32 | b) ascending, i.e. mass
-//            descending with ties to the lower block index, with a bitonic
-//            network held in registers (E keys per lane, lane-major blocks);
-//            block at sorted position k is kept iff the mass before it is
-//            below eta, which is exactly the shortest prefix reaching eta
-//            (eta >= 1 keeps every block).  The group's query heads OR their
-//            choices in shared memory; the mask is written (DISCOVER) or ORed
-//            into (DISCOVER_UNION), with bits at or past the row's block
-//            count cleared.
+//            (m_i in log2 units of the scaled score).  Slot i is block range
+//            i of the row; an empty range of a sparse row holds (-inf, 0) and
+//            contributes nothing (its accumulator is never read into the sum).
+//            The group's threads share the slots; loads are issued four
+//            slots at a time, so long rows (many splits) are not latency-bound.
+//   select   for discover rows: p_b = l_b 2^(m_b - lse2) per block; the group
+//            sorts 64-bit keys (~bits(p_b) << 32 | b) ascending -- mass
+//            descending, ties to the lower block index -- with a bitonic
+//            network in shared memory; the block at sorted position k is kept
+//            iff the mass before it is below eta, which is exactly the shortest
+//            prefix reaching eta (eta >= 1 keeps every block).  The group's
+//            query heads OR their choices in shared memory; the mask is
+//            written (DISCOVER) or ORed into (DISCOVER_UNION), with bits at or
+//            past the row's block count cleared.
+#include <mutex>
+
 #include "internal.h"
 
 namespace wise {
 
+__device__ __forceinline__ void group_sync(int id, int threads) {
+  if (threads == 32) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+  }
+}
+
+// Exclusive prefix over the group's threads (thread th contributes v);
+// `scratch` holds one float per warp of the group.
+__device__ __forceinline__ float group_exclusive_scan(float v, int th, int wph, float* scratch,
+                                                      int bar_id) {
+  const int lane = th & 31, wsub = th >> 5;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (wph == 1) return incl - v;
+  if (lane == 31) scratch[wsub] = incl;
+  group_sync(bar_id, wph * 32);
+  float before = 0.f;
+  for (int w = 0; w < wsub; ++w) before += scratch[w];
+  group_sync(bar_id, wph * 32);
+  return before + incl - v;
+}
+
+__device__ __forceinline__ float group_max(float v, int th, int wph, float* scratch, int bar_id) {
+  const float m = warp_max(v);
+  if (wph == 1) return m;
+  if ((th & 31) == 0) scratch[th >> 5] = m;
+  group_sync(bar_id, wph * 32);
+  float r = scratch[0];
+  for (int w = 1; w < wph; ++w) r = fmaxf(r, scratch[w]);
+  group_sync(bar_id, wph * 32);
+  return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(1024)
+    finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
+                  const WsView ws, const KParams kp, uint32_t* __restrict__ support,
+                  T* __restrict__ out, float* __restrict__ lse, int wph, int npad_max) {
+  extern __shared__ __align__(16) uint8_t fsm[];
+  __shared__ uint32_t smask[32];
+  grid_dependency_wait();    // the partial pass's results
+  grid_dependents_launch();  // the next call's compaction may start launching
+  const int G = kp.G, D = kp.D;
+  const int gs = wph * 32;                 // threads per query head
+  const int hgrp = threadIdx.x / gs;       // query head within the KV group
+  const int th = threadIdx.x - hgrp * gs;  // thread within the head's group
+  const int lane = threadIdx.x & 31, wsub = th >> 5;
+  const int bar_id = 1 + hgrp;
+  // Shared memory: keys [G][npad_max] u64 | scratch [G][wph][D + 2] f32.
+  uint64_t* keys = reinterpret_cast<uint64_t*>(fsm) + (size_t)hgrp * npad_max;
+  float* scratch = reinterpret_cast<float*>(fsm + (size_t)G * npad_max * 8) +
+                   (size_t)hgrp * wph * (D + 2);
+
+  const int rg = blockIdx.x;
+  const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
+  const int h = g * G + hgrp;
+  const int L = clamp_len(seq_lens[r], kp.cap_tokens);
+  const int mode = modes[r];
+  const int dpl = D >> 5;  // 2 or 4 dims per lane
+  T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+
+  const int4 hi = ws.head_info[rg];
+  if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
+    if (wsub == 0) {
+      if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
+      else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
+      if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
+    }
+    return;
+  }
+
+  // ---- merge the block ranges' partial results
+  const float2* ml = ws.partial_ml + (size_t)hi.x * G + hgrp;  // slot s at ml[s * G]
+  const float* acc = ws.partial_acc + ((size_t)hi.x * G + hgrp) * D + lane * dpl;
+  const int n = hi.y;
+  float M = -INFINITY;
+  for (int s = th; s < n; s += gs) {
+    const float2 t = ml[(size_t)s * G];
+    if (t.y > 0.f) M = fmaxf(M, t.x);
+  }
+  M = group_max(M, th, wph, scratch, bar_id);
+  float lam = 0.f;
+  for (int s0 = wsub; s0 < n; s0 += 4 * wph) {
+    float2 t[4];
+    float4 a[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * wph;
+      const bool in = s < n;
+      t[u] = in ? ml[(size_t)s * G] : make_float2(-INFINITY, 0.f);
+      const float* ap = acc + (size_t)(in ? s : 0) * G * D;
+      a[u] = dpl == 4 ? *reinterpret_cast<const float4*>(ap) : make_float4(ap[0], ap[1], 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool used = t[u].y > 0.f;  // an empty range's accumulator is never used
+      const float w = used ? exp2f(t[u].x - M) : 0.f;
+      lam = fmaf(t[u].y, w, lam);
+      o[0] += used ? a[u].x * w : 0.f;
+      o[1] += used ? a[u].y * w : 0.f;
+      o[2] += used ? a[u].z * w : 0.f;
+      o[3] += used ? a[u].w * w : 0.f;
+    }
+  }
+  if (wph > 1) {
+    // Sum the group's warps (every warp forms the same totals).
+    float* mine = scratch + wsub * (D + 2);
+    if (lane == 0) mine[D] = lam;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < dpl) mine[lane * dpl + j] = o[j];
+    group_sync(bar_id, gs);
+    lam = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = 0.f;
+    for (int w = 0; w < wph; ++w) {
+      const float* part = scratch + w * (D + 2);
+      lam += part[D];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < dpl) o[j] += part[lane * dpl + j];
+    }
+    group_sync(bar_id, gs);
+  }
+  const float lse2 = M + log2f(lam);
+  if (wsub == 0) {
+    const float inv = 1.f / lam;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] *= inv;
+    if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
+    else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
+    if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
+  }
+
+  if ((mode != WISE_MODE_DISCOVER && mode != WISE_MODE_DISCOVER_UNION) || support == nullptr) return;
+
+  // ---- eta selection for this query head
+  if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
+  __syncthreads();
+  const int nb = (L + kTile - 1) / kTile;
+  int npad = 32;
+  while (npad < nb) npad <<= 1;
+  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
+  for (int i = th; i < npad; i += gs) {
+    uint64_t key = ~0ull;
+    if (i < nb) {
+      const float2 t = ts[i];
+      const float p = t.y * exp2f(t.x - lse2);
+      key = ((uint64_t)(~__float_as_uint(p)) << 32) | (uint32_t)i;
+    }
+    keys[i] = key;
+  }
+  group_sync(bar_id, gs);
+  for (int k = 2; k <= npad; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int idx = th; idx < (npad >> 1); idx += gs) {
+        const int i = ((idx & ~(j - 1)) << 1) | (idx & (j - 1));  // lower element of the pair
+        const uint64_t a = keys[i], b = keys[i + j];
+        const bool up = (i & k) == 0;
+        if ((a > b) == up) {
+          keys[i] = b;
+          keys[i + j] = a;
+        }
+      }
+      group_sync(bar_id, gs);
+    }
+  }
+  // Thread th owns sorted positions [th * c, th * c + c), c <= 8 (npad <= 64
+  // with one warp per head, npad <= 1024 with four).
+  const int c = npad >= gs ? npad / gs : 1;
+  float pm[8];
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = th * c + e;
+    const bool ok = e < c && i < npad && keys[i] != ~0ull;
+    pm[e] = ok ? __uint_as_float(~(uint32_t)(keys[i] >> 32)) : 0.f;
+    mine += pm[e];
+  }
+  float before = group_exclusive_scan(mine, th, wph, scratch, bar_id);
+  const bool all = kp.eta >= 1.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = th * c + e;
+    if (e < c && i < npad) {
+      const uint64_t key = keys[i];
+      if (key != ~0ull && (all || before < kp.eta)) {
+        const uint32_t b = (uint32_t)key;
+        atomicOr(&smask[b >> 5], 1u << (b & 31));
+      }
+    }
+    before += pm[e];
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < kp.W) {
+    const int t = threadIdx.x;
+    const int lo = t * 32;
+    const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
+    uint32_t* word = support + (size_t)rg * kp.W + t;
+    uint32_t w = smask[t] & valid;
+    if (mode == WISE_MODE_DISCOVER_UNION) w |= *word & valid;
+    *word = w;
+  }
+}
+
+// ------------------------------------------------------------------ short rows
+// Rows of at most 64 blocks and 8 split slots: one warp per query head, the
+// merge in each lane over all slots (broadcast loads), and the sort in
+// registers with shuffles (E keys per lane, lane-major blocks).
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
   uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, o);
   uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), o);
@@ -64,12 +287,9 @@ __device__ __forceinline__ void warp_bitonic_sort(uint64_t (&key)[E], int lane) 
   }
 }
 
-// Eta selection of one (row, query head): marks the kept blocks in smask.
-// Not inlined: the unrolled network is large and does not depend on the
-// element type, head dim or group size of the calling kernel.
 template <int E>
-__device__ __noinline__ void select_blocks(const float2* __restrict__ ts, int nb, float lse2,
-                                              float eta, uint32_t* smask, int lane) {
+__device__ __forceinline__ void warp_select(const float2* __restrict__ ts, int nb, float lse2,
+                                            float eta, uint32_t* smask, int lane) {
   constexpr uint64_t kPad = ~0ull;
   uint64_t key[E];
 #pragma unroll
@@ -84,7 +304,6 @@ __device__ __noinline__ void select_blocks(const float2* __restrict__ ts, int nb
     }
   }
   warp_bitonic_sort<E>(key, lane);
-
   float pm[E];
   float tot = 0.f;
 #pragma unroll
@@ -92,7 +311,6 @@ __device__ __noinline__ void select_blocks(const float2* __restrict__ ts, int nb
     pm[e] = key[e] == kPad ? 0.f : __uint_as_float(~(uint32_t)(key[e] >> 32));
     tot += pm[e];
   }
-  // Exclusive scan of the lane totals: mass of every earlier lane's keys.
   float incl = tot;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -112,14 +330,11 @@ __device__ __noinline__ void select_blocks(const float2* __restrict__ ts, int nb
   }
 }
 
-// One CTA per (row, KV head) with one warp per query head of the group; the
-// head dim (64 or 128) and group size are runtime values: the merge is a few
-// loads per item, so only the element type is a template parameter.
 template <typename T>
 __global__ void __launch_bounds__(256)
-    finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                  const WsView ws, const KParams kp, uint32_t* __restrict__ support,
-                  T* __restrict__ out, float* __restrict__ lse) {
+    finish_short_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
+                        const WsView ws, const KParams kp, uint32_t* __restrict__ support,
+                        T* __restrict__ out, float* __restrict__ lse) {
   __shared__ uint32_t smask[32];
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
@@ -127,13 +342,12 @@ __global__ void __launch_bounds__(256)
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G = kp.G, D = kp.D;
-  const int dpl = D >> 5;  // 2 or 4 dims per lane
+  const int dpl = D >> 5;
   const int h = g * G + warp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
   const int mode = modes[r];
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
-
   const int4 hi = ws.head_info[rg];
   if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
     if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
@@ -141,18 +355,17 @@ __global__ void __launch_bounds__(256)
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
     return;
   }
-
   const float2* ml = ws.partial_ml;
   float M = -INFINITY;
-  // hi.x = first partial slot of this (row, KV head) (rg * S_max); its hi.y
-  // block ranges occupy the next slots (an empty range of a sparse row
-  // holds (-inf, 0) and is skipped).
-  for (int i = 0; i < hi.y; ++i) M = fmaxf(M, ml[(size_t)(hi.x + i) * G + warp].x);
+  for (int i = 0; i < hi.y; ++i) {
+    const float2 t = ml[(size_t)(hi.x + i) * G + warp];
+    if (t.y > 0.f) M = fmaxf(M, t.x);
+  }
   float lam = 0.f;
   for (int i = 0; i < hi.y; ++i) {
     const size_t idx = (size_t)(hi.x + i) * G + warp;
     const float2 t = ml[idx];
-    if (!(t.y > 0.f)) continue;
+    if (!(t.y > 0.f)) continue;  // an empty range of a sparse row
     const float w = exp2f(t.x - M);
     lam = fmaf(t.y, w, lam);
     const float* a = ws.partial_acc + idx * D + lane * dpl;
@@ -174,17 +387,12 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
 
   if ((mode != WISE_MODE_DISCOVER && mode != WISE_MODE_DISCOVER_UNION) || support == nullptr) return;
-
   if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
   __syncthreads();
   const int nb = (L + kTile - 1) / kTile;
   const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
-  if (nb <= 32) select_blocks<1>(ts, nb, lse2, kp.eta, smask, lane);
-  else if (nb <= 64) select_blocks<2>(ts, nb, lse2, kp.eta, smask, lane);
-  else if (nb <= 128) select_blocks<4>(ts, nb, lse2, kp.eta, smask, lane);
-  else if (nb <= 256) select_blocks<8>(ts, nb, lse2, kp.eta, smask, lane);
-  else if (nb <= 512) select_blocks<16>(ts, nb, lse2, kp.eta, smask, lane);
-  else select_blocks<32>(ts, nb, lse2, kp.eta, smask, lane);
+  if (nb <= 32) warp_select<1>(ts, nb, lse2, kp.eta, smask, lane);
+  else warp_select<2>(ts, nb, lse2, kp.eta, smask, lane);
   __syncthreads();
   if ((int)threadIdx.x < kp.W) {
     const int t = threadIdx.x;
@@ -197,17 +405,54 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Warps per query head: one for short rows, four when a row can have many
+// split slots or blocks to sort.
+static int finish_wph(const KParams& kp) { return (kp.S_max > 8 || kp.max_blocks > 64) ? 4 : 1; }
+
+static int finish_npad(const KParams& kp) {
+  int n = 32;
+  while (n < kp.max_blocks) n <<= 1;
+  return n;
+}
+
+template <typename T>
+static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
+                                   const int32_t* seq_lens, const WsView& ws, uint32_t* support,
+                                   void* out, float* lse, cudaStream_t stream) {
+  const int wph = finish_wph(kp);
+  if (wph == 1)
+    return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
+                      modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
+  const int npad = finish_npad(kp);
+  const size_t smem = (size_t)kp.G * npad * 8 + (size_t)kp.G * wph * (kp.D + 2) * 4;
+  // The shared-memory opt-in is set once per device (so a call inside a
+  // stream capture issues only the launch).
+  static std::mutex mu;
+  static size_t configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured[dev] < smem) {
+      e = cudaFuncSetAttribute(finish_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+      configured[dev] = smem;
+    }
+  }
+  return launch_pdl(finish_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G * wph), smem, stream,
+                    modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse, wph, npad);
+}
+
 cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,
                           const int32_t* seq_lens, const WsView& ws, uint32_t* support,
                           void* out, float* lse, cudaStream_t stream) {
   if (kp.R == 0) return cudaSuccess;
-  const int grid = kp.R * kp.Hkv;
-  const int threads = 32 * kp.G;
   if (dtype == WISE_DTYPE_BF16)
-    return launch_pdl(finish_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, stream, modes,
-                      seq_lens, ws, kp, support, static_cast<__nv_bfloat16*>(out), lse);
-  return launch_pdl(finish_kernel<float>, dim3(grid), dim3(threads), 0, stream, modes, seq_lens,
-                    ws, kp, support, static_cast<float*>(out), lse);
+    return launch_finish_t<__nv_bfloat16>(kp, modes, seq_lens, ws, support, out, lse, stream);
+  return launch_finish_t<float>(kp, modes, seq_lens, ws, support, out, lse, stream);
 }
 
 }  // namespace wise

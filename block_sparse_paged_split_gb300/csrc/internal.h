@@ -10,8 +10,7 @@ namespace wise {
 // Launchers (host).  Each enqueues one kernel on `stream` and returns the
 // launch status; none allocates or synchronises.
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const int32_t* page_table, const WsView& ws,
-                           cudaStream_t stream);
+                           const uint32_t* support, const WsView& ws, cudaStream_t stream);
 
 cudaError_t launch_partial_bf16(const KParams& kp, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const void* q, const int32_t* page_table, const int32_t* seq_lens,

@@ -10,15 +10,17 @@
 //   * C consumer warps, each owning an S-deep ring of shared-memory stages;
 //     one stage holds one 32-token tile of K and of V (and, for the first tile
 //     of a work item, the item's query rows).
-//   * One producer warp.  Its lane c feeds consumer c: it takes the next work
-//     item from the largest-first schedule through an atomic counter (one
-//     self-contained record per item, fetched an item ahead), reads the tile
-//     list and page table two tiles ahead, writes a small descriptor into the stage,
-//     and issues one TMA bulk-tensor copy per page and cache (box = one page of
-//     one KV head) plus a bulk copy of q, all completing on the stage's "full"
-//     mbarrier.  Consumers release a stage through its "empty" mbarrier.  The
-//     producer polls with non-blocking tests, so one lane's wait never holds
-//     another consumer's refill; consumers never wait on a global load.
+//   * One producer warp per consumer (one active lane).  It takes the next
+//     work item from the largest-first schedule through an atomic counter
+//     (one self-contained record per item, its tiles as a bitmap over its
+//     block range, claimed shortly before it is needed), reads the page
+//     table a tile ahead, writes a small
+//     descriptor into the stage, and issues one TMA bulk-tensor copy per page
+//     and cache (box = one page of one KV head) plus a bulk copy of q, all
+//     completing on the stage's "full" mbarrier.  Consumers release a stage
+//     through its "empty" mbarrier; the producer waits on it with a
+//     suspending try_wait, so it costs no issue slots while idle and
+//     consumers never wait on a global load.
 //   * Math is FP32 FMA: multi-head decode reads each K/V element once (about
 //     one FMA per byte, far below the tensor-core ridge).  Lane l holds dims
 //     [l*DPL, (l+1)*DPL) of the query; lane l computes token (i XOR l) at
@@ -33,6 +35,7 @@
 #pragma once
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -46,8 +49,8 @@ struct StageDesc {
   int rg;     // row * Hkv + kv head
 };
 
-// A tile the producer lane has prepared: its stage descriptor, the page ids
-// of its (one or two) pages, and where its query rows live.
+// A tile the producer has prepared: its stage descriptor, the page ids of
+// its (one or two) pages, and where its query rows live.
 struct Prepared {
   StageDesc d;
   int pages[2];
@@ -55,21 +58,34 @@ struct Prepared {
   bool ok;
 };
 
+// The tensor-core path (bf16 K/V with 2, 4 or 8 query heads per KV head).
+template <typename T, int G>
+struct UseMma {
+  static constexpr bool value = std::is_same<T, __nv_bfloat16>::value && G >= 2;
+};
+
 template <typename T, int D, int G, int C, int S>
 struct PartialCfg {
+  static constexpr bool MMA = UseMma<T, G>::value;
   static constexpr int DPL = D / 32;
   static constexpr int ROW_BYTES = D * (int)sizeof(T);
   static constexpr int TILE_BYTES = kTile * ROW_BYTES;
   static constexpr int Q_BYTES = G * ROW_BYTES;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES + ((Q_BYTES + 127) / 128) * 128;
+  // Stages are 1024-byte aligned on the tensor-core path (the 128-byte TMA
+  // swizzle repeats every 1024 bytes).
+  static constexpr int STAGE_ALIGN = MMA ? 1024 : 128;
+  static constexpr int STAGE_BYTES =
+      ((2 * TILE_BYTES + Q_BYTES + STAGE_ALIGN - 1) / STAGE_ALIGN) * STAGE_ALIGN;
   static constexpr int RING_BYTES = S * STAGE_BYTES;
   static constexpr int DESC_BYTES = S * (int)sizeof(StageDesc);
   static constexpr int BAR_BYTES = 2 * S * 8;  // full[S], empty[S]
-  static constexpr int PBUF_BYTES = G * kTile * 4;
-  static constexpr int EXTRA_BYTES = ((DESC_BYTES + BAR_BYTES + PBUF_BYTES + 127) / 128) * 128;
+  // FMA path: fp32 probabilities per head; tensor-core path: bf16 P[8][32].
+  static constexpr int PBUF_BYTES = MMA ? 8 * kTile * 2 : G * kTile * 4;
+  static constexpr int EXTRA_BYTES =
+      ((DESC_BYTES + BAR_BYTES + PBUF_BYTES + STAGE_ALIGN - 1) / STAGE_ALIGN) * STAGE_ALIGN;
   static constexpr int CONSUMER_BYTES = RING_BYTES + EXTRA_BYTES;
   static constexpr int SMEM_BYTES = C * CONSUMER_BYTES;
-  static constexpr int THREADS = (C + 1) * 32;
+  static constexpr int THREADS = 2 * C * 32;  // C consumer warps, C producer warps
 };
 
 // Launch shape per element type and head dim: two stages per consumer and as
@@ -179,8 +195,201 @@ struct QRegs<float, DPL> {
   }
 };
 
+// ---------------------------------------------------------------- tensor cores
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// c += a * b, m16n8k16, bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared-memory address of the 16-byte chunk `chunk` (0..7) of token row
+// `tok` in 128-byte half row `half` of a swizzled tile (the TMA 128-byte
+// swizzle XORs the chunk index with the row index modulo 8).
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int half, int tok, int chunk) {
+  return tile + half * (kTile * 128) + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+}
+
+// Consumer of the tensor-core path: a query-head group (G = 2, 4 or 8)
+// against one 32-token tile is a small dense contraction.  Scores are
+// S^T = K Q^T (m16n8k16: 16 tokens x 8 head columns x 16 dims; tokens as M
+// so the group of G <= 8 heads fills N), the output is O^T = V^T P^T with
+// P rounded to bf16 in shared memory (fp32 accumulators throughout; the
+// exp-sums and per-tile statistics use the fp32 probabilities).  Lane
+// (g8, q4) = (lane / 4, lane % 4) holds heads 2 q4 and 2 q4 + 1 of tokens
+// g8 (+8) of each 16-token half, and dims g8 (+8) of each 16-dim block of O^T.
+template <int D, int G, int S, typename Cfg>
+__device__ __forceinline__ void mma_consume(const WsView& ws, const KParams& kp, uint8_t* ring_base,
+                                            const StageDesc* descs, uint32_t full0,
+                                            uint32_t empty0, uint16_t* ps, int lane) {
+  constexpr int KS = D / 16;  // 16-dim blocks: k-steps of S^T, m-tiles of O^T
+  const int g8 = lane >> 2, q4 = lane & 3;
+  const bool hv[2] = {2 * q4 < G, 2 * q4 + 1 < G};
+  uint32_t qb[KS][2];
+  float o[KS][4];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_lane[2] = {0.f, 0.f};
+  for (int i = lane; i < 8 * kTile; i += 32) ps[i] = 0;  // padding heads stay 0
+  __syncwarp();
+  uint32_t seq = 0;
+  while (true) {
+    const int stage = seq % S;
+    if (!mbar_wait(full0 + 8 * stage, (seq / S) & 1)) {
+      if (lane == 0) flag_error(ws.status, WISE_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    const StageDesc d = descs[stage];
+    if (d.item < 0) break;
+    uint8_t* kt = ring_base + stage * Cfg::STAGE_BYTES;
+    const uint32_t kb = smem_u32(kt);
+    const uint32_t vb = kb + Cfg::TILE_BYTES;
+    const int n_valid = d.info & 255;
+    const bool disc = (d.info & 1024) != 0;
+    if (d.info & 256) {
+      const uint8_t* qrow = kt + 2 * Cfg::TILE_BYTES + g8 * Cfg::ROW_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[ks][0] = g8 < G ? *reinterpret_cast<const uint32_t*>(qrow + (16 * ks + 2 * q4) * 2) : 0u;
+        qb[ks][1] = g8 < G ? *reinterpret_cast<const uint32_t*>(qrow + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) o[ks][v] = 0.f;
+      }
+      m_run[0] = m_run[1] = -INFINITY;
+      l_lane[0] = l_lane[1] = 0.f;
+    }
+    if (n_valid < kTile) {
+      // Last tile of the row: V rows past the length may hold anything (even
+      // NaN) and P . V multiplies every row, so zero them.
+      for (int i = lane; i < (kTile - n_valid) * (D / 8); i += 32) {
+        const int tok = n_valid + i / (D / 8), c = i % (D / 8);
+        *reinterpret_cast<uint4*>(kt + Cfg::TILE_BYTES + (c >> 3) * (kTile * 128) + tok * 128 + (c & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // S^T = K Q^T
+    float sc[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) sc[mt][v] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int m = lane >> 3;
+        const int tok = 16 * mt + (m & 1) * 8 + (lane & 7);
+        uint32_t a[4];
+        ldsm_x4(swz(kb, ks >> 2, tok, (ks & 3) * 2 + (m >> 1)), a);
+        mma_bf16(sc[mt], a, qb[ks][0], qb[ks][1]);
+      }
+    }
+
+    // Online softmax per head column (all lanes shuffle; padding heads do
+    // not update any state).
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float sv[4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = 16 * mt + g8 + 8 * i;
+          sv[2 * mt + i] = tok < n_valid ? sc[mt][2 * i + j] * kp.scale_log2 : -INFINITY;
+        }
+      float lm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) lm = fmaxf(lm, __shfl_xor_sync(kFull, lm, o2));
+      if (disc) {
+        float e = fast_exp2(sv[0] - lm) + fast_exp2(sv[1] - lm) + fast_exp2(sv[2] - lm) +
+                  fast_exp2(sv[3] - lm);
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) e += __shfl_xor_sync(kFull, e, o2);
+        if (g8 == 0 && hv[j])
+          ws.tile_stats[(size_t)(d.rg * G + 2 * q4 + j) * kp.max_blocks + d.tile] = make_float2(lm, e);
+      }
+      uint16_t* prow = ps + (2 * q4 + j) * kTile;
+      if (hv[j]) {
+        const float m_new = fmaxf(m_run[j], lm);
+        const float alpha = fast_exp2(m_run[j] - m_new);
+        float lsum = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float pv = fast_exp2(sv[2 * mt + i] - m_new);
+            lsum += pv;
+            prow[16 * mt + g8 + 8 * i] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+          }
+        l_lane[j] = fmaf(l_lane[j], alpha, lsum);
+        m_run[j] = m_new;
+#pragma unroll
+        for (int md = 0; md < KS; ++md) {
+          o[md][j] *= alpha;
+          o[md][2 + j] *= alpha;
+        }
+      }
+    }
+    __syncwarp();
+
+    // O^T += V^T P^T
+    uint32_t pb[2][2];
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      pb[k2][0] = *reinterpret_cast<const uint32_t*>(ps + g8 * kTile + 16 * k2 + 2 * q4);
+      pb[k2][1] = *reinterpret_cast<const uint32_t*>(ps + g8 * kTile + 16 * k2 + 8 + 2 * q4);
+    }
+#pragma unroll
+    for (int md = 0; md < KS; ++md) {
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int m = lane >> 3;
+        const int tok = 16 * k2 + 8 * (m >> 1) + (lane & 7);
+        const int d0 = 16 * md + 8 * (m & 1);
+        uint32_t a[4];
+        ldsm_x4_trans(swz(vb, d0 >> 6, tok, (d0 & 63) >> 3), a);
+        mma_bf16(o[md], a, pb[k2][0], pb[k2][1]);
+      }
+    }
+
+    if (d.info & 512) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float l_tot = l_lane[j];
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) l_tot += __shfl_xor_sync(kFull, l_tot, o2);
+        if (g8 == 0 && hv[j]) ws.partial_ml[(size_t)d.item * G + 2 * q4 + j] = make_float2(m_run[j], l_tot);
+      }
+#pragma unroll
+      for (int md = 0; md < KS; ++md)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int hh = 2 * q4 + (v & 1);
+          if (hh < G)
+            ws.partial_acc[((size_t)d.item * G + hh) * D + 16 * md + g8 + (v >= 2 ? 8 : 0)] = o[md][v];
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    ++seq;
+  }
+}
+
 template <typename T, int D, int G, int C, int S>
-__global__ void __launch_bounds__((C + 1) * 32, 1)
+__global__ void __launch_bounds__(2 * C * 32, 1)
     partial_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const T* __restrict__ q, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int8_t* __restrict__ modes,
@@ -202,7 +411,9 @@ __global__ void __launch_bounds__((C + 1) * 32, 1)
   };
   auto empty_bar = [&](int c, int s) { return full_bar(c, 0) + 8 * (S + s); };
 
+  __shared__ int cta_done;  // producers of this CTA past the queue
   if (threadIdx.x == 0) {
+    cta_done = 0;
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     for (int c = 0; c < C; ++c)
@@ -217,156 +428,147 @@ __global__ void __launch_bounds__((C + 1) * 32, 1)
 
   const int n_items = *ws.num_items;
 
-  if (warp == C) {
-    // ------------------------------------------------------------ producer
-    // Lane c serves consumer c.  It holds the next work item's record (loaded
-    // as soon as the current item starts) and up to two tiles prepared ahead
-    // (descriptor and page ids, whose loads overlap the wait for a free
-    // stage), so a stage that frees gets its copies issued at once.
-    const bool active = lane < C;
-    const int c = lane;
+  if (warp >= C) {
+    // ------------------------------------------------------------ producers
+    // Warp C + c feeds consumer c; one lane does the work.  It holds the next
+    // work item's record (claimed when the current item is about to run out)
+    // and the next tile prepared (descriptor and page ids), so a stage that
+    // frees gets its copies issued at once.  It waits for a free stage with a
+    // suspending try_wait, so an idle producer takes no issue slots.
+    if (lane != 0) return;
+    const int c = warp - C;
     uint32_t seq = 0;
-    bool exhausted = !active, posted_done = !active;
+    bool exhausted = false, first_claim = true;
     int4 nxt = make_int4(0, 0, 0, 0), cur = make_int4(0, 0, 0, 0);
     bool nxt_ok = false, cur_ok = false;
     int k = 0;
-    Prepared p0{}, p1{};
-    uint64_t idle_since = 0;
+    Prepared p{};
     // Each consumer's first item is its own schedule slot (no atomic on the
     // launch's critical path); later ones come from the counter, offset by
     // the number of consumers in the grid.
     const int n_consumers = gridDim.x * C;
-    bool first_claim = true;
+    bool timed_out = false;
     while (true) {
-      bool progressed = false;
-      if (!posted_done) {
-        if (!cur_ok && nxt_ok) {
-          cur = nxt;
-          cur_ok = true;
-          nxt_ok = false;
-          k = 0;
-        }
-        // Claim the next item only when the current one is about to run out
-        // (two tiles left to prepare): claiming earlier would hoard items
-        // other consumers could start sooner.
-        if (!nxt_ok && !exhausted && (!cur_ok || (cur.z & 0xff) - k <= 2)) {
-          const int slot = first_claim ? blockIdx.x * C + c : n_consumers + atomicAdd(ws.queue, 1);
-          first_claim = false;
-          if (slot < n_items) {
-            nxt = ws.items[slot];
-            nxt_ok = true;
-          } else {
-            exhausted = true;
-          }
-        }
-        if (cur_ok && !p1.ok) {
-          // Prepare tile k of the current item into p1.
-          const int rg = cur.x;
-          const int ntiles = cur.z & 0xff;
-          const int row = rg / kp.Hkv;
-          int b;
-          if (cur.z & kItemSparse) {
-            // One load: the compacted tile with its page ids.
-            const int4 t = ws.tile_list[(size_t)rg * kp.max_blocks + cur.y + k];
-            b = t.x;
-            p1.pages[0] = t.y;
-            p1.pages[1] = t.z;
-          } else {
-            b = cur.y + k;
-            const int32_t* pt = page_table + (size_t)row * kp.max_pages + b * (kTile / kp.P);
-            const bool two = kp.P * 2 == kTile && b * kTile + kp.P < cur.w;
-            p1.pages[0] = pt[0];
-            p1.pages[1] = two ? pt[1] : 0;
-          }
-          const int tok0 = b * kTile;
-          const int rem = cur.w - tok0;
-          const int pages_in_tile = kTile / kp.P;
-          int npg = (rem + kp.P - 1) / kp.P;
-          npg = npg < pages_in_tile ? npg : pages_in_tile;
-          p1.npg = npg;
-          p1.row = row;
-          p1.head = rg - row * kp.Hkv;
-          p1.d.item = rg * kp.S_max + ((cur.z >> 8) & 0xffff);
-          p1.d.tile = b;
-          p1.d.info = (rem < kTile ? rem : kTile) | (k == 0 ? 256 : 0) | (k + 1 == ntiles ? 512 : 0) |
-                      ((cur.z & kItemDiscover) ? 1024 : 0);
-          p1.d.rg = rg;
-          p1.ok = true;
-          if (++k == ntiles) cur_ok = false;
-          if (!p0.ok) {
-            p0 = p1;
-            p1.ok = false;
-          }
-        }
-        const bool all_out = !p0.ok && !cur_ok && !nxt_ok && exhausted;
-        if (p0.ok || all_out) {
-          const int stage = seq % S;
-          if (mbar_test_wait(empty_bar(c, stage), ((seq / S) & 1) ^ 1)) {
-            StageDesc* d = descs(c) + stage;
-            const uint32_t fb = full_bar(c, stage);
-            if (p0.ok) {
-              *d = p0.d;
-              const bool first = (p0.d.info & 256) != 0;
-              mbar_arrive_expect_tx(fb, (uint32_t)(2 * p0.npg * kp.P * Cfg::ROW_BYTES) +
-                                            (first ? (uint32_t)Cfg::Q_BYTES : 0u));
-              const uint32_t kdst = smem_u32(ring(c) + stage * Cfg::STAGE_BYTES);
-#pragma unroll
-              for (int pp = 0; pp < 2; ++pp) {
-                if (pp < p0.npg) {
-                  const int page = p0.pages[pp];
-                  // A page id outside the pool reads the out-of-bounds fill (zeros).
-                  const int tok = (page >= 0 && page < kp.num_pages) ? page * kp.P : kp.num_pages * kp.P;
-                  const uint32_t off = pp * kp.P * Cfg::ROW_BYTES;
-                  tma_load_3d(kdst + off, &tmK, 0, p0.head, tok, fb);
-                  tma_load_3d(kdst + Cfg::TILE_BYTES + off, &tmV, 0, p0.head, tok, fb);
-                }
-              }
-              if (first)
-                bulk_load(kdst + 2 * Cfg::TILE_BYTES, q + ((size_t)p0.row * kp.Hq + p0.head * G) * D,
-                          Cfg::Q_BYTES, fb);
-              ++seq;
-              p0 = p1;
-              p1.ok = false;
-            } else {
-              d->item = -1;
-              mbar_arrive(fb);
-              posted_done = true;
-            }
-            progressed = true;
-          }
-        }
+      if (!cur_ok && nxt_ok) {
+        cur = nxt;
+        cur_ok = true;
+        nxt_ok = false;
+        k = 0;
       }
-      if (__all_sync(kFull, posted_done)) {
-        // Every lane of this CTA is past the queue.  The last CTA to get here
-        // puts the counter back to 0, so a later partial launch over the
-        // same compaction (the next depth reusing a mask) starts afresh.
-        if (lane == 0) {
-          grid_dependents_launch();  // the finish pass may start launching
-          __threadfence();
-          if (atomicAdd(ws.queue_done, 1) == (int)gridDim.x - 1) {
-            __threadfence();
-            atomicExch(ws.queue, 0);
-            atomicExch(ws.queue_done, 0);
-          }
+      // Claim the next item only when the current one is about to run out
+      // (two tiles left to prepare): claiming earlier would hoard items other
+      // consumers could start sooner.
+      if (!nxt_ok && !exhausted && (!cur_ok || ((cur.z >> 16) & 0xff) - k <= 2)) {
+        const int slot = first_claim ? blockIdx.x * C + c : n_consumers + atomicAdd(ws.queue, 1);
+        first_claim = false;
+        if (slot < n_items) {
+          nxt = ws.items[slot];
+          nxt_ok = true;
+        } else {
+          exhausted = true;
         }
+        if (!cur_ok && nxt_ok) continue;  // start on it right away
+      }
+      if (cur_ok && !p.ok) {
+        // Prepare tile k of the current item: the k-th set bit of its range
+        // bitmap, and the page ids of its one or two pages.
+        const int rg = cur.x;
+        const int ntiles = (cur.z >> 16) & 0xff;
+        const int L = cur.w & kItemLenMask;
+        const int row = rg / kp.Hkv;
+        const int b = cur.y * kp.T + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 1);
+        {
+          const int32_t* pt = page_table + (size_t)row * kp.max_pages + b * (kTile / kp.P);
+          const bool two = kp.P * 2 == kTile && b * kTile + kp.P < L;
+          p.pages[0] = pt[0];
+          p.pages[1] = two ? pt[1] : 0;
+        }
+        const int tok0 = b * kTile;
+        const int rem = L - tok0;
+        const int pages_in_tile = kTile / kp.P;
+        int npg = (rem + kp.P - 1) / kp.P;
+        p.npg = npg < pages_in_tile ? npg : pages_in_tile;
+        p.row = row;
+        p.head = rg - row * kp.Hkv;
+        p.d.item = rg * kp.S_max + cur.y;
+        p.d.tile = b;
+        p.d.info = (rem < kTile ? rem : kTile) | (k == 0 ? 256 : 0) | (k + 1 == ntiles ? 512 : 0) |
+                   ((cur.w & kItemDiscover) ? 1024 : 0);
+        p.d.rg = rg;
+        p.ok = true;
+        if (++k == ntiles) cur_ok = false;
+      }
+      if (!p.ok && (cur_ok || nxt_ok || !exhausted)) continue;
+      // Wait for the stage (bounded), then issue the prepared tile or, with
+      // nothing left, the end marker.
+      const int stage = seq % S;
+      if (!mbar_wait(empty_bar(c, stage), ((seq / S) & 1) ^ 1)) {
+        flag_error(ws.status, WISE_DEVERR_WAIT_TIMEOUT);
+        timed_out = true;
         break;
       }
-      if (__any_sync(kFull, progressed)) {
-        idle_since = 0;
-      } else {
-        const uint64_t now = global_ns();
-        if (idle_since == 0) idle_since = now;
-        if (now - idle_since > kWaitLimitNs) {
-          flag_error(ws.status, WISE_DEVERR_WAIT_TIMEOUT);
-          break;
+      StageDesc* d = descs(c) + stage;
+      const uint32_t fb = full_bar(c, stage);
+      if (!p.ok) {
+        d->item = -1;
+        mbar_arrive(fb);
+        break;
+      }
+      *d = p.d;
+      const bool first = (p.d.info & 256) != 0;
+      mbar_arrive_expect_tx(fb, (uint32_t)(2 * p.npg * kp.P * Cfg::ROW_BYTES) +
+                                    (first ? (uint32_t)Cfg::Q_BYTES : 0u));
+      const uint32_t kdst = smem_u32(ring(c) + stage * Cfg::STAGE_BYTES);
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        if (pp < p.npg) {
+          const int page = p.pages[pp];
+          // A page id outside the pool reads the out-of-bounds fill (zeros).
+          const int tok = (page >= 0 && page < kp.num_pages) ? page * kp.P : kp.num_pages * kp.P;
+          if constexpr (Cfg::MMA) {
+            // 64-element half rows with the 128-byte swizzle: half h of the
+            // tile is [32 tokens][128 B] at h * 4 KB.
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+              const uint32_t off = h * (kTile * 128) + pp * kp.P * 128;
+              tma_load_3d(kdst + off, &tmK, h * 64, p.head, tok, fb);
+              tma_load_3d(kdst + Cfg::TILE_BYTES + off, &tmV, h * 64, p.head, tok, fb);
+            }
+          } else {
+            const uint32_t off = pp * kp.P * Cfg::ROW_BYTES;
+            tma_load_3d(kdst + off, &tmK, 0, p.head, tok, fb);
+            tma_load_3d(kdst + Cfg::TILE_BYTES + off, &tmV, 0, p.head, tok, fb);
+          }
         }
-        __nanosleep(32);
+      }
+      if (first)
+        bulk_load(kdst + 2 * Cfg::TILE_BYTES, q + ((size_t)p.row * kp.Hq + p.head * G) * D,
+                  Cfg::Q_BYTES, fb);
+      ++seq;
+      p.ok = false;
+    }
+    // This CTA's last producer past the queue tells the grid; the last CTA
+    // puts the counter back to 0, so a later partial launch over the same
+    // compaction (the next depth reusing a mask) starts afresh.
+    if (!timed_out && atomicAdd(&cta_done, 1) == C - 1) {
+      grid_dependents_launch();  // the finish pass may start launching
+      __threadfence();
+      if (atomicAdd(ws.queue_done, 1) == (int)gridDim.x - 1) {
+        __threadfence();
+        atomicExch(ws.queue, 0);
+        atomicExch(ws.queue_done, 0);
       }
     }
     return;
   }
 
   // ------------------------------------------------------------ consumers
+  if constexpr (Cfg::MMA) {
+    mma_consume<D, G, S, Cfg>(
+        ws, kp, ring(warp), descs(warp), full_bar(warp, 0), empty_bar(warp, 0),
+        reinterpret_cast<uint16_t*>(ring(warp) + Cfg::RING_BYTES + Cfg::DESC_BYTES + Cfg::BAR_BYTES),
+        lane);
+  } else {
   const int c = warp;
   float* pbuf = reinterpret_cast<float*>(ring(c) + Cfg::RING_BYTES + Cfg::DESC_BYTES + Cfg::BAR_BYTES);
   QRegs<T, DPL> qr[G];
@@ -470,6 +672,7 @@ __global__ void __launch_bounds__((C + 1) * 32, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(c, stage));
     ++seq;
+  }
   }
 }
 

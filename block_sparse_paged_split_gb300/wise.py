@@ -54,7 +54,7 @@ class wise_shape(ctypes.Structure):
 
 class wise_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status_word", "num_items", "queue", "head_info", "tile_list", "items",
+        "status_word", "num_items", "queue", "head_info", "items",
         "partial_ml", "partial_acc", "tile_stats", "max_items", "total_bytes")]
 
 
@@ -73,7 +73,7 @@ def library() -> ctypes.CDLL:
         sigs = {
             "wise_workspace_bytes": [S, ctypes.POINTER(ctypes.c_size_t)],
             "wise_workspace_layout": [S, ctypes.POINTER(wise_layout)],
-            "wise_compact_tiles": [S, P, P, P, P, P, SZ, P],
+            "wise_compact_tiles": [S, P, P, P, P, SZ, P],
             "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
             "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
@@ -152,12 +152,11 @@ def alloc_workspace(shape: wise_shape, device=None) -> torch.Tensor:
                        device=device or torch.device("cuda"))
 
 
-def wise_compact_tiles(shape, modes, seq_lens, support, page_table, workspace,
-                       stream=None) -> None:
+def wise_compact_tiles(shape, modes, seq_lens, support, workspace, stream=None) -> None:
     _check(library().wise_compact_tiles(
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
-        _ptr(support, torch.int32, "support"), _ptr(page_table, torch.int32, "page_table"),
-        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+        _ptr(support, torch.int32, "support"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
 
 
 def wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
@@ -233,7 +232,6 @@ def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, tor
         "status": region(lay["status_word"], 1, torch.int32),
         "num_items": region(lay["num_items"], 1, torch.int32),
         "head_info": region(lay["head_info"], R * Hkv * 4, torch.int32).view(R, Hkv, 4),
-        "tile_list": region(lay["tile_list"], R * Hkv * shape.max_blocks * 4, torch.int32).view(R, Hkv, shape.max_blocks, 4),
         "items": region(lay["items"], mi * 4, torch.int32).view(mi, 4),
         "queue": region(lay["queue"], 1, torch.int32),
         "partial_ml": region(lay["partial_ml"], mi * G * 2, torch.float32).view(mi, G, 2),

@@ -136,14 +136,11 @@ typedef struct {
                            the partial pass (both back to 0 after each pass) */
   size_t head_info;     /* int32x4 [R*Hkv]: first partial slot (rg * S),
                            block ranges, tiles, non-empty items                */
-  size_t tile_list;     /* int32x4 [R*Hkv, max_blocks]: sparse rows' tiles in
-                           ascending order: block, page of its first
-                           page_size tokens, page of the next (or 0), 0      */
   size_t items;         /* int32x4 [max_items], in schedule order (tile count
-                           descending): row*Hkv + KV head, first tile-list
-                           index (sparse) or first block, tile count |
-                           range s << 8 | sparse << 24 | discover << 25,
-                           sequence length                                     */
+                           descending): row*Hkv + KV head, block range s,
+                           tile bitmap (bit i: block s*T + i) | tile count
+                           << 16, sequence length | sparse << 24 |
+                           discover << 25                                      */
   size_t partial_ml;    /* float32x2 [max_items, G]: running max (log2 units)
                            and exp-sum per item and query head; range s of
                            (row, KV head) rg lives in slot rg * S + s, with
@@ -166,17 +163,18 @@ wise_status wise_workspace_layout(const wise_shape *shape,
 
 /* Compaction [WISE PR, "What changes": sparse rows are compacted first so
  * the loop has no branch; programs cover about eight tiles].  For each
- * (row, KV head): the tile list (ascending selected blocks below the row's
- * block count for sparse rows, each with its page ids; implicitly 0..n_b-1
- * for the other modes), cut in order into work items of at most
- * tiles_per_item tiles.  Reads modes, seq_lens and, for sparse rows, support
- * and page_table; writes the workspace (items, head info, tile lists) and
- * clears its status word.  The workspace must be 256-byte aligned and at
- * least wise_workspace_bytes long. */
+ * (row, KV head) and each range s of T = tiles_per_item blocks: a work item
+ * holding the range's tiles (every block below the row's block count for
+ * dense and discover rows, the selected ones for sparse rows; no item for an
+ * empty range) as a bitmap over the range, written in schedule order (tile
+ * count descending).  Reads modes, seq_lens and, for sparse rows, support;
+ * writes the workspace (items, head info) and clears its status word.  The
+ * workspace must be 256-byte aligned and at least wise_workspace_bytes
+ * long. */
 wise_status wise_compact_tiles(const wise_shape *shape, const int8_t *modes,
                                const int32_t *seq_lens, const uint32_t *support,
-                               const int32_t *page_table, void *workspace,
-                               size_t workspace_bytes, wise_stream_t stream);
+                               void *workspace, size_t workspace_bytes,
+                               wise_stream_t stream);
 
 /* Split partial pass [WISE PR, "What changes": split-KV paged decode with
  * per-row modes].  For every work item written by wise_compact_tiles and

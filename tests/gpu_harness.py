@@ -89,7 +89,7 @@ def gpu_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.num_rows, w.num_q_heads), dtype=torch.float32, device="cuda")
     if stepwise:
-        W.wise_compact_tiles(shape, modes_t, b.seq_lens, sup, b.page_table, ws)
+        W.wise_compact_tiles(shape, modes_t, b.seq_lens, sup, ws)
         W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
                               modes_t, ws)
         W.wise_decode_finish(shape, modes_t, b.seq_lens, ws, sup, out, lse)

@@ -48,7 +48,7 @@ def test_workspace_layout_is_aligned_and_sized(lib):
     s = _shape()
     lay = W.wise_workspace_layout(s)
     assert lay["total_bytes"] == W.wise_workspace_bytes(s)
-    offs = [lay[k] for k in ("head_info", "tile_list", "items", "partial_ml", "partial_acc", "tile_stats")]
+    offs = [lay[k] for k in ("head_info", "items", "partial_ml", "partial_acc", "tile_stats")]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
     # max items: every (row, KV head) split into ceil(max_blocks / 8) block
     # ranges (the default range is 8 blocks)
@@ -78,13 +78,13 @@ def test_host_checks_before_any_launch(lib):
     n = W.wise_workspace_bytes(s)
     P = ctypes.c_void_p
     # NULL workspace
-    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(16), None, n, None)
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, None, n, None)
     assert st == 3
     # misaligned workspace
-    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(16), P(4096 + 8), n, None)
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, P(4096 + 8), n, None)
     assert st == 3
-    # NULL page table
-    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), P(16), None, None, P(4096), n, None)
+    # NULL lengths
+    st = lib.wise_compact_tiles(ctypes.byref(s), P(16), None, None, P(4096), n, None)
     assert st == 1
     # workspace too small
     st = lib.wise_decode_partial(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),

@@ -97,9 +97,10 @@ def test_tiny_schedule_f32():
 
 
 def test_compaction_matches_oracle():
-    """Tile lists (with page ids), per-head counts and work items: bit-exact."""
+    """Work items (tiles as bitmaps over their block range) and per-head
+    counts, against the oracle's lists and items: bit-exact."""
     rng = np.random.default_rng(5)
-    for T in (1, 2, 4, 8):
+    for T in (1, 2, 4, 8, 16):
         lens = rng.integers(0, 700, size=9).astype(np.int32)
         w = _wl(4, 2, 64, "bf16", lens=lens, seed=9)
         R = w.num_rows
@@ -109,27 +110,25 @@ def test_compaction_matches_oracle():
         shape = shape_for(w, tiles_per_item=T)
         ws = W.alloc_workspace(shape)
         W.wise_compact_tiles(shape, torch.from_numpy(modes).cuda(), torch.from_numpy(lens).cuda(),
-                             dev_support(sup), torch.from_numpy(w.page_table).cuda(), ws)
+                             dev_support(sup), ws)
         torch.cuda.synchronize()
         v = {k: t.cpu().numpy() for k, t in W.workspace_views(shape, ws).items()}
         ref = O.compact_tiles(sup, modes, lens, 32, T)
         n = int(v["num_items"][0])
         assert n == ref["items"].shape[0]
         rec = v["items"][:n]
-        # Records are in schedule order: the tile counts never increase.
-        sizes = rec[:, 2] & 0xFF
-        assert np.all(np.diff(sizes) <= 0)
-        ranges = (rec[:, 2] >> 8) & 0xFFFF
-        # In canonical (row, KV head, range) order they are the oracle's items.
-        order = np.lexsort((ranges, rec[:, 0]))
-        canon, crange = rec[order], ranges[order]
-        mine = np.stack([canon[:, 0] // 2, canon[:, 0] % 2, crange, canon[:, 1], canon[:, 2] & 0xFF], 1)
-        assert np.array_equal(mine, ref["items"])
-        for row in canon:
-            r = row[0] // 2
-            assert bool(row[2] & (1 << 24)) == (modes[r] == W.MODE_SPARSE)
-            assert bool(row[2] & (1 << 25)) == (modes[r] in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION))
-            assert row[3] == lens[r]
+        counts = (rec[:, 2] >> 16) & 0xFF
+        assert np.all(np.diff(counts) <= 0)  # schedule order: tile count descending
+        canon = rec[np.lexsort((rec[:, 1], rec[:, 0]))]
+        for (rg, s_, z, wfield), (r, g, s_ref, first, cnt) in zip(canon, ref["items"]):
+            assert (rg, s_) == (r * 2 + g, s_ref)
+            bitmap = int(z) & 0xFFFF
+            tiles = [s_ * T + i for i in range(16) if bitmap >> i & 1]
+            assert len(tiles) == cnt == (int(z) >> 16) & 0xFF
+            assert tiles == ref["lists"][r][g][first:first + cnt].tolist()
+            assert (int(wfield) & 0xFFFFFF) == lens[r]
+            assert bool(wfield & (1 << 24)) == (modes[r] == W.MODE_SPARSE)
+            assert bool(wfield & (1 << 25)) == (modes[r] in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION))
         assert int(v["queue"][0]) == 0
         S_max = -(-shape.max_blocks // T)
         for r in range(R):
@@ -139,13 +138,8 @@ def test_compaction_matches_oracle():
                 hi = v["head_info"][r, g]
                 assert hi[0] == (r * 2 + g) * S_max
                 assert hi[1] == -(-nb // T) and hi[2] == lst.shape[0]
+                assert hi[3] == len(set((lst // T).tolist()))
                 if modes[r] == W.MODE_SPARSE:
-                    tl = v["tile_list"][r, g, :lst.shape[0]]
-                    assert np.array_equal(tl[:, 0], lst)
-                    # each tile carries the pages of its valid tokens (0 past the row)
-                    for (b_, p0, p1, _z) in tl:
-                        assert p0 == w.page_table[r, 2 * b_]
-                        assert p1 == (w.page_table[r, 2 * b_ + 1] if 32 * b_ + 16 < lens[r] else 0)
                     # empty ranges are marked so the finish pass skips them
                     ml = v["partial_ml"][hi[0]:hi[0] + hi[1]]
                     for s_ in range(hi[1]):
@@ -212,7 +206,7 @@ def test_partial_reuses_a_compaction():
     shape = shape_for(w)
     ws = W.alloc_workspace(shape)
     modes = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
-    W.wise_compact_tiles(shape, modes, b.seq_lens, sup, b.page_table, ws)
+    W.wise_compact_tiles(shape, modes, b.seq_lens, sup, ws)
     outs = []
     for depth in (0, 1, 1):
         d = b.dev(depth)
@@ -311,8 +305,7 @@ def test_seq_len_above_capacity_is_clamped_and_flagged():
     lens[0] = cap + 1000
     ws = W.alloc_workspace(shape)
     modes = torch.zeros(4, dtype=torch.int8, device="cuda")
-    W.wise_compact_tiles(shape, modes, torch.from_numpy(lens).cuda(), None,
-                         torch.from_numpy(w.page_table).cuda(), ws)
+    W.wise_compact_tiles(shape, modes, torch.from_numpy(lens).cuda(), None, ws)
     torch.cuda.synchronize()
     v = W.workspace_views(shape, ws)
     assert int(v["status"].item()) & W.wise.DEVERR_SEQ_LEN_CLAMPED
