@@ -97,14 +97,24 @@ __global__ void __launch_bounds__(kCompactThreads)
   const int rounds = (nunits + kCompactThreads - 1) / kCompactThreads;
   UnitInfo cache[kCached];
 
-  // Phase A: item sizes.
+  // Phase A: item sizes.  The cached rounds' loads are all issued before
+  // any is used (one memory round trip instead of one per round).
+#pragma unroll
+  for (int c = 0; c < kCached; ++c) {
+    const int u = c * kCompactThreads + threadIdx.x;
+    cache[c] = UnitInfo{0u, 0, 0, false};
+    if (c < rounds && u < nunits) cache[c] = unit_info(u / S, u % S, modes, seq_lens, support, kp);
+  }
   for (int i = 0; i < rounds; ++i) {
     const int u = i * kCompactThreads + threadIdx.x;
     UnitInfo ui{0u, 0, 0, false};
-    if (u < nunits) ui = unit_info(u / S, u % S, modes, seq_lens, support, kp);
+    if (i < kCached) {
 #pragma unroll
-    for (int c = 0; c < kCached; ++c)
-      if (c == i) cache[c] = ui;
+      for (int c = 0; c < kCached; ++c)
+        if (c == i) ui = cache[c];
+    } else if (u < nunits) {
+      ui = unit_info(u / S, u % S, modes, seq_lens, support, kp);
+    }
     const int n = __popc(ui.bits);
     const unsigned same = __match_any_sync(kFull, n);
     if (n > 0 && lane == __ffs(same) - 1) {

@@ -287,16 +287,18 @@ __device__ __forceinline__ void warp_bitonic_sort(uint64_t (&key)[E], int lane) 
   }
 }
 
+// Selection over the warp's blocks: st[e] holds the (prefetched) statistics
+// of block lane * E + e.
 template <int E>
-__device__ __forceinline__ void warp_select(const float2* __restrict__ ts, int nb, float lse2,
-                                            float eta, uint32_t* smask, int lane) {
+__device__ __forceinline__ void warp_select(const float2 (&st)[2], int nb, float lse2, float eta,
+                                            uint32_t* smask, int lane) {
   constexpr uint64_t kPad = ~0ull;
   uint64_t key[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int i = lane * E + e;
     if (i < nb) {
-      const float2 t = ts[i];
+      const float2 t = st[e];
       const float p = t.y * exp2f(t.x - lse2);
       key[e] = ((uint64_t)(~__float_as_uint(p)) << 32) | (uint32_t)i;
     } else {
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(256)
     finish_short_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                         const WsView ws, const KParams kp, uint32_t* __restrict__ support,
                         T* __restrict__ out, float* __restrict__ lse) {
+  constexpr int kSlots = 8;  // short rows: at most 8 split slots
   __shared__ uint32_t smask[32];
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
@@ -346,37 +349,59 @@ __global__ void __launch_bounds__(256)
   const int h = g * G + warp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
   const int mode = modes[r];
+  const int nb = (L + kTile - 1) / kTile;
+  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
+  // Everything this CTA reads is addressed from the row length alone, so
+  // all loads go out together: the split slots (rg * S_max + i, i < ranges),
+  // the tile statistics and the old mask word.
+  const int nslots = (nb + kp.T - 1) / kp.T;
+  const size_t slot0 = (size_t)rg * kp.S_max;
+  float2 t[kSlots];
+  float4 a[kSlots];
+#pragma unroll
+  for (int i = 0; i < kSlots; ++i) {
+    const bool in = i < nslots;
+    const size_t idx = (slot0 + (in ? i : 0)) * G + warp;
+    t[i] = in ? ws.partial_ml[idx] : make_float2(-INFINITY, 0.f);
+    const float* ap = ws.partial_acc + idx * D + lane * dpl;
+    a[i] = dpl == 4 ? *reinterpret_cast<const float4*>(ap) : make_float4(ap[0], ap[1], 0.f, 0.f);
+  }
+  // Tile statistics in the layout of the selection: block lane * E + e,
+  // E = 1 for rows of up to 32 blocks, 2 up to 64.
+  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
+  const int E = nb > 32 ? 2 : 1;
+  float2 st[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int i = lane * E + e;
+    st[e] = disc && e < E && i < nb ? ts[i] : make_float2(0.f, 0.f);
+  }
+  const uint32_t old_word =
+      (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W) ? support[(size_t)rg * kp.W + threadIdx.x] : 0u;
+  const int4 hi = ws.head_info[rg];
+
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
-  const int4 hi = ws.head_info[rg];
   if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
     if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
     else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
     return;
   }
-  const float2* ml = ws.partial_ml;
   float M = -INFINITY;
-  for (int i = 0; i < hi.y; ++i) {
-    const float2 t = ml[(size_t)(hi.x + i) * G + warp];
-    if (t.y > 0.f) M = fmaxf(M, t.x);
-  }
+#pragma unroll
+  for (int i = 0; i < kSlots; ++i)
+    if (t[i].y > 0.f) M = fmaxf(M, t[i].x);
   float lam = 0.f;
-  for (int i = 0; i < hi.y; ++i) {
-    const size_t idx = (size_t)(hi.x + i) * G + warp;
-    const float2 t = ml[idx];
-    if (!(t.y > 0.f)) continue;  // an empty range of a sparse row
-    const float w = exp2f(t.x - M);
-    lam = fmaf(t.y, w, lam);
-    const float* a = ws.partial_acc + idx * D + lane * dpl;
-    if (dpl == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(a);
-      o[0] = fmaf(v.x, w, o[0]); o[1] = fmaf(v.y, w, o[1]);
-      o[2] = fmaf(v.z, w, o[2]); o[3] = fmaf(v.w, w, o[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(a);
-      o[0] = fmaf(v.x, w, o[0]); o[1] = fmaf(v.y, w, o[1]);
-    }
+#pragma unroll
+  for (int i = 0; i < kSlots; ++i) {
+    const bool used = t[i].y > 0.f;  // an empty range's accumulator is never used
+    const float w = used ? exp2f(t[i].x - M) : 0.f;
+    lam = fmaf(t[i].y, w, lam);
+    o[0] += used ? a[i].x * w : 0.f;
+    o[1] += used ? a[i].y * w : 0.f;
+    o[2] += used ? a[i].z * w : 0.f;
+    o[3] += used ? a[i].w * w : 0.f;
   }
   const float inv = 1.f / lam;
 #pragma unroll
@@ -386,22 +411,19 @@ __global__ void __launch_bounds__(256)
   const float lse2 = M + log2f(lam);
   if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
 
-  if ((mode != WISE_MODE_DISCOVER && mode != WISE_MODE_DISCOVER_UNION) || support == nullptr) return;
+  if (!disc) return;
   if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
   __syncthreads();
-  const int nb = (L + kTile - 1) / kTile;
-  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
-  if (nb <= 32) warp_select<1>(ts, nb, lse2, kp.eta, smask, lane);
-  else warp_select<2>(ts, nb, lse2, kp.eta, smask, lane);
+  if (nb <= 32) warp_select<1>(st, nb, lse2, kp.eta, smask, lane);
+  else warp_select<2>(st, nb, lse2, kp.eta, smask, lane);
   __syncthreads();
   if ((int)threadIdx.x < kp.W) {
-    const int t = threadIdx.x;
-    const int lo = t * 32;
+    const int tw = threadIdx.x;
+    const int lo = tw * 32;
     const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
-    uint32_t* word = support + (size_t)rg * kp.W + t;
-    uint32_t w = smask[t] & valid;
-    if (mode == WISE_MODE_DISCOVER_UNION) w |= *word & valid;
-    *word = w;
+    uint32_t w = smask[tw] & valid;
+    if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
+    support[(size_t)rg * kp.W + tw] = w;
   }
 }
 
