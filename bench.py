@@ -157,14 +157,15 @@ def record_traffic(raw_csv: str, rows: int, workload: str) -> None:
     print(json.dumps(out))
 
 
-def recorded_traffic(rows: int):
+def recorded_traffic(rows: int, workload: str):
     """Average per-launch DRAM bytes of the partial pass, or None when no
-    capture exists for the current kernel source."""
+    capture exists for the current kernel source and this workload."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         rec = json.load(f)
-    if rec.get("kernel_source_sha256") != kernel_source_hash() or not rec.get("per_launch_bytes"):
+    if (rec.get("kernel_source_sha256") != kernel_source_hash() or not rec.get("per_launch_bytes")
+            or rec.get("workload") != workload):
         return None
     per = rec["per_launch_bytes"][:4]
     return sum(per) / len(per) * rows / rec["captured_rows"]
@@ -438,6 +439,35 @@ def e2e_region(pipe, K):
     return s.elapsed_time(e), h2d, d2h
 
 
+# ----------------------------------------------------------------------------- ranks
+def rank_env():
+    """(world size, rank, local rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank: int):
+    """Seed of a rank's own batch: every rank decodes different rows of the
+    same shape (weak scaling; rows are independent, so nothing is exchanged
+    on the data path).  Rank 0 keeps the workload's own seed."""
+    return None if rank == 0 else 100000 + rank
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (the job takes as long as its
+    slowest rank)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(world: int, units_per_step: int, steps: int, ms: float) -> float:
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return world * units_per_step * steps / (ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -452,9 +482,7 @@ def main_ours(args):
     import torch
     import torch.distributed as tdist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         tdist.init_process_group("nccl")
@@ -465,8 +493,7 @@ def main_ours(args):
     from block_sparse_paged_split_gb300.workload import make_workload
     build_library()
     # Weak scaling: every rank decodes its own batch (rows are independent).
-    w = make_workload(args.workload, num_rows=args.rows,
-                      seed=None if rank == 0 else 100000 + rank)
+    w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item)
 
     for _ in range(max(args.warmup, 3)):
@@ -506,10 +533,8 @@ def main_ours(args):
     wall = time.time() - wall0
 
     # Max over ranks.
-    t = torch.tensor([ms, ms_dense_graph, ms_eager, ms_dense], dtype=torch.float64, device="cuda")
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, ms_dense_graph, ms_eager, ms_dense = (float(x) for x in t)
+    ms, ms_dense_graph, ms_eager, ms_dense = max_over_ranks(
+        [ms, ms_dense_graph, ms_eager, ms_dense], dist, "cuda")
 
     def summarize(evts):
         per = {}
@@ -555,8 +580,9 @@ def main_ours(args):
 
     e2e_ms, h2d, d2h = e2e_region(pipe, args.steps)
     rows_per_step = R * w.num_depths
-    value = world * rows_per_step * args.steps / (ms * 1e-3)
-    e2e_value = world * rows_per_step * args.steps / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks([e2e_ms], dist, "cuda")[0]
+    value = whole_job_rate(world, rows_per_step, args.steps, ms)
+    e2e_value = whole_job_rate(world, rows_per_step, args.steps, e2e_ms)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -577,7 +603,7 @@ def main_ours(args):
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": (round(traffic) if (traffic := recorded_traffic(R)) else None),
+                     "traffic": (round(traffic) if (traffic := recorded_traffic(R, args.workload)) else None),
                      "algorithmic_bytes_per_launch": round(
                          part_bytes / sum(1 for k in per if k[2] == "partial")),
                      "kernel": "partial_kernel (split-KV partial pass, all four depths)",
@@ -585,7 +611,7 @@ def main_ours(args):
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "eager": {"ms_per_step": round(ms_eager / args.steps, 4),
-                  "rows_per_s": round(world * rows_per_step * args.steps / (ms_eager * 1e-3), 1),
+                  "rows_per_s": round(whole_job_rate(world, rows_per_step, args.steps, ms_eager), 1),
                   "note": "every launch bracketed by CUDA events"},
         "speedup_vs_dense": round(ms_dense_graph / ms, 3),
         "gpu_launches": launches,
@@ -601,7 +627,7 @@ def main_ours(args):
 
 
 def main_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    rank = rank_env()[1]
     if rank != 0:
         return
     K, Wm = args.steps, args.warmup
