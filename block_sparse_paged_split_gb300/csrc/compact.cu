@@ -13,6 +13,8 @@
 namespace wise {
 
 constexpr int kCompactThreads = 1024;
+constexpr int kCompactCluster = 8;  // CTAs of the one cluster the kernel runs as
+constexpr int kMaxT = 16;           // largest tiles_per_item
 
 // Work items are block ranges: item (rg, s) holds the tiles of (row, KV head)
 // rg that lie in blocks [s*T, s*T + T) -- all of them for dense and discover
@@ -31,9 +33,14 @@ constexpr int kCompactThreads = 1024;
 // the partial pass hands them out (through an atomic counter): tile count
 // descending, so the last warps do not finish long items alone.
 //
-// Work is flattened to one unit per (row, KV head, range): phase A counts
-// each unit's tiles and builds a histogram of item sizes (warp-aggregated
-// shared-memory atomics); phase B writes each item at its schedule slot and
+// Work is flattened to one unit per (row, KV head, range) and spread over
+// the threads of one thread-block cluster (8 CTAs of 1024 threads).  Phase A
+// counts each unit's tiles into its CTA's histogram of item sizes
+// (warp-aggregated shared-memory atomics).  After a cluster barrier every CTA
+// reads the others' histograms through distributed shared memory and works
+// out where its items of each size start in the schedule (larger sizes
+// first, then lower CTA ranks), so no counter in global memory has to be
+// reset between calls.  Phase B writes each item at its schedule slot and
 // marks the partial slots of a sparse row's empty ranges; a thread per
 // (row, KV head) writes its head info.
 __device__ __forceinline__ uint32_t range_bitmap(bool sparse, const uint32_t* words, int s, int T,
@@ -70,43 +77,65 @@ __device__ __forceinline__ UnitInfo unit_info(int pair, int s, const int8_t* __r
   return u;
 }
 
-__global__ void __launch_bounds__(kCompactThreads)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// An int in CTA `rank`'s shared memory at the address of `p` in this CTA's.
+__device__ __forceinline__ int load_peer(const int* p, uint32_t rank) {
+  uint32_t remote;
+  int v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompactThreads)
     compact_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                    const uint32_t* __restrict__ support, const WsView ws, const KParams kp) {
   grid_dependency_wait();
   grid_dependents_launch();  // the partial pass may start its prologue now
-  __shared__ int size_slot[17];  // items per size (1..T), then the next schedule slot
-  __shared__ int total_items;
+  __shared__ int hist[kMaxT + 1];                     // this CTA's items of each size
+  __shared__ int next[kMaxT + 1];                     // its next schedule slot of each size
+  __shared__ int peer[kCompactCluster][kMaxT + 1];    // every CTA's histogram
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
+  const uint32_t crank = cluster_rank();
+  const int nthreads = kCompactCluster * kCompactThreads;
+  const int gt = (int)crank * kCompactThreads + threadIdx.x;
+  if (gt == 0) {
     *ws.status = 0;
     *ws.queue = 0;
     *ws.queue_done = 0;
-    total_items = 0;
   }
-  for (int i = threadIdx.x; i <= 16; i += blockDim.x) size_slot[i] = 0;
+  if (threadIdx.x <= kMaxT) hist[threadIdx.x] = 0;
   __syncthreads();
   const int npair = kp.R * kp.Hkv;
   const int S = kp.S_max;
   const int nunits = npair * S;
 
-  // A thread's units are u = threadIdx.x + i * kCompactThreads; up to
-  // kCached of them stay in registers between the two phases (more are
-  // looked up again in phase B).
-  constexpr int kCached = 8;
-  const int rounds = (nunits + kCompactThreads - 1) / kCompactThreads;
+  // The thread's units are u = gt + i * nthreads; up to kCached of them stay
+  // in registers between the two phases (more are looked up again in phase
+  // B).  The cached rounds' loads are all issued before any is used.
+  constexpr int kCached = 4;
+  const int rounds = (nunits + nthreads - 1) / nthreads;
   UnitInfo cache[kCached];
-
-  // Phase A: item sizes.  The cached rounds' loads are all issued before
-  // any is used (one memory round trip instead of one per round).
 #pragma unroll
   for (int c = 0; c < kCached; ++c) {
-    const int u = c * kCompactThreads + threadIdx.x;
+    const int u = c * nthreads + gt;
     cache[c] = UnitInfo{0u, 0, 0, false};
     if (c < rounds && u < nunits) cache[c] = unit_info(u / S, u % S, modes, seq_lens, support, kp);
   }
-  for (int i = 0; i < rounds; ++i) {
-    const int u = i * kCompactThreads + threadIdx.x;
+  auto unit = [&](int i, int u) {
     UnitInfo ui{0u, 0, 0, false};
     if (i < kCached) {
 #pragma unroll
@@ -115,42 +144,51 @@ __global__ void __launch_bounds__(kCompactThreads)
     } else if (u < nunits) {
       ui = unit_info(u / S, u % S, modes, seq_lens, support, kp);
     }
-    const int n = __popc(ui.bits);
+    return ui;
+  };
+
+  // Phase A: this CTA's histogram of item sizes.
+  for (int i = 0; i < rounds; ++i) {
+    const int n = __popc(unit(i, i * nthreads + gt).bits);
     const unsigned same = __match_any_sync(kFull, n);
-    if (n > 0 && lane == __ffs(same) - 1) {
-      atomicAdd(&size_slot[n], __popc(same));
-      atomicAdd(&total_items, __popc(same));
-    }
+    if (n > 0 && lane == __ffs(same) - 1) atomicAdd(&hist[n], __popc(same));
   }
+  cluster_arrive();  // every CTA's histogram is complete (and the resets above visible)
+  cluster_wait();
+  for (int i = threadIdx.x; i < kCompactCluster * (kMaxT + 1); i += blockDim.x) {
+    const int c = i / (kMaxT + 1), sz = i - c * (kMaxT + 1);
+    peer[c][sz] = sz <= kp.T ? load_peer(&hist[sz], c) : 0;
+  }
+  cluster_arrive();  // this CTA is done reading the others' shared memory
   __syncthreads();
-  if (threadIdx.x == 0) {
-    *ws.num_items = total_items;
-    int run = 0;
-    for (int sz = kp.T; sz >= 1; --sz) {
-      const int n = size_slot[sz];
-      size_slot[sz] = run;
-      run += n;
+  // Schedule: sizes T..1; within a size, CTA 0's items first.
+  if (threadIdx.x >= 1 && threadIdx.x <= kp.T) {
+    const int sz = threadIdx.x;
+    int before = 0;
+    for (int c = 0; c < kCompactCluster; ++c) {
+      for (int s2 = sz + 1; s2 <= kp.T; ++s2) before += peer[c][s2];
+      if (c < (int)crank) before += peer[c][sz];
     }
+    next[sz] = before;
+  }
+  if (gt == 0) {
+    int total = 0;
+    for (int c = 0; c < kCompactCluster; ++c)
+      for (int sz = 1; sz <= kp.T; ++sz) total += peer[c][sz];
+    *ws.num_items = total;
   }
   __syncthreads();
 
   // Phase B: item records at their schedule slots; empty-range markers.
   for (int i = 0; i < rounds; ++i) {
-    const int u = i * kCompactThreads + threadIdx.x;
+    const int u = i * nthreads + gt;
     const int pair = u / S, s = u % S;
-    UnitInfo ui{0u, 0, 0, false};
-    if (i < kCached) {
-#pragma unroll
-      for (int c = 0; c < kCached; ++c)
-        if (c == i) ui = cache[c];
-    } else if (u < nunits) {
-      ui = unit_info(pair, s, modes, seq_lens, support, kp);
-    }
+    const UnitInfo ui = unit(i, u);
     const int n = __popc(ui.bits);
     const unsigned same = __match_any_sync(kFull, n);
     const int leader = __ffs(same) - 1;
     int slot = 0;
-    if (n > 0 && lane == leader) slot = atomicAdd(&size_slot[n], __popc(same));
+    if (n > 0 && lane == leader) slot = atomicAdd(&next[n], __popc(same));
     slot = __shfl_sync(kFull, slot, leader);
     if (n > 0) {
       ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
@@ -164,7 +202,7 @@ __global__ void __launch_bounds__(kCompactThreads)
   }
 
   // Head info: first partial slot, block ranges, tiles, items.
-  for (int pair = threadIdx.x; pair < npair; pair += kCompactThreads) {
+  for (int pair = gt; pair < npair; pair += nthreads) {
     const int r = pair / kp.Hkv;
     const int raw = seq_lens[r];
     const int L = clamp_len(raw, kp.cap_tokens);
@@ -186,12 +224,13 @@ __global__ void __launch_bounds__(kCompactThreads)
     }
     ws.head_info[pair] = make_int4(pair * S, nr, count, nitems);
   }
+  cluster_wait();  // no CTA leaves while another may still read its histogram
 }
 
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                            const uint32_t* support, const WsView& ws, cudaStream_t stream) {
-  return launch_pdl(compact_kernel, dim3(1), dim3(kCompactThreads), 0, stream, modes, seq_lens,
-                    support, ws, kp);
+  return launch_pdl(compact_kernel, dim3(kCompactCluster), dim3(kCompactThreads), 0, stream, modes,
+                    seq_lens, support, ws, kp);
 }
 
 // ------------------------------------------------------------------ union

@@ -3,25 +3,23 @@
 // [WISE PR, "What changes"]: a finish kernel merges the splits and runs the
 // selection for discovery rows.  One CTA per (row, KV head).  Rows of up to
 // 64 blocks use one warp per query head (finish_short_kernel); longer rows
-// give each query head WPH = 4 warps (its "group" of threads, synchronised
-// by a named barrier of its own).
+// give each query head a group of wph = min(8, 32 / G) warps, synchronised by
+// a named barrier of its own (finish_kernel).
 //
 //   merge    M = max_i m_i, Lambda = sum_i l_i 2^(m_i - M),
 //            out = sum_i acc_i 2^(m_i - M) / Lambda, lse = (M + log2 Lambda) ln 2
 //            (m_i in log2 units of the scaled score).  Slot i is block range
 //            i of the row; an empty range of a sparse row holds (-inf, 0) and
 //            contributes nothing (its accumulator is never read into the sum).
-//            The group's threads share the slots; loads are issued four
-//            slots at a time, so long rows (many splits) are not latency-bound.
-//   select   for discover rows: p_b = l_b 2^(m_b - lse2) per block; the group
-//            sorts 64-bit keys (~bits(p_b) << 32 | b) ascending -- mass
-//            descending, ties to the lower block index -- with a bitonic
-//            network in shared memory; the block at sorted position k is kept
-//            iff the mass before it is below eta, which is exactly the shortest
-//            prefix reaching eta (eta >= 1 keeps every block).  The group's
-//            query heads OR their choices in shared memory; the mask is
-//            written (DISCOVER) or ORed into (DISCOVER_UNION), with bits at or
-//            past the row's block count cleared.
+//   select   for discover rows: p_b = l_b 2^(m_b - lse2) per block; 64-bit
+//            keys (~bits(p_b) << 32 | b) are sorted ascending -- mass
+//            descending, ties to the lower block index -- by a bitonic
+//            network; the block at sorted position k is kept iff the mass
+//            before it is below eta, which is exactly the shortest prefix
+//            reaching eta (eta >= 1 keeps every block).  The group's query
+//            heads OR their choices in shared memory; the mask is written
+//            (DISCOVER) or ORed into (DISCOVER_UNION), with bits at or past
+//            the row's block count cleared.
 #include <mutex>
 
 #include "internal.h"
@@ -67,7 +65,122 @@ __device__ __forceinline__ float group_max(float v, int th, int wph, float* scra
   return r;
 }
 
-template <typename T>
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
+  uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, o);
+  uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), o);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// One bitonic stage whose partner distance J (< E) stays within a thread's
+// registers; `base` is the group-wide index of the thread's key 0.
+template <int E, int J>
+__device__ __forceinline__ void bitonic_reg_stage(uint64_t (&key)[E], int base, int k) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e & J) == 0) {
+      const bool up = ((base + e) & k) == 0;
+      const uint64_t a = key[e], b = key[e + J];
+      const bool swap = up ? (a > b) : (a < b);
+      key[e] = swap ? b : a;
+      key[e + J] = swap ? a : b;
+    }
+  }
+}
+
+// Ascending bitonic sort of a group's npad = 32 * E * wph keys: key i
+// (i = wsub * 32E + lane * E + e) lives in register e of lane `lane` of the
+// group's warp wsub.  Stages whose partner lies in another warp exchange
+// through shared memory (`xbuf`, npad keys, one named barrier each side);
+// stages within a warp use shuffles, stages within a thread its registers.
+template <int E>
+__device__ __forceinline__ void group_bitonic_sort(uint64_t (&key)[E], int lane, int wsub, int wph,
+                                                   uint64_t* xbuf, int bar_id) {
+  const int npad = 32 * E * wph;
+  const int base = wsub * 32 * E + lane * E;
+  for (int k = 2; k <= npad; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32 * E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) xbuf[base + e] = key[e];
+        group_sync(bar_id, wph * 32);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = base + e;
+          const uint64_t other = xbuf[i ^ j];
+          const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+          key[e] = keep_min ? (key[e] < other ? key[e] : other) : (key[e] < other ? other : key[e]);
+        }
+        group_sync(bar_id, wph * 32);
+      } else if (j >= E) {
+        const int lj = j / E;  // partner lane distance
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const bool up = ((base + e) & k) == 0;
+          const uint64_t other = shfl_xor_u64(key[e], lj);
+          const uint64_t mn = key[e] < other ? key[e] : other;
+          const uint64_t mx = key[e] < other ? other : key[e];
+          key[e] = (lower == up) ? mn : mx;
+        }
+      } else if (j == 4) {
+        if constexpr (E > 4) bitonic_reg_stage<E, 4>(key, base, k);
+      } else if (j == 2) {
+        if constexpr (E > 2) bitonic_reg_stage<E, 2>(key, base, k);
+      } else {
+        if constexpr (E > 1) bitonic_reg_stage<E, 1>(key, base, k);
+      }
+    }
+  }
+}
+
+// Selection for one query head by its group of wph warps: keys from the
+// (prefetched) tile statistics st[e] of block wsub * 32E + lane * E + e,
+// sorted, then each kept block ORed into smask.
+template <int E>
+__device__ __forceinline__ void group_select(const float2 (&st)[E], int nb, float lse2, float eta,
+                                             int lane, int wsub, int wph, uint64_t* xbuf,
+                                             float* scratch, int bar_id, uint32_t* smask) {
+  constexpr uint64_t kPad = ~0ull;
+  const int base = wsub * 32 * E + lane * E;
+  uint64_t key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = base + e;
+    if (i < nb) {
+      const float p = st[e].y * exp2f(st[e].x - lse2);
+      key[e] = ((uint64_t)(~__float_as_uint(p)) << 32) | (uint32_t)i;
+    } else {
+      key[e] = kPad;
+    }
+  }
+  group_bitonic_sort<E>(key, lane, wsub, wph, xbuf, bar_id);
+  float pm[E];
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    pm[e] = key[e] == kPad ? 0.f : __uint_as_float(~(uint32_t)(key[e] >> 32));
+    mine += pm[e];
+  }
+  float before = group_exclusive_scan(mine, wsub * 32 + lane, wph, scratch, bar_id);
+  const bool all = eta >= 1.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (key[e] != kPad && (all || before < eta)) {
+      const uint32_t b = (uint32_t)key[e];
+      atomicOr(&smask[b >> 5], 1u << (b & 31));
+    }
+    before += pm[e];
+  }
+}
+
+// Long rows: one CTA per (row, KV head), a group of wph warps per query head.
+//   merge   the group's warps take the split slots round-robin, four loads
+//           in flight per lane, with an online rescale; the warps' (m, l,
+//           acc) are then combined through shared memory.
+//   select  npad = 32 * E * wph keys (npad >= max_blocks, a power of two;
+//           blocks past the row's n_b are padding) are sorted mostly in
+//           registers (see group_bitonic_sort).
+template <typename T, int E>
 __global__ void __launch_bounds__(1024)
     finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                   const WsView ws, const KParams kp, uint32_t* __restrict__ support,
@@ -83,7 +196,7 @@ __global__ void __launch_bounds__(1024)
   const int lane = threadIdx.x & 31, wsub = th >> 5;
   const int bar_id = 1 + hgrp;
   // Shared memory: keys [G][npad_max] u64 | scratch [G][wph][D + 2] f32.
-  uint64_t* keys = reinterpret_cast<uint64_t*>(fsm) + (size_t)hgrp * npad_max;
+  uint64_t* xbuf = reinterpret_cast<uint64_t*>(fsm) + (size_t)hgrp * npad_max;
   float* scratch = reinterpret_cast<float*>(fsm + (size_t)G * npad_max * 8) +
                    (size_t)hgrp * wph * (D + 2);
 
@@ -92,10 +205,23 @@ __global__ void __launch_bounds__(1024)
   const int h = g * G + hgrp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
   const int mode = modes[r];
+  const int nb = (L + kTile - 1) / kTile;
+  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
   const int dpl = D >> 5;  // 2 or 4 dims per lane
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 
+  // The tile statistics and the old mask word go out with the first loads.
+  float2 st[E];
+  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = wsub * 32 * E + lane * E + e;
+    st[e] = disc && i < nb ? ts[i] : make_float2(0.f, 0.f);
+  }
+  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W)
+                                ? support[(size_t)rg * kp.W + threadIdx.x]
+                                : 0u;
   const int4 hi = ws.head_info[rg];
   if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
     if (wsub == 0) {
@@ -110,13 +236,7 @@ __global__ void __launch_bounds__(1024)
   const float2* ml = ws.partial_ml + (size_t)hi.x * G + hgrp;  // slot s at ml[s * G]
   const float* acc = ws.partial_acc + ((size_t)hi.x * G + hgrp) * D + lane * dpl;
   const int n = hi.y;
-  float M = -INFINITY;
-  for (int s = th; s < n; s += gs) {
-    const float2 t = ml[(size_t)s * G];
-    if (t.y > 0.f) M = fmaxf(M, t.x);
-  }
-  M = group_max(M, th, wph, scratch, bar_id);
-  float lam = 0.f;
+  float m_w = -INFINITY, lam = 0.f;
   for (int s0 = wsub; s0 < n; s0 += 4 * wph) {
     float2 t[4];
     float4 a[4];
@@ -128,10 +248,21 @@ __global__ void __launch_bounds__(1024)
       const float* ap = acc + (size_t)(in ? s : 0) * G * D;
       a[u] = dpl == 4 ? *reinterpret_cast<const float4*>(ap) : make_float4(ap[0], ap[1], 0.f, 0.f);
     }
+    float mb = m_w;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (t[u].y > 0.f) mb = fmaxf(mb, t[u].x);
+    if (mb > m_w) {  // rescale what this warp has summed so far
+      const float sc = exp2f(m_w - mb);
+      lam *= sc;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] *= sc;
+      m_w = mb;
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const bool used = t[u].y > 0.f;  // an empty range's accumulator is never used
-      const float w = used ? exp2f(t[u].x - M) : 0.f;
+      const float w = used ? exp2f(t[u].x - m_w) : 0.f;
       lam = fmaf(t[u].y, w, lam);
       o[0] += used ? a[u].x * w : 0.f;
       o[1] += used ? a[u].y * w : 0.f;
@@ -139,27 +270,36 @@ __global__ void __launch_bounds__(1024)
       o[3] += used ? a[u].w * w : 0.f;
     }
   }
-  if (wph > 1) {
-    // Sum the group's warps (every warp forms the same totals).
+  // Combine the group's warps: every warp forms M and Lambda, warp 0 the output.
+  {
     float* mine = scratch + wsub * (D + 2);
-    if (lane == 0) mine[D] = lam;
+    if (lane == 0) {
+      mine[D] = m_w;
+      mine[D + 1] = lam;
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       if (j < dpl) mine[lane * dpl + j] = o[j];
     group_sync(bar_id, gs);
+    float M = -INFINITY;
+    for (int w = 0; w < wph; ++w) M = fmaxf(M, scratch[w * (D + 2) + D]);
     lam = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) o[j] = 0.f;
     for (int w = 0; w < wph; ++w) {
       const float* part = scratch + w * (D + 2);
-      lam += part[D];
+      const float sc = part[D + 1] > 0.f ? exp2f(part[D] - M) : 0.f;
+      lam = fmaf(part[D + 1], sc, lam);
+      if (wsub == 0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j < dpl) o[j] += part[lane * dpl + j];
+        for (int j = 0; j < 4; ++j)
+          if (j < dpl) o[j] = fmaf(part[lane * dpl + j], sc, o[j]);
+      }
     }
+    m_w = M;
     group_sync(bar_id, gs);
   }
-  const float lse2 = M + log2f(lam);
+  const float lse2 = m_w + log2f(lam);
   if (wsub == 0) {
     const float inv = 1.f / lam;
 #pragma unroll
@@ -169,74 +309,20 @@ __global__ void __launch_bounds__(1024)
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
   }
 
-  if ((mode != WISE_MODE_DISCOVER && mode != WISE_MODE_DISCOVER_UNION) || support == nullptr) return;
+  if (!disc) return;
 
   // ---- eta selection for this query head
   if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
   __syncthreads();
-  const int nb = (L + kTile - 1) / kTile;
-  int npad = 32;
-  while (npad < nb) npad <<= 1;
-  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
-  for (int i = th; i < npad; i += gs) {
-    uint64_t key = ~0ull;
-    if (i < nb) {
-      const float2 t = ts[i];
-      const float p = t.y * exp2f(t.x - lse2);
-      key = ((uint64_t)(~__float_as_uint(p)) << 32) | (uint32_t)i;
-    }
-    keys[i] = key;
-  }
-  group_sync(bar_id, gs);
-  for (int k = 2; k <= npad; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int idx = th; idx < (npad >> 1); idx += gs) {
-        const int i = ((idx & ~(j - 1)) << 1) | (idx & (j - 1));  // lower element of the pair
-        const uint64_t a = keys[i], b = keys[i + j];
-        const bool up = (i & k) == 0;
-        if ((a > b) == up) {
-          keys[i] = b;
-          keys[i + j] = a;
-        }
-      }
-      group_sync(bar_id, gs);
-    }
-  }
-  // Thread th owns sorted positions [th * c, th * c + c), c <= 8 (npad <= 64
-  // with one warp per head, npad <= 1024 with four).
-  const int c = npad >= gs ? npad / gs : 1;
-  float pm[8];
-  float mine = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int i = th * c + e;
-    const bool ok = e < c && i < npad && keys[i] != ~0ull;
-    pm[e] = ok ? __uint_as_float(~(uint32_t)(keys[i] >> 32)) : 0.f;
-    mine += pm[e];
-  }
-  float before = group_exclusive_scan(mine, th, wph, scratch, bar_id);
-  const bool all = kp.eta >= 1.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int i = th * c + e;
-    if (e < c && i < npad) {
-      const uint64_t key = keys[i];
-      if (key != ~0ull && (all || before < kp.eta)) {
-        const uint32_t b = (uint32_t)key;
-        atomicOr(&smask[b >> 5], 1u << (b & 31));
-      }
-    }
-    before += pm[e];
-  }
+  group_select<E>(st, nb, lse2, kp.eta, lane, wsub, wph, xbuf, scratch, bar_id, smask);
   __syncthreads();
   if ((int)threadIdx.x < kp.W) {
     const int t = threadIdx.x;
     const int lo = t * 32;
     const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
-    uint32_t* word = support + (size_t)rg * kp.W + t;
     uint32_t w = smask[t] & valid;
-    if (mode == WISE_MODE_DISCOVER_UNION) w |= *word & valid;
-    *word = w;
+    if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
+    support[(size_t)rg * kp.W + t] = w;
   }
 }
 
@@ -244,11 +330,6 @@ __global__ void __launch_bounds__(1024)
 // Rows of at most 64 blocks and 8 split slots: one warp per query head, the
 // merge in each lane over all slots (broadcast loads), and the sort in
 // registers with shuffles (E keys per lane, lane-major blocks).
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
-  uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, o);
-  uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), o);
-  return ((uint64_t)hi << 32) | lo;
-}
 
 // Sorts the warp's 32*E keys ascending; key i lives in lane i / E, slot i % E.
 template <int E>
@@ -427,28 +508,25 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Warps per query head: one for short rows, four when a row can have many
-// split slots or blocks to sort.
-static int finish_wph(const KParams& kp) { return (kp.S_max > 8 || kp.max_blocks > 64) ? 4 : 1; }
+// Rows of at most 64 blocks and 8 split slots take the short kernel (one
+// warp per query head); longer ones a group of wph = min(8, 32 / G) warps
+// per query head (up to 1024 threads a CTA, at most 8 keys a thread).
+static bool finish_short(const KParams& kp) { return kp.S_max <= 8 && kp.max_blocks <= 64; }
+
+static int finish_wph(const KParams& kp) { return kp.G >= 4 ? 32 / kp.G : 8; }
 
 static int finish_npad(const KParams& kp) {
-  int n = 32;
+  int n = 32 * finish_wph(kp);
   while (n < kp.max_blocks) n <<= 1;
   return n;
 }
 
-template <typename T>
-static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
-                                   const int32_t* seq_lens, const WsView& ws, uint32_t* support,
-                                   void* out, float* lse, cudaStream_t stream) {
-  const int wph = finish_wph(kp);
-  if (wph == 1)
-    return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
-                      modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
-  const int npad = finish_npad(kp);
-  const size_t smem = (size_t)kp.G * npad * 8 + (size_t)kp.G * wph * (kp.D + 2) * 4;
-  // The shared-memory opt-in is set once per device (so a call inside a
-  // stream capture issues only the launch).
+template <typename T, int E>
+static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
+                               const WsView& ws, uint32_t* support, void* out, float* lse,
+                               cudaStream_t stream, int wph, int npad, size_t smem) {
+  // The shared-memory opt-in is set once per device and instantiation (so a
+  // call inside a stream capture issues only the launch).
   static std::mutex mu;
   static size_t configured[64] = {0};
   int dev = 0;
@@ -458,14 +536,33 @@ static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
   {
     std::lock_guard<std::mutex> lock(mu);
     if (configured[dev] < smem) {
-      e = cudaFuncSetAttribute(finish_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(finish_kernel<T, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
       configured[dev] = smem;
     }
   }
-  return launch_pdl(finish_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G * wph), smem, stream,
+  return launch_pdl(finish_kernel<T, E>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G * wph), smem, stream,
                     modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse, wph, npad);
+}
+
+template <typename T>
+static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
+                                   const int32_t* seq_lens, const WsView& ws, uint32_t* support,
+                                   void* out, float* lse, cudaStream_t stream) {
+  if (finish_short(kp))
+    return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
+                      modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
+  const int wph = finish_wph(kp);
+  const int npad = finish_npad(kp);
+  const int E = npad / (32 * wph);  // 1, 2, 4 or 8 keys per thread
+  const size_t smem = (size_t)kp.G * npad * 8 + (size_t)kp.G * wph * (kp.D + 2) * 4;
+  switch (E) {
+    case 1: return launch_long<T, 1>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
+    case 2: return launch_long<T, 2>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
+    case 4: return launch_long<T, 4>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
+    default: return launch_long<T, 8>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
+  }
 }
 
 cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,

@@ -310,3 +310,36 @@ def test_seq_len_above_capacity_is_clamped_and_flagged():
     v = W.workspace_views(shape, ws)
     assert int(v["status"].item()) & W.wise.DEVERR_SEQ_LEN_CLAMPED
     assert int(v["head_info"][0, 0, 2].item()) == -(-cap // 32)
+
+
+# Long rows take the multi-warp finish kernel; its sort keeps E keys per
+# thread, E set by the group size (8 warps per query head, 4 with 8 query
+# heads per KV head) and the padded block count.  One case per layout.
+LONG_CASES = [
+    (2, 2, np.array([3000, 100, 0, 2049], np.int32)),         # G=1, 94 blocks -> E=1
+    (4, 2, np.array([10000, 5000, 1, 33], np.int32)),         # G=2, 313 blocks -> E=2
+    (4, 1, np.array([20000, 700, 9999], np.int32)),           # G=4, 625 blocks -> E=4
+    (8, 1, np.array([20000, 3000, 700, 100, 17000], np.int32)),  # G=8, 625 blocks -> E=8
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens", LONG_CASES)
+def test_long_rows_match_oracle(Hq, Hkv, lens):
+    w = _wl(Hq, Hkv, 128, "bf16", lens=lens, seed=11, n_planted=6)
+    b = Batch(w)
+    R = w.num_rows
+    junk = np.random.default_rng(2).integers(0, 2**32, size=(R, Hkv, words(w)), dtype=np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, junk), oracle_call(b, 0, m, junk)
+    assert not compare_outputs(w, g, o)
+    cm = compare_masks(w, g["support"], o, m)
+    assert not cm["fails"] and cm["checked"] > 0, cm
+    s0 = o["support"]
+    m = np.full(R, W.MODE_DISCOVER_UNION, np.int8)
+    g, o = gpu_call(b, 1, m, s0), oracle_call(b, 1, m, s0)
+    assert not compare_outputs(w, g, o)
+    assert not compare_masks(w, g["support"], o, m, support_in=s0)["fails"]
+    s1 = o["support"]
+    m = np.array([W.MODE_SPARSE, W.MODE_DENSE] * R, np.int8)[:R]
+    g, o = gpu_call(b, 2, m, s1), oracle_call(b, 2, m, s1)
+    assert not compare_outputs(w, g, o)
