@@ -34,47 +34,65 @@ constexpr int kMaxT = 16;           // largest tiles_per_item
 // descending, so the last warps do not finish long items alone.
 //
 // Work is flattened to one unit per (row, KV head, range) and spread over
-// the threads of one thread-block cluster (8 CTAs of 1024 threads).  Phase A
+// the threads of one thread-block cluster (8 CTAs of 1024 threads).  Every
+// global load a unit needs (the row's mode and length, the range's mask word)
+// goes out at once, so the kernel makes one memory round trip.  Phase A
 // counts each unit's tiles into its CTA's histogram of item sizes
-// (warp-aggregated shared-memory atomics).  After a cluster barrier every CTA
-// reads the others' histograms through distributed shared memory and works
-// out where its items of each size start in the schedule (larger sizes
-// first, then lower CTA ranks), so no counter in global memory has to be
-// reset between calls.  Phase B writes each item at its schedule slot and
-// marks the partial slots of a sparse row's empty ranges; a thread per
-// (row, KV head) writes its head info.
-__device__ __forceinline__ uint32_t range_bitmap(bool sparse, const uint32_t* words, int s, int T,
-                                                 int nb) {
-  const int lo = s * T;
-  if (lo >= nb) return 0u;
-  const int n = min(T, nb - lo);
-  const uint32_t full = n >= 32 ? 0xffffffffu : (1u << n) - 1u;
-  if (!sparse) return full;
-  if (!words) return 0u;
-  // T is a power of two up to 16, so a range never straddles mask words.
-  return (words[lo >> 5] >> (lo & 31)) & full;
-}
-
+// (warp-aggregated shared-memory atomics), and the thread of a pair's range 0
+// writes the pair's head info (a sparse pair's tile and item counts start at
+// 0).  After a cluster barrier every CTA reads the others' histograms through
+// distributed shared memory and works out where its items of each size start
+// in the schedule (larger sizes first, then lower CTA ranks), so no counter
+// in global memory has to be reset between calls.  Phase B writes each item
+// at its schedule slot, adds a sparse range's tiles to its pair's counts and
+// marks the partial slots of a sparse row's empty ranges.
 struct UnitInfo {
-  uint32_t bits;
+  uint32_t bits;  // tiles of the range (bit i: block s*T + i)
   int L, flags;
   bool sparse;
+  int raw;        // the row's length before clamping
 };
 
-__device__ __forceinline__ UnitInfo unit_info(int pair, int s, const int8_t* __restrict__ modes,
+// The loads of one unit (issued together; nothing here waits on them).
+struct UnitLoad {
+  int mode, raw;
+  uint32_t word;
+};
+
+__device__ __forceinline__ UnitLoad unit_load(int u, int nunits, const int8_t* __restrict__ modes,
                                               const int32_t* __restrict__ seq_lens,
                                               const uint32_t* __restrict__ support,
                                               const KParams& kp) {
-  UnitInfo u;
-  const int r = pair / kp.Hkv;
-  const int mode = modes[r];
-  u.L = clamp_len(seq_lens[r], kp.cap_tokens);
-  u.sparse = mode == WISE_MODE_SPARSE;
-  u.flags = (u.sparse ? kItemSparse : 0) |
-            (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION ? kItemDiscover : 0);
-  const uint32_t* words = (u.sparse && support) ? support + (size_t)pair * kp.W : nullptr;
-  u.bits = range_bitmap(u.sparse, words, s, kp.T, (u.L + kTile - 1) / kTile);
-  return u;
+  UnitLoad l{-1, 0, 0u};
+  if (u < nunits) {
+    const int pair = u / kp.S_max, s = u - pair * kp.S_max;
+    const int r = pair / kp.Hkv;
+    l.mode = modes[r];
+    l.raw = seq_lens[r];
+    // s * T < max_blocks <= 32 W: the word is inside the pair's mask.
+    if (support) l.word = support[(size_t)pair * kp.W + ((s * kp.T) >> 5)];
+  }
+  return l;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(int u, const UnitLoad& l, const KParams& kp) {
+  UnitInfo ui{0u, 0, 0, false, 0};
+  if (l.mode < 0) return ui;  // past the last unit
+  const int s = u % kp.S_max;
+  ui.raw = l.raw;
+  ui.L = clamp_len(l.raw, kp.cap_tokens);
+  ui.sparse = l.mode == WISE_MODE_SPARSE;
+  ui.flags = (ui.sparse ? kItemSparse : 0) |
+             (l.mode == WISE_MODE_DISCOVER || l.mode == WISE_MODE_DISCOVER_UNION ? kItemDiscover : 0);
+  const int nb = (ui.L + kTile - 1) / kTile;
+  const int lo = s * kp.T;
+  if (lo < nb) {
+    const int n = min(kp.T, nb - lo);
+    const uint32_t full = n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+    // T is a power of two up to 16, so a range never straddles mask words.
+    ui.bits = ui.sparse ? (l.word >> (lo & 31)) & full : full;
+  }
+  return ui;
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -107,11 +125,22 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
   grid_dependents_launch();  // the partial pass may start its prologue now
   __shared__ int hist[kMaxT + 1];                     // this CTA's items of each size
   __shared__ int next[kMaxT + 1];                     // its next schedule slot of each size
-  __shared__ int peer[kCompactCluster][kMaxT + 1];    // every CTA's histogram
   const int lane = threadIdx.x & 31;
   const uint32_t crank = cluster_rank();
   const int nthreads = kCompactCluster * kCompactThreads;
   const int gt = (int)crank * kCompactThreads + threadIdx.x;
+  const int S = kp.S_max;
+  const int nunits = kp.R * kp.Hkv * S;
+
+  // The thread's units are u = gt + i * nthreads; the first kCached stay in
+  // registers between the two phases (more are looked up again in phase B).
+  constexpr int kCached = 4;
+  const int rounds = (nunits + nthreads - 1) / nthreads;
+  UnitLoad ld[kCached];
+#pragma unroll
+  for (int c = 0; c < kCached; ++c)
+    ld[c] = c < rounds ? unit_load(c * nthreads + gt, nunits, modes, seq_lens, support, kp)
+                       : UnitLoad{-1, 0, 0u};
   if (gt == 0) {
     *ws.status = 0;
     *ws.queue = 0;
@@ -119,70 +148,67 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
   }
   if (threadIdx.x <= kMaxT) hist[threadIdx.x] = 0;
   __syncthreads();
-  const int npair = kp.R * kp.Hkv;
-  const int S = kp.S_max;
-  const int nunits = npair * S;
-
-  // The thread's units are u = gt + i * nthreads; up to kCached of them stay
-  // in registers between the two phases (more are looked up again in phase
-  // B).  The cached rounds' loads are all issued before any is used.
-  constexpr int kCached = 4;
-  const int rounds = (nunits + nthreads - 1) / nthreads;
-  UnitInfo cache[kCached];
-#pragma unroll
-  for (int c = 0; c < kCached; ++c) {
-    const int u = c * nthreads + gt;
-    cache[c] = UnitInfo{0u, 0, 0, false};
-    if (c < rounds && u < nunits) cache[c] = unit_info(u / S, u % S, modes, seq_lens, support, kp);
-  }
   auto unit = [&](int i, int u) {
-    UnitInfo ui{0u, 0, 0, false};
     if (i < kCached) {
+      UnitLoad l{-1, 0, 0u};
 #pragma unroll
       for (int c = 0; c < kCached; ++c)
-        if (c == i) ui = cache[c];
-    } else if (u < nunits) {
-      ui = unit_info(u / S, u % S, modes, seq_lens, support, kp);
+        if (c == i) l = ld[c];
+      return unit_info(u, l, kp);
     }
-    return ui;
+    return unit_info(u, unit_load(u, nunits, modes, seq_lens, support, kp), kp);
   };
 
-  // Phase A: this CTA's histogram of item sizes.
+  // Phase A: this CTA's histogram of item sizes; head info from each pair's
+  // range 0.
   for (int i = 0; i < rounds; ++i) {
-    const int n = __popc(unit(i, i * nthreads + gt).bits);
+    const int u = i * nthreads + gt;
+    const UnitInfo ui = unit(i, u);
+    const int n = __popc(ui.bits);
     const unsigned same = __match_any_sync(kFull, n);
     if (n > 0 && lane == __ffs(same) - 1) atomicAdd(&hist[n], __popc(same));
+    if (u < nunits && u % S == 0) {
+      const int pair = u / S;
+      const int nb = (ui.L + kTile - 1) / kTile;
+      const int nr = (nb + kp.T - 1) / kp.T;
+      ws.head_info[pair] = ui.sparse ? make_int4(pair * S, nr, 0, 0) : make_int4(pair * S, nr, nb, nr);
+    }
   }
-  cluster_arrive();  // every CTA's histogram is complete (and the resets above visible)
+  cluster_arrive();  // histograms complete; head info and the resets above visible
   cluster_wait();
-  for (int i = threadIdx.x; i < kCompactCluster * (kMaxT + 1); i += blockDim.x) {
-    const int c = i / (kMaxT + 1), sz = i - c * (kMaxT + 1);
-    peer[c][sz] = sz <= kp.T ? load_peer(&hist[sz], c) : 0;
+  // Warp 0: lane sz reads every CTA's count of items of size sz (distributed
+  // shared memory, all loads in flight together), then a suffix sum over the
+  // lanes gives the items of larger sizes.  Schedule: sizes T..1; within a
+  // size, CTA 0's items first.
+  if (threadIdx.x < 32) {
+    const int sz = lane;
+    int cnt[kCompactCluster];
+#pragma unroll
+    for (int c = 0; c < kCompactCluster; ++c)
+      cnt[c] = (sz >= 1 && sz <= kp.T) ? load_peer(&hist[sz], c) : 0;
+    int tot = 0, mine_before = 0;
+#pragma unroll
+    for (int c = 0; c < kCompactCluster; ++c) {
+      tot += cnt[c];
+      if (c < (int)crank) mine_before += cnt[c];
+    }
+    int suffix = tot;  // items of size >= sz
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(kFull, suffix, o);
+      if (lane + o < 32) suffix += y;
+    }
+    if (sz >= 1 && sz <= kp.T) next[sz] = suffix - tot + mine_before;
+    if (gt == 0) *ws.num_items = suffix;  // lane 0 (size 0 holds nothing)
   }
   cluster_arrive();  // this CTA is done reading the others' shared memory
   __syncthreads();
-  // Schedule: sizes T..1; within a size, CTA 0's items first.
-  if (threadIdx.x >= 1 && threadIdx.x <= kp.T) {
-    const int sz = threadIdx.x;
-    int before = 0;
-    for (int c = 0; c < kCompactCluster; ++c) {
-      for (int s2 = sz + 1; s2 <= kp.T; ++s2) before += peer[c][s2];
-      if (c < (int)crank) before += peer[c][sz];
-    }
-    next[sz] = before;
-  }
-  if (gt == 0) {
-    int total = 0;
-    for (int c = 0; c < kCompactCluster; ++c)
-      for (int sz = 1; sz <= kp.T; ++sz) total += peer[c][sz];
-    *ws.num_items = total;
-  }
-  __syncthreads();
 
-  // Phase B: item records at their schedule slots; empty-range markers.
+  // Phase B: item records at their schedule slots, sparse pairs' counts,
+  // empty-range markers.
   for (int i = 0; i < rounds; ++i) {
     const int u = i * nthreads + gt;
-    const int pair = u / S, s = u % S;
+    const int pair = u / S, s = u - pair * S;
     const UnitInfo ui = unit(i, u);
     const int n = __popc(ui.bits);
     const unsigned same = __match_any_sync(kFull, n);
@@ -193,36 +219,18 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
     if (n > 0) {
       ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
           make_int4(pair, s, (int)(ui.bits | ((uint32_t)n << 16)), ui.L | ui.flags);
+      if (ui.sparse) {
+        atomicAdd(&ws.head_info[pair].z, n);
+        atomicAdd(&ws.head_info[pair].w, 1);
+      }
     } else if (u < nunits && ui.sparse && s * kp.T < (ui.L + kTile - 1) / kTile) {
       // An empty range of a sparse row: mark its partial slot so the finish
       // pass skips it.
       for (int h = 0; h < kp.G; ++h)
         ws.partial_ml[((size_t)pair * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
     }
-  }
-
-  // Head info: first partial slot, block ranges, tiles, items.
-  for (int pair = gt; pair < npair; pair += nthreads) {
-    const int r = pair / kp.Hkv;
-    const int raw = seq_lens[r];
-    const int L = clamp_len(raw, kp.cap_tokens);
-    if (raw > kp.cap_tokens && pair % kp.Hkv == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
-    const int nb = (L + kTile - 1) / kTile;
-    const int nr = (nb + kp.T - 1) / kp.T;
-    int count = nb, nitems = nr;
-    if (modes[r] == WISE_MODE_SPARSE) {
-      count = 0;
-      nitems = 0;
-      const uint32_t* words = support ? support + (size_t)pair * kp.W : nullptr;
-      for (int w = 0; words && w * 32 < nb; ++w) {
-        const int lo = w * 32;
-        const uint32_t bits = words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u);
-        count += __popc(bits);
-        for (int g = 0; g < 32; g += kp.T)
-          nitems += ((bits >> g) & (kp.T >= 32 ? 0xffffffffu : (1u << kp.T) - 1u)) != 0u;
-      }
-    }
-    ws.head_info[pair] = make_int4(pair * S, nr, count, nitems);
+    if (u < nunits && s == 0 && pair % kp.Hkv == 0 && ui.raw > kp.cap_tokens)
+      flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
   }
   cluster_wait();  // no CTA leaves while another may still read its histogram
 }

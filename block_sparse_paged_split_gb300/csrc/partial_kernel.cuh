@@ -426,8 +426,6 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   __syncthreads();
   grid_dependency_wait();  // compaction's items, schedule and counters
 
-  const int n_items = *ws.num_items;
-
   if (warp >= C) {
     // ------------------------------------------------------------ producers
     // Warp C + c feeds consumer c; one lane does the work.  It holds the next
@@ -443,10 +441,17 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     bool nxt_ok = false, cur_ok = false;
     int k = 0;
     Prepared p{};
+    int ahead[2] = {0, 0};  // page ids of the current item's tile k (when ahead_ok)
+    bool ahead_ok = false;
     // Each consumer's first item is its own schedule slot (no atomic on the
     // launch's critical path); later ones come from the counter, offset by
     // the number of consumers in the grid.
     const int n_consumers = gridDim.x * C;
+    // The item count and the first item's record are loaded together (the
+    // record's slot is inside the item array whatever the count).
+    const int first_slot = blockIdx.x * C + c;
+    const int4 first_rec = first_slot < ws.max_items ? ws.items[first_slot] : make_int4(0, 0, 0, 0);
+    const int n_items = *ws.num_items;
     bool timed_out = false;
     while (true) {
       if (!cur_ok && nxt_ok) {
@@ -459,14 +464,14 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // (two tiles left to prepare): claiming earlier would hoard items other
       // consumers could start sooner.
       if (!nxt_ok && !exhausted && (!cur_ok || ((cur.z >> 16) & 0xff) - k <= 2)) {
-        const int slot = first_claim ? blockIdx.x * C + c : n_consumers + atomicAdd(ws.queue, 1);
-        first_claim = false;
+        const int slot = first_claim ? first_slot : n_consumers + atomicAdd(ws.queue, 1);
         if (slot < n_items) {
-          nxt = ws.items[slot];
+          nxt = first_claim ? first_rec : ws.items[slot];
           nxt_ok = true;
         } else {
           exhausted = true;
         }
+        first_claim = false;
         if (!cur_ok && nxt_ok) continue;  // start on it right away
       }
       if (cur_ok && !p.ok) {
@@ -477,12 +482,22 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         const int L = cur.w & kItemLenMask;
         const int row = rg / kp.Hkv;
         const int b = cur.y * kp.T + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 1);
-        {
-          const int32_t* pt = page_table + (size_t)row * kp.max_pages + b * (kTile / kp.P);
-          const bool two = kp.P * 2 == kTile && b * kTile + kp.P < L;
-          p.pages[0] = pt[0];
-          p.pages[1] = two ? pt[1] : 0;
+        // A tile's page ids are loaded one tile ahead (with the previous
+        // tile's), so two tiles' copies go out back to back at an item's start.
+        auto load_pages = [&](int blk, int (&pg)[2]) {
+          const int32_t* pt = page_table + (size_t)row * kp.max_pages + blk * (kTile / kp.P);
+          const bool two = kp.P * 2 == kTile && blk * kTile + kp.P < L;
+          pg[0] = pt[0];
+          pg[1] = two ? pt[1] : 0;
+        };
+        if (ahead_ok) {
+          p.pages[0] = ahead[0];
+          p.pages[1] = ahead[1];
+        } else {
+          load_pages(b, p.pages);
         }
+        ahead_ok = k + 1 < ntiles;
+        if (ahead_ok) load_pages(cur.y * kp.T + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 2), ahead);
         const int tok0 = b * kTile;
         const int rem = L - tok0;
         const int pages_in_tile = kTile / kp.P;
