@@ -152,6 +152,17 @@ __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Spreads L2 prefetches of the first `bytes` (at most 4 MiB) of a buffer over
+// every thread of the grid, one 128-byte line each.
+__device__ __forceinline__ void prefetch_l2(const void* base, size_t bytes) {
+  constexpr size_t kCap = size_t(4) << 20;
+  if (bytes > kCap) bytes = kCap;
+  const size_t lines = (bytes + 127) / 128;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += stride)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(base) + i * 128));
+}
+
 // Element-type traits: how a lane loads its DPL = D/32 consecutive elements of
 // one K or V row from shared memory and widens them to float.
 template <typename T>

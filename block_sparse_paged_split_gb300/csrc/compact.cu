@@ -53,25 +53,44 @@ struct UnitInfo {
   int raw;        // the row's length before clamping
 };
 
-// The loads of one unit (issued together; nothing here waits on them).
+// The loads of one unit (issued together; nothing here waits on them).  The
+// row's mode and length are the caller's inputs and are read before the
+// dependency wait; the mask word may come from the previous call's finish
+// pass and is read after it.
 struct UnitLoad {
   int mode, raw;
   uint32_t word;
 };
 
+__device__ __forceinline__ void unit_load_inputs(UnitLoad& l, int u, int nunits,
+                                                 const int8_t* __restrict__ modes,
+                                                 const int32_t* __restrict__ seq_lens,
+                                                 const KParams& kp) {
+  l = UnitLoad{-1, 0, 0u};
+  if (u < nunits) {
+    const int r = u / kp.S_max / kp.Hkv;
+    l.mode = modes[r];
+    l.raw = seq_lens[r];
+  }
+}
+
+__device__ __forceinline__ void unit_load_mask(UnitLoad& l, int u, int nunits,
+                                               const uint32_t* __restrict__ support,
+                                               const KParams& kp) {
+  if (u < nunits && support) {
+    const int pair = u / kp.S_max, s = u - pair * kp.S_max;
+    // s * T < max_blocks <= 32 W: the word is inside the pair's mask.
+    l.word = support[(size_t)pair * kp.W + ((s * kp.T) >> 5)];
+  }
+}
+
 __device__ __forceinline__ UnitLoad unit_load(int u, int nunits, const int8_t* __restrict__ modes,
                                               const int32_t* __restrict__ seq_lens,
                                               const uint32_t* __restrict__ support,
                                               const KParams& kp) {
-  UnitLoad l{-1, 0, 0u};
-  if (u < nunits) {
-    const int pair = u / kp.S_max, s = u - pair * kp.S_max;
-    const int r = pair / kp.Hkv;
-    l.mode = modes[r];
-    l.raw = seq_lens[r];
-    // s * T < max_blocks <= 32 W: the word is inside the pair's mask.
-    if (support) l.word = support[(size_t)pair * kp.W + ((s * kp.T) >> 5)];
-  }
+  UnitLoad l;
+  unit_load_inputs(l, u, nunits, modes, seq_lens, kp);
+  unit_load_mask(l, u, nunits, support, kp);
   return l;
 }
 
@@ -121,8 +140,6 @@ __device__ __forceinline__ int load_peer(const int* p, uint32_t rank) {
 __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompactThreads)
     compact_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                    const uint32_t* __restrict__ support, const WsView ws, const KParams kp) {
-  grid_dependency_wait();
-  grid_dependents_launch();  // the partial pass may start its prologue now
   __shared__ int hist[kMaxT + 1];                     // this CTA's items of each size
   __shared__ int next[kMaxT + 1];                     // its next schedule slot of each size
   const int lane = threadIdx.x & 31;
@@ -138,9 +155,15 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
   const int rounds = (nunits + nthreads - 1) / nthreads;
   UnitLoad ld[kCached];
 #pragma unroll
+  for (int c = 0; c < kCached; ++c) {
+    ld[c] = UnitLoad{-1, 0, 0u};
+    if (c < rounds) unit_load_inputs(ld[c], c * nthreads + gt, nunits, modes, seq_lens, kp);
+  }
+  grid_dependency_wait();    // the previous call's mask
+  grid_dependents_launch();  // the partial pass may start its prologue now
+#pragma unroll
   for (int c = 0; c < kCached; ++c)
-    ld[c] = c < rounds ? unit_load(c * nthreads + gt, nunits, modes, seq_lens, support, kp)
-                       : UnitLoad{-1, 0, 0u};
+    if (c < rounds) unit_load_mask(ld[c], c * nthreads + gt, nunits, support, kp);
   if (gt == 0) {
     *ws.status = 0;
     *ws.queue = 0;

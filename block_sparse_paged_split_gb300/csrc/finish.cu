@@ -187,8 +187,6 @@ __global__ void __launch_bounds__(1024)
                   T* __restrict__ out, float* __restrict__ lse, int wph, int npad_max) {
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ uint32_t smask[32];
-  grid_dependency_wait();    // the partial pass's results
-  grid_dependents_launch();  // the next call's compaction may start launching
   const int G = kp.G, D = kp.D;
   const int gs = wph * 32;                 // threads per query head
   const int hgrp = threadIdx.x / gs;       // query head within the KV group
@@ -211,7 +209,15 @@ __global__ void __launch_bounds__(1024)
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 
-  // The tile statistics and the old mask word go out with the first loads.
+  // Read before the dependency wait: the caller's inputs, the old mask word
+  // (its last writer finished before the partial pass began) and the head
+  // info (written by compaction, likewise complete).
+  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W)
+                                ? support[(size_t)rg * kp.W + threadIdx.x]
+                                : 0u;
+  const int4 hi = ws.head_info[rg];
+  grid_dependency_wait();    // the partial pass's results
+  grid_dependents_launch();  // the next call's compaction may start launching
   float2 st[E];
   const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
 #pragma unroll
@@ -219,10 +225,6 @@ __global__ void __launch_bounds__(1024)
     const int i = wsub * 32 * E + lane * E + e;
     st[e] = disc && i < nb ? ts[i] : make_float2(0.f, 0.f);
   }
-  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W)
-                                ? support[(size_t)rg * kp.W + threadIdx.x]
-                                : 0u;
-  const int4 hi = ws.head_info[rg];
   if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
     if (wsub == 0) {
       if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
@@ -420,8 +422,6 @@ __global__ void __launch_bounds__(256)
                         T* __restrict__ out, float* __restrict__ lse) {
   constexpr int kSlots = 8;  // short rows: at most 8 split slots
   __shared__ uint32_t smask[32];
-  grid_dependency_wait();    // the partial pass's results
-  grid_dependents_launch();  // the next call's compaction may start launching
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -432,9 +432,16 @@ __global__ void __launch_bounds__(256)
   const int mode = modes[r];
   const int nb = (L + kTile - 1) / kTile;
   const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
-  // Everything this CTA reads is addressed from the row length alone, so
-  // all loads go out together: the split slots (rg * S_max + i, i < ranges),
-  // the tile statistics and the old mask word.
+  // Read before the dependency wait: the old mask word (its last writer
+  // finished before the partial pass began) and compaction's head info.
+  const uint32_t old_word =
+      (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W) ? support[(size_t)rg * kp.W + threadIdx.x] : 0u;
+  const int4 hi = ws.head_info[rg];
+  grid_dependency_wait();    // the partial pass's results
+  grid_dependents_launch();  // the next call's compaction may start launching
+  // Everything else this CTA reads is addressed from the row length alone,
+  // so all loads go out together: the split slots (rg * S_max + i, i <
+  // ranges) and the tile statistics.
   const int nslots = (nb + kp.T - 1) / kp.T;
   const size_t slot0 = (size_t)rg * kp.S_max;
   float2 t[kSlots];
@@ -457,9 +464,6 @@ __global__ void __launch_bounds__(256)
     const int i = lane * E + e;
     st[e] = disc && e < E && i < nb ? ts[i] : make_float2(0.f, 0.f);
   }
-  const uint32_t old_word =
-      (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W) ? support[(size_t)rg * kp.W + threadIdx.x] : 0u;
-  const int4 hi = ws.head_info[rg];
 
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};

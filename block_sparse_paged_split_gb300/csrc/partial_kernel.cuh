@@ -423,6 +423,11 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       }
     fence_mbar_init();
   }
+  // The caller's inputs that every item reads first -- the page table and the
+  // query rows -- are pulled into L2 while the previous kernel finishes (a
+  // prefetch returns no data, so it may run before the dependency wait).
+  prefetch_l2(page_table, (size_t)kp.R * kp.max_pages * sizeof(int32_t));
+  prefetch_l2(q, (size_t)kp.R * kp.Hq * D * sizeof(T));
   __syncthreads();
   grid_dependency_wait();  // compaction's items, schedule and counters
 
