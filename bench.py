@@ -10,10 +10,11 @@ through its four recurrent depths, each with its own K/V pool:
     depth 2  sparse           compact + partial + finish
     depth 3  sparse           partial + finish (the mask is depth 2's)
 
-`value` is decode attention rows per second over the whole step (4 x 64
-row-calls per step).  Every kernel launch in the timed region is bracketed by
-CUDA events on the launching stream, which gives the per-mode times and the
-roofline of the dominant kernel (the split partial pass).  The same K steps
+(`--fold`: the finish folded into the partial pass, for rows of at most 64
+blocks.)  `value` is decode attention rows per second over the whole step
+(4 x 64 row-calls per step).  Every kernel launch in the timed region is
+bracketed by CUDA events on the launching stream, which gives the per-mode
+times and the roofline of the dominant kernel (the split partial pass).  The same K steps
 are also timed in dense mode (the baseline the method is compared with).
 Inputs per step are 2.1 GB of K/V (larger than the 129 MB L2).
 
@@ -53,6 +54,8 @@ def parse():
     p.add_argument("--tiles-per-item", type=int, default=0,
                    help="split work-item size (0: the library default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fold", action="store_true",
+                   help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     p.add_argument("--record-traffic", default=None, metavar="RAW_CSV",
                    help="store the DRAM bytes of the partial-kernel launches in an ncu "
@@ -225,7 +228,7 @@ class ClockSampler:
 class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
-    def __init__(self, w, tiles_per_item: int = 0):
+    def __init__(self, w, tiles_per_item: int = 0, fold: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -261,12 +264,26 @@ class Pipeline:
         sup = self.support.data_ptr()
         pt, sl = self.page_table.data_ptr(), self.seq_lens.data_ptr()
 
+        # fold=True: the partial pass with the finish folded in
+        # (wise_decode_partial_finish; one launch for rows of at most 64 blocks
+        # and 8 splits).  Measured slower than the two launches (every item
+        # then pays a device-wide release and a ticket round trip), so the
+        # step keeps them apart by default.
+        T = tiles_per_item or 8
+        self.folded = fold and w.max_blocks <= 64 and -(-w.max_blocks // T) <= 8
+
         def calls(modes_t, t, compact=True):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
             if compact:
                 c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, ws, nws, st)))
+            if self.folded:
+                c.append(("partial", lib.wise_decode_partial_finish,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, sup, self.out[t].data_ptr(),
+                           self.lse[t].data_ptr(), st)))
+                return c
             c.append(("partial", lib.wise_decode_partial,
                       (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                        pt, sl, m, ws, nws, st)))
@@ -494,7 +511,7 @@ def main_ours(args):
     build_library()
     # Weak scaling: every rank decodes its own batch (rows are independent).
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank))
-    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item)
+    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -606,7 +623,8 @@ def main_ours(args):
                      "traffic": (round(traffic) if (traffic := recorded_traffic(R, args.workload)) else None),
                      "algorithmic_bytes_per_launch": round(
                          part_bytes / sum(1 for k in per if k[2] == "partial")),
-                     "kernel": "partial_kernel (split-KV partial pass, all four depths)",
+                     "kernel": ("partial_kernel (split-KV partial pass with the finish folded in, all four depths)"
+                                if pipe.folded else "partial_kernel (split-KV partial pass, all four depths)"),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -107,6 +107,7 @@ void compute_layout(const wise_shape* s, wise_layout* l) {
   l->partial_ml = off;  off = up256(off + max_items * kp.G * sizeof(float2));
   l->partial_acc = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
   l->tile_stats = off;  off = up256(off + (size_t)kp.R * kp.Hq * kp.max_blocks * sizeof(float2));
+  l->tickets = off;     off = up256(off + pairs * sizeof(int32_t));
   l->max_items = max_items;
   l->total_bytes = off;
 }
@@ -128,6 +129,7 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v)
   v->partial_ml = reinterpret_cast<float2*>(b + l.partial_ml);
   v->partial_acc = reinterpret_cast<float*>(b + l.partial_acc);
   v->tile_stats = reinterpret_cast<float2*>(b + l.tile_stats);
+  v->tickets = reinterpret_cast<int32_t*>(b + l.tickets);
   v->max_items = (int32_t)l.max_items;
   return WISE_OK;
 }
@@ -281,10 +283,15 @@ wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "compact launch");
 }
 
-wise_status wise_decode_partial(const wise_shape* shape, const void* q, const void* k_cache,
-                                const void* v_cache, const int32_t* page_table,
-                                const int32_t* seq_lens, const int8_t* modes, void* workspace,
-                                size_t workspace_bytes, wise_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The partial pass, with the finish folded in when `fa.out` is set.
+wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
+                         const int8_t* modes, void* workspace, size_t workspace_bytes,
+                         const FoldArgs& fa, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   WsView ws;
@@ -300,9 +307,46 @@ wise_status wise_decode_partial(const wise_shape* shape, const void* q, const vo
   const KParams kp = make_params(shape);
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = shape->dtype == WISE_DTYPE_BF16
-                      ? launch_partial_bf16(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, st_)
-                      : launch_partial_f32(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, st_);
+                      ? launch_partial_bf16(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, st_)
+                      : launch_partial_f32(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, st_);
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "partial launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+wise_status wise_decode_partial(const wise_shape* shape, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* page_table,
+                                const int32_t* seq_lens, const int8_t* modes, void* workspace,
+                                size_t workspace_bytes, wise_stream_t stream) {
+  return partial_pass(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                      workspace_bytes, FoldArgs{nullptr, nullptr, nullptr}, stream);
+}
+
+wise_status wise_decode_partial_finish(const wise_shape* shape, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* page_table, const int32_t* seq_lens,
+                                       const int8_t* modes, void* workspace,
+                                       size_t workspace_bytes, uint32_t* support, void* out,
+                                       float* lse, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (!can_fold_finish(make_params(shape))) {
+    // Long rows: the two passes as separate launches.
+    st = wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                             workspace_bytes, stream);
+    if (st != WISE_OK) return st;
+    return wise_decode_finish(shape, modes, seq_lens, workspace, workspace_bytes, support, out,
+                              lse, stream);
+  }
+  if (shape->num_rows > 0 && (!out || !lse))
+    return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (shape->num_rows > 0 &&
+      (!aligned(out, 16) || !aligned(lse, 4) || (support && !aligned(support, 4))))
+    return fail(WISE_ERR_INVALID_ARG, "out must be 16-byte aligned, lse and support 4-byte");
+  return partial_pass(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                      workspace_bytes, FoldArgs{support, out, lse}, stream);
 }
 
 wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,

@@ -42,6 +42,8 @@ struct WsView {
   float2* partial_ml;  // [max_items, G], split s of rg in slot rg * S_max + s
   float* partial_acc;  // [max_items, G, D]
   float2* tile_stats;  // [R*Hq, max_blocks]
+  int32_t* tickets;    // [R*Hkv]: items of the pair completed in the running partial
+                       // pass (zeroed by compaction and by the pair's finisher)
   int32_t max_items;
 };
 

@@ -195,6 +195,7 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
       const int nb = (ui.L + kTile - 1) / kTile;
       const int nr = (nb + kp.T - 1) / kp.T;
       ws.head_info[pair] = ui.sparse ? make_int4(pair * S, nr, 0, 0) : make_int4(pair * S, nr, nb, nr);
+      ws.tickets[pair] = 0;
     }
   }
   cluster_arrive();  // histograms complete; head info and the resets above visible

@@ -22,6 +22,7 @@
 //            the row's block count cleared.
 #include <mutex>
 
+#include "finish_short.cuh"
 #include "internal.h"
 
 namespace wise {
@@ -63,12 +64,6 @@ __device__ __forceinline__ float group_max(float v, int th, int wph, float* scra
   for (int w = 1; w < wph; ++w) r = fmaxf(r, scratch[w]);
   group_sync(bar_id, wph * 32);
   return r;
-}
-
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
-  uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, o);
-  uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), o);
-  return ((uint64_t)hi << 32) | lo;
 }
 
 // One bitonic stage whose partner distance J (< E) stays within a thread's
@@ -330,104 +325,18 @@ __global__ void __launch_bounds__(1024)
 
 // ------------------------------------------------------------------ short rows
 // Rows of at most 64 blocks and 8 split slots: one warp per query head, the
-// merge in each lane over all slots (broadcast loads), and the sort in
-// registers with shuffles (E keys per lane, lane-major blocks).
-
-// Sorts the warp's 32*E keys ascending; key i lives in lane i / E, slot i % E.
-template <int E>
-__device__ __forceinline__ void warp_bitonic_sort(uint64_t (&key)[E], int lane) {
-  constexpr int N = 32 * E;
-#pragma unroll
-  for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j >= E) {
-        const int lj = j / E;  // partner lane distance
-        const bool lower = (lane & lj) == 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int i = lane * E + e;
-          const bool up = (i & k) == 0;
-          const uint64_t other = shfl_xor_u64(key[e], lj);
-          const uint64_t mn = key[e] < other ? key[e] : other;
-          const uint64_t mx = key[e] < other ? other : key[e];
-          key[e] = (lower == up) ? mn : mx;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if ((e & j) == 0) {
-            const int i = lane * E + e;
-            const bool up = (i & k) == 0;
-            const uint64_t a = key[e], b = key[e ^ j];
-            const bool swap = up ? (a > b) : (a < b);
-            key[e] = swap ? b : a;
-            key[e ^ j] = swap ? a : b;
-          }
-        }
-      }
-    }
-  }
-}
-
-// Selection over the warp's blocks: st[e] holds the (prefetched) statistics
-// of block lane * E + e.
-template <int E>
-__device__ __forceinline__ void warp_select(const float2 (&st)[2], int nb, float lse2, float eta,
-                                            uint32_t* smask, int lane) {
-  constexpr uint64_t kPad = ~0ull;
-  uint64_t key[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int i = lane * E + e;
-    if (i < nb) {
-      const float2 t = st[e];
-      const float p = t.y * exp2f(t.x - lse2);
-      key[e] = ((uint64_t)(~__float_as_uint(p)) << 32) | (uint32_t)i;
-    } else {
-      key[e] = kPad;
-    }
-  }
-  warp_bitonic_sort<E>(key, lane);
-  float pm[E];
-  float tot = 0.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    pm[e] = key[e] == kPad ? 0.f : __uint_as_float(~(uint32_t)(key[e] >> 32));
-    tot += pm[e];
-  }
-  float incl = tot;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  float before = __shfl_up_sync(kFull, incl, 1);
-  if (lane == 0) before = 0.f;
-  const bool all = eta >= 1.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if (key[e] != kPad && (all || before < eta)) {
-      const uint32_t b = (uint32_t)key[e];
-      atomicOr(&smask[b >> 5], 1u << (b & 31));
-    }
-    before += pm[e];
-  }
-}
-
+// merge in each lane over all slots, the sort in registers with shuffles
+// (finish_short.cuh); the group's selections are ORed in shared memory.
 template <typename T>
 __global__ void __launch_bounds__(256)
     finish_short_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                         const WsView ws, const KParams kp, uint32_t* __restrict__ support,
                         T* __restrict__ out, float* __restrict__ lse) {
-  constexpr int kSlots = 8;  // short rows: at most 8 split slots
-  __shared__ uint32_t smask[32];
+  __shared__ uint32_t smask[2];
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int G = kp.G, D = kp.D;
-  const int dpl = D >> 5;
-  const int h = g * G + warp;
+  const int h = g * kp.G + warp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
   const int mode = modes[r];
   const int nb = (L + kTile - 1) / kTile;
@@ -437,70 +346,25 @@ __global__ void __launch_bounds__(256)
   const uint32_t old_word =
       (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W) ? support[(size_t)rg * kp.W + threadIdx.x] : 0u;
   const int4 hi = ws.head_info[rg];
+  if (threadIdx.x < 2) smask[threadIdx.x] = 0u;
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
-  // Everything else this CTA reads is addressed from the row length alone,
-  // so all loads go out together: the split slots (rg * S_max + i, i <
-  // ranges) and the tile statistics.
-  const int nslots = (nb + kp.T - 1) / kp.T;
-  const size_t slot0 = (size_t)rg * kp.S_max;
-  float2 t[kSlots];
-  float4 a[kSlots];
-#pragma unroll
-  for (int i = 0; i < kSlots; ++i) {
-    const bool in = i < nslots;
-    const size_t idx = (slot0 + (in ? i : 0)) * G + warp;
-    t[i] = in ? ws.partial_ml[idx] : make_float2(-INFINITY, 0.f);
-    const float* ap = ws.partial_acc + idx * D + lane * dpl;
-    a[i] = dpl == 4 ? *reinterpret_cast<const float4*>(ap) : make_float4(ap[0], ap[1], 0.f, 0.f);
-  }
-  // Tile statistics in the layout of the selection: block lane * E + e,
-  // E = 1 for rows of up to 32 blocks, 2 up to 64.
-  const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
-  const int E = nb > 32 ? 2 : 1;
   float2 st[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int i = lane * E + e;
-    st[e] = disc && e < E && i < nb ? ts[i] : make_float2(0.f, 0.f);
-  }
-
-  T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
-    if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
-    else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
-    if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
-    return;
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kSlots; ++i)
-    if (t[i].y > 0.f) M = fmaxf(M, t[i].x);
-  float lam = 0.f;
-#pragma unroll
-  for (int i = 0; i < kSlots; ++i) {
-    const bool used = t[i].y > 0.f;  // an empty range's accumulator is never used
-    const float w = used ? exp2f(t[i].x - M) : 0.f;
-    lam = fmaf(t[i].y, w, lam);
-    o[0] += used ? a[i].x * w : 0.f;
-    o[1] += used ? a[i].y * w : 0.f;
-    o[2] += used ? a[i].z * w : 0.f;
-    o[3] += used ? a[i].w * w : 0.f;
-  }
-  const float inv = 1.f / lam;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) o[j] *= inv;
-  if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
-  else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
-  const float lse2 = M + log2f(lam);
-  if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
-
-  if (!disc) return;
-  if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
+  if (disc) short_load_stats<false>(ws, kp, r, h, nb, lane, st);
+  const int nslots = (L == 0 || hi.z == 0) ? 0 : (nb + kp.T - 1) / kp.T;
+  const float lse2 = short_merge_head<T, false>(ws, kp, rg, warp, nslots,
+                                                out + ((size_t)r * kp.Hq + h) * kp.D,
+                                                lse + (size_t)r * kp.Hq + h, lane);
+  if (!disc || L == 0) return;  // a padding row's mask is left as it is
   __syncthreads();
-  if (nb <= 32) warp_select<1>(st, nb, lse2, kp.eta, smask, lane);
-  else warp_select<2>(st, nb, lse2, kp.eta, smask, lane);
+  if (lse2 > -INFINITY) {
+    const uint2 w = nb > 32 ? warp_select_words<2>(st, nb, lse2, kp.eta, lane)
+                            : warp_select_words<1>(st, nb, lse2, kp.eta, lane);
+    if (lane == 0) {
+      atomicOr(&smask[0], w.x);
+      atomicOr(&smask[1], w.y);
+    }
+  }
   __syncthreads();
   if ((int)threadIdx.x < kp.W) {
     const int tw = threadIdx.x;
@@ -512,11 +376,10 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Rows of at most 64 blocks and 8 split slots take the short kernel (one
-// warp per query head); longer ones a group of wph = min(8, 32 / G) warps
-// per query head (up to 1024 threads a CTA, at most 8 keys a thread).
-static bool finish_short(const KParams& kp) { return kp.S_max <= 8 && kp.max_blocks <= 64; }
-
+// Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
+// short kernel (one warp per query head); longer ones a group of
+// wph = min(8, 32 / G) warps per query head (up to 1024 threads a CTA, at
+// most 8 keys a thread).
 static int finish_wph(const KParams& kp) { return kp.G >= 4 ? 32 / kp.G : 8; }
 
 static int finish_npad(const KParams& kp) {
@@ -554,7 +417,7 @@ template <typename T>
 static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
                                    const int32_t* seq_lens, const WsView& ws, uint32_t* support,
                                    void* out, float* lse, cudaStream_t stream) {
-  if (finish_short(kp))
+  if (can_fold_finish(kp))
     return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
                       modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
   const int wph = finish_wph(kp);

@@ -12,12 +12,25 @@ namespace wise {
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                            const uint32_t* support, const WsView& ws, cudaStream_t stream);
 
+// Where the finish pass writes when it is folded into the partial pass
+// (out == nullptr: not folded).
+struct FoldArgs {
+  uint32_t* support;
+  void* out;
+  float* lse;
+};
+
+// The folded finish handles rows of at most 64 blocks and 8 split slots.
+inline bool can_fold_finish(const KParams& kp) { return kp.S_max <= 8 && kp.max_blocks <= 64; }
+
 cudaError_t launch_partial_bf16(const KParams& kp, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const void* q, const int32_t* page_table, const int32_t* seq_lens,
-                                const int8_t* modes, const WsView& ws, cudaStream_t stream);
+                                const int8_t* modes, const WsView& ws, const FoldArgs& fa,
+                                cudaStream_t stream);
 cudaError_t launch_partial_f32(const KParams& kp, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const void* q, const int32_t* page_table, const int32_t* seq_lens,
-                               const int8_t* modes, const WsView& ws, cudaStream_t stream);
+                               const int8_t* modes, const WsView& ws, const FoldArgs& fa,
+                               cudaStream_t stream);
 
 cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,
                           const int32_t* seq_lens, const WsView& ws, uint32_t* support,

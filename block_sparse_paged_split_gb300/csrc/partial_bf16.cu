@@ -6,10 +6,11 @@ namespace wise {
 
 cudaError_t launch_partial_bf16(const KParams& kp, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const void* q, const int32_t* page_table, const int32_t* seq_lens,
-                                  const int8_t* modes, const WsView& ws, cudaStream_t stream) {
+                                  const int8_t* modes, const WsView& ws, const FoldArgs& fa,
+                                  cudaStream_t stream) {
   if (kp.D == 128)
-    return launch_partial_d<__nv_bfloat16, 128>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
-  return launch_partial_d<__nv_bfloat16, 64>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
+    return launch_partial_d<__nv_bfloat16, 128>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
+  return launch_partial_d<__nv_bfloat16, 64>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
 }
 
 }  // namespace wise

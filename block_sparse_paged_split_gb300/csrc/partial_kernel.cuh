@@ -37,6 +37,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "finish_short.cuh"
 #include "internal.h"
 
 namespace wise {
@@ -233,10 +234,77 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int half, int tok, int ch
 // exp-sums and per-tile statistics use the fp32 probabilities).  Lane
 // (g8, q4) = (lane / 4, lane % 4) holds heads 2 q4 and 2 q4 + 1 of tokens
 // g8 (+8) of each 16-token half, and dims g8 (+8) of each 16-dim block of O^T.
+// The finish pass folded into the partial pass (rows of at most 64 blocks
+// and 8 split slots): where the caller's mask, output and LSE go.  out ==
+// nullptr: not folded (a separate finish launch follows).
+template <typename T>
+struct Fold {
+  uint32_t* support;
+  T* out;
+  float* lse;
+};
+
+// Called by a consumer warp after it has written item `d`'s partial result:
+// the item is counted on its (row, KV head)'s ticket, and the warp that
+// completes the pair's last item finishes the pair (merge, output, LSE,
+// selection and mask), then puts the ticket back to 0 so a later launch over
+// the same compaction starts afresh.  nit: the pair's item count.
+template <typename T>
+__device__ __forceinline__ void fold_item_done(const WsView& ws, const KParams& kp, const Fold<T>& fold,
+                                               const int32_t* __restrict__ seq_lens,
+                                               const int8_t* __restrict__ modes, int rg, int nit,
+                                               int lane) {
+  __threadfence();  // this warp's partial result and tile statistics, before the ticket
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(ws.tickets + rg, 1) + 1 == nit;
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence();  // every other item of the pair is visible past the ticket
+  const int row = rg / kp.Hkv;
+  short_finish_pair_warp<T>(ws, kp, rg, clamp_len(seq_lens[row], kp.cap_tokens), modes[row],
+                            fold.support, fold.out, fold.lse, lane);
+  if (lane == 0) ws.tickets[rg] = 0;
+}
+
+// Pairs without any work item (padding rows, sparse rows selecting nothing)
+// are never finished by a ticket: the consumer warps write their output (0)
+// and LSE (-inf) at the start, 32 pairs a warp at a time.
+template <typename T>
+__device__ __forceinline__ void fold_empty_pairs(const WsView& ws, const KParams& kp,
+                                                 const Fold<T>& fold, int warp_id, int n_warps,
+                                                 int lane) {
+  const int npair = kp.R * kp.Hkv;
+  const int dpl = kp.D >> 5;
+  for (int base = warp_id * 32; base < npair; base += n_warps * 32) {
+    const int pr = base + lane;
+    const bool empty = pr < npair && ws.head_info[pr].w == 0;
+    unsigned todo = __ballot_sync(kFull, empty);
+    while (todo) {
+      const int e = base + __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int r = e / kp.Hkv, g = e - r * kp.Hkv;
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int hl = 0; hl < kp.G; ++hl) {
+        const size_t h = (size_t)r * kp.Hq + g * kp.G + hl;
+        T* orow = fold.out + h * kp.D + lane * dpl;
+        if (dpl == 4) Elem<T>::template store_global<4>(orow, z);
+        else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(z));
+        if (lane == 0) fold.lse[h] = -INFINITY;
+      }
+    }
+  }
+}
+
 template <int D, int G, int S, typename Cfg>
 __device__ __forceinline__ void mma_consume(const WsView& ws, const KParams& kp, uint8_t* ring_base,
                                             const StageDesc* descs, uint32_t full0,
-                                            uint32_t empty0, uint16_t* ps, int lane) {
+                                            uint32_t empty0, uint16_t* ps, int lane,
+                                            const Fold<__nv_bfloat16>& fold,
+                                            const int32_t* __restrict__ seq_lens,
+                                            const int8_t* __restrict__ modes) {
+  const bool folded = fold.out != nullptr;
+  int nit = 0;  // the current item's pair: its item count (folded finish)
   constexpr int KS = D / 16;  // 16-dim blocks: k-steps of S^T, m-tiles of O^T
   const int g8 = lane >> 2, q4 = lane & 3;
   const bool hv[2] = {2 * q4 < G, 2 * q4 + 1 < G};
@@ -260,6 +328,7 @@ __device__ __forceinline__ void mma_consume(const WsView& ws, const KParams& kp,
     const int n_valid = d.info & 255;
     const bool disc = (d.info & 1024) != 0;
     if (d.info & 256) {
+      if (folded) nit = ws.head_info[d.rg].w;
       const uint8_t* qrow = kt + 2 * Cfg::TILE_BYTES + g8 * Cfg::ROW_BYTES;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
@@ -385,6 +454,8 @@ __device__ __forceinline__ void mma_consume(const WsView& ws, const KParams& kp,
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * stage);
     ++seq;
+    if (folded && (d.info & 512))
+      fold_item_done<__nv_bfloat16>(ws, kp, fold, seq_lens, modes, d.rg, nit, lane);
   }
 }
 
@@ -393,7 +464,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     partial_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const T* __restrict__ q, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int8_t* __restrict__ modes,
-                   const WsView ws, const KParams kp) {
+                   const WsView ws, const KParams kp, const Fold<T> fold) {
   using Cfg = PartialCfg<T, D, G, C, S>;
   constexpr int DPL = Cfg::DPL;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -583,17 +654,20 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   }
 
   // ------------------------------------------------------------ consumers
+  if (fold.out != nullptr) fold_empty_pairs<T>(ws, kp, fold, blockIdx.x * C + warp, gridDim.x * C, lane);
   if constexpr (Cfg::MMA) {
     mma_consume<D, G, S, Cfg>(
         ws, kp, ring(warp), descs(warp), full_bar(warp, 0), empty_bar(warp, 0),
         reinterpret_cast<uint16_t*>(ring(warp) + Cfg::RING_BYTES + Cfg::DESC_BYTES + Cfg::BAR_BYTES),
-        lane);
+        lane, fold, seq_lens, modes);
   } else {
   const int c = warp;
   float* pbuf = reinterpret_cast<float*>(ring(c) + Cfg::RING_BYTES + Cfg::DESC_BYTES + Cfg::BAR_BYTES);
   QRegs<T, DPL> qr[G];
   float m_run[G], l_lane[G], acc[G][DPL];
   uint32_t seq = 0;
+  const bool folded = fold.out != nullptr;
+  int nit = 0;  // the current item's pair: its item count (folded finish)
   while (true) {
     const int stage = seq % S;
     if (!mbar_wait(full_bar(c, stage), (seq / S) & 1)) {
@@ -607,6 +681,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     const int n_valid = d.info & 255;
     const bool disc = (d.info & 1024) != 0;
     if (d.info & 256) {
+      if (folded) nit = ws.head_info[d.rg].w;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         qr[h].load(kt + 2 * Cfg::TILE_BYTES + h * Cfg::ROW_BYTES, lane);
@@ -692,6 +767,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(c, stage));
     ++seq;
+    if (folded && (d.info & 512)) fold_item_done<T>(ws, kp, fold, seq_lens, modes, d.rg, nit, lane);
   }
   }
 }
@@ -700,7 +776,8 @@ template <typename T, int D, int G>
 inline cudaError_t launch_partial_t(const KParams& kp, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const void* q,
                                     const int32_t* page_table, const int32_t* seq_lens,
-                                    const int8_t* modes, const WsView& ws, cudaStream_t stream) {
+                                    const int8_t* modes, const WsView& ws, const FoldArgs& fa,
+                                    cudaStream_t stream) {
   constexpr int C = PartialTune<T, D, G>::C;
   constexpr int S = PartialTune<T, D, G>::S;
   using Cfg = PartialCfg<T, D, G, C, S>;
@@ -728,20 +805,22 @@ inline cudaError_t launch_partial_t(const KParams& kp, const CUtensorMap& tmK,
     }
     grid = grid_of_device[dev];
   }
+  const Fold<T> fold{fa.support, static_cast<T*>(fa.out), fa.lse};
   return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, tmK, tmV,
-                    static_cast<const T*>(q), page_table, seq_lens, modes, ws, kp);
+                    static_cast<const T*>(q), page_table, seq_lens, modes, ws, kp, fold);
 }
 
 template <typename T, int D>
 inline cudaError_t launch_partial_d(const KParams& kp, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const void* q,
                                     const int32_t* page_table, const int32_t* seq_lens,
-                                    const int8_t* modes, const WsView& ws, cudaStream_t stream) {
+                                    const int8_t* modes, const WsView& ws, const FoldArgs& fa,
+                                    cudaStream_t stream) {
   switch (kp.G) {
-    case 1: return launch_partial_t<T, D, 1>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
-    case 2: return launch_partial_t<T, D, 2>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
-    case 4: return launch_partial_t<T, D, 4>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
-    case 8: return launch_partial_t<T, D, 8>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, stream);
+    case 1: return launch_partial_t<T, D, 1>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
+    case 2: return launch_partial_t<T, D, 2>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
+    case 4: return launch_partial_t<T, D, 4>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
+    case 8: return launch_partial_t<T, D, 8>(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, stream);
     default: return cudaErrorInvalidValue;
   }
 }

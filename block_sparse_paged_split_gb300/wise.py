@@ -55,7 +55,7 @@ class wise_shape(ctypes.Structure):
 class wise_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status_word", "num_items", "queue", "head_info", "items",
-        "partial_ml", "partial_acc", "tile_stats", "max_items", "total_bytes")]
+        "partial_ml", "partial_acc", "tile_stats", "tickets", "max_items", "total_bytes")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -76,6 +76,7 @@ def library() -> ctypes.CDLL:
             "wise_compact_tiles": [S, P, P, P, P, SZ, P],
             "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
+            "wise_decode_partial_finish": [S, P, P, P, P, P, P, P, SZ, P, P, P, P],
             "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_noalloc": [S, P, P, P, P, P, P, P, P, P, P],
             "wise_support_union": [P, P, I64, P],
@@ -178,6 +179,17 @@ def wise_decode_finish(shape, modes, seq_lens, workspace, support, out, lse, str
         _stream(stream)))
 
 
+def wise_decode_partial_finish(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                               support, out, lse, stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_partial_finish(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(support, torch.int32, "support"), _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"),
+        _stream(stream)))
+
+
 def wise_decode(shape, q, k_cache, v_cache, page_table, seq_lens, modes, support, out, lse,
                 workspace, stream=None) -> None:
     e = _elem(shape)
@@ -237,6 +249,7 @@ def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, tor
         "partial_ml": region(lay["partial_ml"], mi * G * 2, torch.float32).view(mi, G, 2),
         "partial_acc": region(lay["partial_acc"], mi * G * D, torch.float32).view(mi, G, D),
         "tile_stats": region(lay["tile_stats"], R * Hq * shape.max_blocks * 2, torch.float32).view(R, Hq, shape.max_blocks, 2),
+        "tickets": region(lay["tickets"], R * Hkv, torch.int32).view(R, Hkv),
     }
 
 

@@ -149,6 +149,9 @@ typedef struct {
   size_t partial_acc;   /* float32 [max_items, G, D]: unnormalised outputs     */
   size_t tile_stats;    /* float32x2 [R*Hq, max_blocks]: per tile max (log2
                            units of the scaled score) and exp-sum (discover)  */
+  size_t tickets;       /* int32 [R*Hkv]: items of each (row, KV head) the
+                           running wise_decode_partial_finish has completed;
+                           0 between calls                                    */
   size_t max_items;     /* capacity of the item arrays                         */
   size_t total_bytes;   /* = wise_workspace_bytes                              */
 } wise_layout;
@@ -201,6 +204,27 @@ wise_status wise_decode_finish(const wise_shape *shape, const int8_t *modes,
                                const int32_t *seq_lens, void *workspace,
                                size_t workspace_bytes, uint32_t *support,
                                void *out, float *lse, wise_stream_t stream);
+
+/* The partial pass with the finish folded in [WISE PR, "What changes": split
+ * partials, then the merge and the selection for discovery rows]: the same
+ * results as wise_decode_partial followed by wise_decode_finish, bit for
+ * bit, in one launch when every row is short (max_blocks <= 64 and
+ * ceil(max_blocks / tiles_per_item) <= 8).  Each work item is counted on
+ * its (row, KV head)'s ticket in the workspace once its partial result is
+ * written; the warp that completes a pair's last item merges the pair's
+ * splits, writes out and lse and, for discover rows, the mask.  Pairs with
+ * no item (padding rows, sparse rows selecting nothing) get out 0 and lse
+ * -inf.  Nothing waits on a ticket.  Tickets are zeroed by
+ * wise_compact_tiles and by the finishing warp, so several calls may reuse
+ * one compaction.  For longer rows the two passes are launched one after the
+ * other.  Arguments as for the two calls; out must be 16-byte aligned. */
+wise_status wise_decode_partial_finish(const wise_shape *shape, const void *q,
+                                       const void *k_cache, const void *v_cache,
+                                       const int32_t *page_table,
+                                       const int32_t *seq_lens, const int8_t *modes,
+                                       void *workspace, size_t workspace_bytes,
+                                       uint32_t *support, void *out, float *lse,
+                                       wise_stream_t stream);
 
 /* compact + partial + finish, in that order, on one stream. */
 wise_status wise_decode(const wise_shape *shape, const void *q,

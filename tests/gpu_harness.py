@@ -77,9 +77,13 @@ class Batch:
 
 
 def gpu_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
-             eta: Optional[float] = None, tiles_per_item: int = 0, stepwise: bool = True):
+             eta: Optional[float] = None, tiles_per_item: int = 0, stepwise: bool = True,
+             fused: bool = False):
     """One decode call through the C ABI; returns out (float64 numpy), lse,
-    the support after the call and the workspace views."""
+    the support after the call and the workspace views.  stepwise: compact,
+    partial and finish as three calls; fused: compact, then the partial pass
+    with the finish folded in (the benchmark's launch sequence); otherwise the
+    one-call entry point."""
     w = b.w
     shape = shape_for(w, eta, tiles_per_item)
     d = b.dev(depth)
@@ -88,7 +92,11 @@ def gpu_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
     sup = dev_support(support)
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.num_rows, w.num_q_heads), dtype=torch.float32, device="cuda")
-    if stepwise:
+    if fused:
+        W.wise_compact_tiles(shape, modes_t, b.seq_lens, sup, ws)
+        W.wise_decode_partial_finish(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, modes_t, ws, sup, out, lse)
+    elif stepwise:
         W.wise_compact_tiles(shape, modes_t, b.seq_lens, sup, ws)
         W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
                               modes_t, ws)

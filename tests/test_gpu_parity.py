@@ -343,3 +343,73 @@ def test_long_rows_match_oracle(Hq, Hkv, lens):
     m = np.array([W.MODE_SPARSE, W.MODE_DENSE] * R, np.int8)[:R]
     g, o = gpu_call(b, 2, m, s1), oracle_call(b, 2, m, s1)
     assert not compare_outputs(w, g, o)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
+def test_folded_finish_matches_two_passes_bitwise(Hq, Hkv, D, dtype):
+    """The partial pass with the finish folded in gives the partial + finish
+    results bit for bit in every mode (padding rows, a garbage mask under
+    discover, a sparse head selecting nothing), and leaves every ticket at 0."""
+    w = _wl(Hq, Hkv, D, dtype)
+    b = Batch(w)
+    R = w.num_rows
+    rng = np.random.default_rng(8)
+    bits = rng.random((R, Hkv, words(w) * 32)) < 0.3
+    sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, Hkv, -1).copy()
+    sup[1, 0] = 0  # a sparse (row, KV head) selecting nothing
+    mixed = np.array([W.MODE_SPARSE, W.MODE_DISCOVER, W.MODE_DENSE, W.MODE_DISCOVER_UNION] * 2,
+                     np.int8)[:R]
+    for m in [np.full(R, x, np.int8) for x in (0, 1, 2, 3)] + [mixed]:
+        a = gpu_call(b, 0, m, sup, stepwise=True)
+        f = gpu_call(b, 0, m, sup, fused=True)
+        assert torch.equal(a["out_raw"], f["out_raw"]), m
+        assert np.array_equal(a["lse"], f["lse"]), m
+        assert np.array_equal(a["support"], f["support"]), m
+        assert not f["ws"]["tickets"].any()
+        assert int(f["ws"]["status"][0]) == 0
+
+
+def test_folded_finish_reuses_a_compaction():
+    """Three folded calls over one compaction (tickets back to 0 after each)
+    match separate calls."""
+    w = _wl(8, 2, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    rng = np.random.default_rng(6)
+    bits = rng.random((R, 2, words(w) * 32)) < 0.4
+    sup_np = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 2, -1).copy()
+    sup = dev_support(sup_np)
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    modes = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
+    W.wise_compact_tiles(shape, modes, b.seq_lens, sup, ws)
+    outs = []
+    for depth in (0, 1, 2):
+        d = b.dev(depth)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, 8), dtype=torch.float32, device="cuda")
+        W.wise_decode_partial_finish(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, modes, ws, sup, out, lse)
+        outs.append((out.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert not W.workspace_views(shape, ws)["tickets"].any()
+    for depth, (out, lse) in zip((0, 1, 2), outs):
+        ref = gpu_call(b, depth, np.full(R, W.MODE_SPARSE, np.int8), sup_np)
+        assert torch.equal(out.cpu(), ref["out_raw"])
+        assert np.array_equal(lse.cpu().numpy(), ref["lse"])
+
+
+def test_folded_finish_matches_oracle():
+    """Discover, union-discover and sparse through the folded path against the
+    oracle (8 query heads per KV head: the tensor-core consumer folds too)."""
+    for Hq, Hkv in ((4, 4), (8, 1)):
+        w = _wl(Hq, Hkv, 128, "bf16", seed=21)
+        b = Batch(w)
+        R = w.num_rows
+        sup = np.zeros((R, Hkv, words(w)), np.uint32)
+        for depth, mode in enumerate((W.MODE_DISCOVER, W.MODE_DISCOVER_UNION, W.MODE_SPARSE)):
+            m = np.full(R, mode, np.int8)
+            g, o = gpu_call(b, depth, m, sup, fused=True), oracle_call(b, depth, m, sup)
+            assert not compare_outputs(w, g, o)
+            assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
+            sup = o["support"]
