@@ -390,6 +390,17 @@ wise_status wise_support_union(uint32_t* dst, const uint32_t* src, int64_t n_wor
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "union launch");
 }
 
+wise_status wise_support_head_union(const wise_shape* shape, uint32_t* support,
+                                    wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (shape->num_rows == 0) return WISE_OK;
+  if (!support) return fail(WISE_ERR_INVALID_ARG, "support is NULL");
+  if (!aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
+  cudaError_t e = launch_head_union(make_params(shape), support, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "head union launch");
+}
+
 wise_status wise_validate(const wise_shape* shape, const int32_t* page_table,
                           const int32_t* seq_lens, const int8_t* modes, const uint32_t* support,
                           int32_t* err_word, wise_stream_t stream) {

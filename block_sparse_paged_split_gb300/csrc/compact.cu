@@ -297,6 +297,34 @@ cudaError_t launch_union(uint32_t* dst, const uint32_t* src, int64_t n_words, cu
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------- head union
+// [WISE PR, "What changes", FlashAttention decode bullet]: sparse rows attend
+// the head union of their support.  One thread per (row, mask word): the OR
+// of the row's KV heads' words, written back to every head.
+__global__ void head_union_kernel(uint32_t* __restrict__ support, int R, int Hkv, int W) {
+  grid_dependency_wait();  // the mask from the previous kernel
+  grid_dependents_launch();
+  const int64_t n = (int64_t)R * W;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / W, w = i - r * W;
+    uint32_t* base = support + r * Hkv * W + w;
+    uint32_t u = 0u;
+    for (int g = 0; g < Hkv; ++g) u |= base[(int64_t)g * W];
+    for (int g = 0; g < Hkv; ++g) base[(int64_t)g * W] = u;
+  }
+}
+
+cudaError_t launch_head_union(const KParams& kp, uint32_t* support, cudaStream_t stream) {
+  const int64_t n = (int64_t)kp.R * kp.W;
+  if (n == 0) return cudaSuccess;
+  int grid = (int)((n + 255) / 256);
+  const int cap = sm_count() * 4;
+  if (grid > cap) grid = cap;
+  return launch_pdl(head_union_kernel, dim3(grid), dim3(256), 0, stream, support, kp.R, kp.Hkv,
+                    kp.W);
+}
+
 // --------------------------------------------------------------- validate
 __global__ void validate_kernel(const int32_t* __restrict__ page_table,
                                 const int32_t* __restrict__ seq_lens,

@@ -80,6 +80,7 @@ def library() -> ctypes.CDLL:
             "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_noalloc": [S, P, P, P, P, P, P, P, P, P, P],
             "wise_support_union": [P, P, I64, P],
+            "wise_support_head_union": [S, P, P],
             "wise_validate": [S, P, P, P, P, P, P],
         }
         for name, args in sigs.items():
@@ -219,6 +220,11 @@ def wise_support_union(dst: torch.Tensor, src: torch.Tensor, stream=None) -> Non
         raise ValueError("dst and src must have the same number of words")
     _check(library().wise_support_union(_ptr(dst, torch.int32, "dst"), _ptr(src, torch.int32, "src"),
                                         dst.numel(), _stream(stream)))
+
+
+def wise_support_head_union(shape, support, stream=None) -> None:
+    _check(library().wise_support_head_union(ctypes.byref(shape), _ptr(support, torch.int32, "support"),
+                                             _stream(stream)))
 
 
 def wise_validate(shape, page_table, seq_lens, modes, support, err_word, stream=None) -> None:

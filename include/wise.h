@@ -240,6 +240,16 @@ wise_status wise_decode(const wise_shape *shape, const void *q,
 wise_status wise_support_union(uint32_t *dst, const uint32_t *src,
                                int64_t n_words, wise_stream_t stream);
 
+/* Head union of the mask [WISE PR, "What changes", FlashAttention decode
+ * bullet: sparse rows attend the per-layer head union of their support]: for
+ * every row, each KV head's mask words become the OR of all the row's KV
+ * heads' words (support [num_rows, num_kv_heads, ceil(max_blocks / 32)],
+ * in place).  A sparse call on the result reads every selected block for
+ * every head: the page-granular variant of sparse decode, for comparison
+ * with per-head masks. */
+wise_status wise_support_head_union(const wise_shape *shape, uint32_t *support,
+                                    wise_stream_t stream);
+
 /* Checks a batch's device data and ORs WISE_BAD_* / WISE_EMPTY_SPARSE_SUPPORT
  * bits into *err_word (device int32; the caller zeroes it first).  support
  * may be NULL when no row is sparse.  Never traps; reading only. */

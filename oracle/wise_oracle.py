@@ -181,6 +181,22 @@ def support_union(dst: np.ndarray, src: np.ndarray) -> np.ndarray:
     return (np.asarray(dst, np.uint32) | np.asarray(src, np.uint32)).astype(np.uint32)
 
 
+def support_head_union(support: np.ndarray) -> np.ndarray:
+    """[WISE PR, "What changes", FlashAttention decode bullet: sparse rows
+    attend the per-layer head union of their support]: every KV head of a row
+    gets each block that any KV head of the row selected.  Bit by bit, over
+    all mask words."""
+    sup = np.asarray(support, dtype=np.uint32)
+    R, Hkv, W = sup.shape
+    out = np.zeros_like(sup)
+    for r in range(R):
+        for b in range(32 * W):
+            word, bit = b // 32, np.uint32(b % 32)
+            if any((int(sup[r, g, word]) >> int(bit)) & 1 for g in range(Hkv)):
+                out[r, :, word] |= np.uint32(1) << bit
+    return out
+
+
 def union_density(support: np.ndarray, seq_lens: np.ndarray, B: int) -> float:
     """Selected blocks of the final union over causal blocks, summed over every
     (row, KV head) with a non-empty row [author reply to the review, item 4:

@@ -10,6 +10,7 @@ What the pins compare against:
   * brute force over every subset of block masses;
   * exact closed-form selections (tests/golden/selection_cases.json);
   * the pages' density example (tests/golden/union_density_example.json);
+  * a hand-worked head-union example (tests/golden/head_union_example.json);
   * invariances the pages state: all-blocks sparse is dense bitwise, block
     masses from the LSE equal softmax block sums, the union equals the OR of
     per-depth selections; and the page layout cannot matter.
@@ -308,6 +309,30 @@ def pin_union(O) -> List[str]:
     return fails
 
 
+def pin_head_union(O) -> List[str]:
+    """Head union of a row's masks [WISE PR, "What changes", FlashAttention
+    decode bullet]: a hand-worked example (tests/golden/head_union_example.json),
+    then on random masks every head's blocks are kept and every kept block
+    has a head that selected it, row by row."""
+    with open(os.path.join(GOLDEN, "head_union_example.json")) as f:
+        gold = json.load(f)
+    fails = []
+    got = O.support_head_union(np.array(gold["support"], np.uint32))
+    if not np.array_equal(got, np.array(gold["expected"], np.uint32)):
+        fails.append(f"head union example: {got.tolist()}")
+    rng = np.random.default_rng(17)
+    sup = (rng.random((4, 3, 2 * 32)) < 0.2)
+    words = np.packbits(sup, axis=-1, bitorder="little").view(np.uint32).reshape(4, 3, 2)
+    u = O.support_head_union(words)
+    for r in range(4):
+        ub = library_bits(u[r, 0], 64)
+        if any(not np.array_equal(library_bits(u[r, g], 64), ub) for g in range(3)):
+            fails.append(f"row {r}: heads differ after the union")
+        if not np.array_equal(ub, sup[r].any(axis=0)):
+            fails.append(f"row {r}: union bits are not the blocks some head selected")
+    return fails
+
+
 def _two_block_input(hot_block: int):
     """One row, one head, D=64, 64 tokens (two causal blocks): every key of the
     hot block equals q, every other key is zero, so the hot block carries all
@@ -392,4 +417,4 @@ def pin_compaction(O) -> List[str]:
 ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_all_blocks_sparse_is_dense,
             pin_paging_invariance, pin_block_masses, pin_selection_bruteforce,
             pin_selection_golden, pin_selection_limits, pin_union, pin_density_example,
-            pin_compaction]
+            pin_compaction, pin_head_union]

@@ -413,3 +413,23 @@ def test_folded_finish_matches_oracle():
             assert not compare_outputs(w, g, o)
             assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
             sup = o["support"]
+
+
+def test_head_union_kernel_and_sparse_on_it():
+    """The head union of a row's masks (bit-exact against the oracle), then a
+    sparse call on the union against the oracle on the same mask."""
+    rng = np.random.default_rng(12)
+    for Hq, Hkv, lens in ((4, 4, RAGGED), (8, 2, np.array([3000, 100, 0, 2049], np.int32))):
+        w = _wl(Hq, Hkv, 128, "bf16", lens=lens, seed=13)
+        b = Batch(w)
+        R = w.num_rows
+        bits = rng.random((R, Hkv, words(w) * 32)) < 0.15
+        sup_np = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, Hkv, -1).copy()
+        sup = dev_support(sup_np)
+        W.wise_support_head_union(shape_for(w), sup)
+        torch.cuda.synchronize()
+        u = np_support(sup)
+        assert np.array_equal(u, O.support_head_union(sup_np))
+        m = np.full(R, W.MODE_SPARSE, np.int8)
+        g, o = gpu_call(b, 0, m, u), oracle_call(b, 0, m, u)
+        assert not compare_outputs(w, g, o)

@@ -149,11 +149,21 @@ def m_compaction_first_index_shifted(O):
     O.compact_tiles = compact_tiles
 
 
+def m_head_union_skips_last_head(O):
+    def support_head_union(support):
+        sup = np.asarray(support, dtype=np.uint32)
+        out = np.zeros_like(sup)
+        acc = np.bitwise_or.reduce(sup[:, :-1], axis=1)
+        out[:] = acc[:, None, :]
+        return out
+    O.support_head_union = support_head_union
+
+
 MUTANTS = [m_scale_squared, m_slot_off_by_one, m_page_order_reversed, m_wrong_kv_head, m_unnormalised_output,
            m_tile_sum_without_max, m_masses_drop_partial_block, m_ties_to_higher_index,
            m_strict_cutoff, m_one_extra_block, m_union_overwrites, m_mask_ignored,
            m_mask_bit_order_reversed, m_compaction_split_off_by_one,
-           m_compaction_first_index_shifted]
+           m_compaction_first_index_shifted, m_head_union_skips_last_head]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
