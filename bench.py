@@ -54,6 +54,11 @@ def parse():
     p.add_argument("--tiles-per-item", type=int, default=0,
                    help="split work-item size (0: the library default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--lse-discover", action="store_true",
+                   help="discover depths rebuild block masses from the LSE by a second read "
+                        "of K instead of recording tile statistics in the partial pass")
+    p.add_argument("--head-union", action="store_true",
+                   help="sparse depths attend the head union of each row's mask")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -228,7 +233,8 @@ class ClockSampler:
 class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
-    def __init__(self, w, tiles_per_item: int = 0, fold: bool = False):
+    def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
+                 lse_discover: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -300,11 +306,35 @@ class Pipeline:
         def all_sparse(m):
             return all(int(x) == W.MODE_SPARSE for x in m)
 
+        def lse_discover_calls(modes_t, t):
+            # Discovery the FlashAttention way: a dense call, the block masses
+            # rebuilt from its LSE by a second read of K, then the finish's
+            # selection (it merges the dense call's splits again).
+            d = self.depth[t]
+            c = calls(self.dense_modes, t)
+            c.append(("mass", lib.wise_block_mass,
+                      (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), pt, sl, modes_t.data_ptr(),
+                       self.lse[t].data_ptr(), ws, nws, st)))
+            c.append(("select", lib.wise_decode_finish,
+                      (S, modes_t.data_ptr(), sl, ws, nws, sup, self.out[t].data_ptr(),
+                       self.lse[t].data_ptr(), st)))
+            return c
+
+        def all_discover(m):
+            return all(int(x) in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION) for x in m)
+
         self.wise_step = []
         for t in range(w.num_depths):
             reuse = t > 0 and all_sparse(w.depth_modes[t]) and all_sparse(w.depth_modes[t - 1])
-            self.wise_step.append((t, depth_name(w.depth_modes[t]),
-                                   calls(self.modes[t], t, compact=not reuse)))
+            if lse_discover and all_discover(w.depth_modes[t]):
+                self.wise_step.append((t, depth_name(w.depth_modes[t]), lse_discover_calls(self.modes[t], t)))
+                continue
+            c = calls(self.modes[t], t, compact=not reuse)
+            if head_union and all_sparse(w.depth_modes[t]) and not reuse:
+                # The page-granular variant: sparse depths attend the head
+                # union of the row's mask.
+                c.insert(0, ("head_union", lib.wise_support_head_union, (S, sup, st)))
+            self.wise_step.append((t, depth_name(w.depth_modes[t]), c))
         self.dense_step = [(t, "dense", calls(self.dense_modes, t)) for t in range(w.num_depths)]
         # Sparse rows of a depth that no earlier depth discovers (a mixed
         # batch) use the support of a prior discovery of the same inputs.
@@ -511,7 +541,8 @@ def main_ours(args):
     build_library()
     # Weak scaling: every rank decodes its own batch (rows are independent).
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank))
-    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold)
+    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
+                    lse_discover=args.lse_discover)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -580,6 +611,7 @@ def main_ours(args):
         call_ms = sum(v for (t2, m2, k2), v in per.items() if t2 == tt)
         modes[f"depth{tt}_{m}"] = {
             "call_us": round(call_ms * 1e3, 2), "partial_us": round(per[(tt, m, k)] * 1e3, 2),
+            "kernels_us": {k2: round(v * 1e3, 2) for (t2, m2, k2), v in per.items() if t2 == tt},
             "rows_per_s": round(R / (call_ms * 1e-3), 1),
             "partial_gbs": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9, 1),
             "partial_frac_of_measured_hbm": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9 / peak, 3),
@@ -608,7 +640,10 @@ def main_ours(args):
         "data": "synthetic (seeded; Ouro-1.4B decode shapes, planted support)",
         "config": {"workload": f"{args.workload}: {R} rows x {int(w.seq_lens.max())} tokens, "
                                f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, D={w.head_dim}, "
-                               f"page {w.page_size}, B=32, eta={w.eta}, 4 depths",
+                               f"page {w.page_size}, B=32, eta={w.eta}, 4 depths"
+                               + (", sparse depths on the head union of the mask" if args.head_union else "")
+                               + (", discovery from the LSE (second read of K)" if args.lse_discover else "")
+                               + (", finish folded into the partial pass" if pipe.folded else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "

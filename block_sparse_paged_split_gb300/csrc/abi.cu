@@ -390,6 +390,24 @@ wise_status wise_support_union(uint32_t* dst, const uint32_t* src, int64_t n_wor
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "union launch");
 }
 
+wise_status wise_block_mass(const wise_shape* shape, const void* q, const void* k_cache,
+                            const int32_t* page_table, const int32_t* seq_lens,
+                            const int8_t* modes, const float* lse, void* workspace,
+                            size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  WsView ws;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
+  if (shape->num_rows == 0) return WISE_OK;
+  if (!q || !k_cache || !page_table || !seq_lens || !modes || !lse)
+    return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(lse, 4))
+    return fail(WISE_ERR_INVALID_ARG, "q and k_cache must be 16-byte aligned, lse 4-byte");
+  cudaError_t e = launch_block_mass(shape->dtype, make_params(shape), q, k_cache, page_table,
+                                    seq_lens, modes, lse, ws, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "block mass launch");
+}
+
 wise_status wise_support_head_union(const wise_shape* shape, uint32_t* support,
                                     wise_stream_t stream) {
   wise_status st = check_shape(shape);

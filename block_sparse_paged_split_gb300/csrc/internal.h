@@ -41,6 +41,11 @@ cudaError_t launch_union(uint32_t* dst, const uint32_t* src, int64_t n_words,
 
 cudaError_t launch_head_union(const KParams& kp, uint32_t* support, cudaStream_t stream);
 
+cudaError_t launch_block_mass(int dtype, const KParams& kp, const void* q, const void* k_cache,
+                              const int32_t* page_table, const int32_t* seq_lens,
+                              const int8_t* modes, const float* lse, const WsView& ws,
+                              cudaStream_t stream);
+
 cudaError_t launch_validate(const KParams& kp, const int32_t* page_table,
                             const int32_t* seq_lens, const int8_t* modes,
                             const uint32_t* support, int32_t* err_word, cudaStream_t stream);

@@ -81,6 +81,7 @@ def library() -> ctypes.CDLL:
             "wise_decode_noalloc": [S, P, P, P, P, P, P, P, P, P, P],
             "wise_support_union": [P, P, I64, P],
             "wise_support_head_union": [S, P, P],
+            "wise_block_mass": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_validate": [S, P, P, P, P, P, P],
         }
         for name, args in sigs.items():
@@ -220,6 +221,16 @@ def wise_support_union(dst: torch.Tensor, src: torch.Tensor, stream=None) -> Non
         raise ValueError("dst and src must have the same number of words")
     _check(library().wise_support_union(_ptr(dst, torch.int32, "dst"), _ptr(src, torch.int32, "src"),
                                         dst.numel(), _stream(stream)))
+
+
+def wise_block_mass(shape, q, k_cache, page_table, seq_lens, modes, lse, workspace,
+                    stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_block_mass(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def wise_support_head_union(shape, support, stream=None) -> None:

@@ -240,6 +240,24 @@ wise_status wise_decode(const wise_shape *shape, const void *q,
 wise_status wise_support_union(uint32_t *dst, const uint32_t *src,
                                int64_t n_words, wise_stream_t stream);
 
+/* Block masses from the LSE by a second read of K [WISE PR, "What changes",
+ * FlashAttention decode bullet: discovery rereads K once to rebuild block
+ * mass from the attention's LSE].  For every discover or discover-union row
+ * r (by `modes`), query head h and block b below the row's block count:
+ * tile_stats[r, h, b] = (lse2, sum over the block's tokens j of
+ * 2^(scale log2(e) <q_h, k_j> - lse2)), with lse2 = lse[r, h] / ln 2, so a
+ * following wise_decode_finish with the same modes selects from these
+ * masses.  lse [num_rows, num_q_heads] is the natural-log LSE of a previous
+ * finish over the same q and K (a dense call, for instance).  Reads K only;
+ * V is not touched.  Other rows are skipped.  q and k_cache must be 16-byte
+ * aligned.  The in-pass statistics of the partial pass make this pass
+ * unnecessary; it exists to measure what they save. */
+wise_status wise_block_mass(const wise_shape *shape, const void *q,
+                            const void *k_cache, const int32_t *page_table,
+                            const int32_t *seq_lens, const int8_t *modes,
+                            const float *lse, void *workspace,
+                            size_t workspace_bytes, wise_stream_t stream);
+
 /* Head union of the mask [WISE PR, "What changes", FlashAttention decode
  * bullet: sparse rows attend the per-layer head union of their support]: for
  * every row, each KV head's mask words become the OR of all the row's KV

@@ -433,3 +433,40 @@ def test_head_union_kernel_and_sparse_on_it():
         m = np.full(R, W.MODE_SPARSE, np.int8)
         g, o = gpu_call(b, 0, m, u), oracle_call(b, 0, m, u)
         assert not compare_outputs(w, g, o)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 128, "bf16"), (8, 2, 128, "bf16"),
+                                            (4, 1, 64, "bf16"), (2, 2, 64, "f32")])
+def test_block_mass_from_lse_matches_oracle(Hq, Hkv, D, dtype):
+    """Discovery without in-pass statistics: a dense call, the block masses
+    rebuilt from its LSE by a second read of K, then the finish's selection;
+    masses and masks against the oracle, outputs bitwise the dense call's."""
+    w = _wl(Hq, Hkv, D, dtype)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    d = b.dev(0)
+    sup = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    dense = torch.zeros(R, dtype=torch.int8, device="cuda")
+    disc_np = np.full(R, W.MODE_DISCOVER, np.int8)
+    disc = torch.from_numpy(disc_np).cuda()
+    out, out2 = torch.empty_like(d["q"]), torch.empty_like(d["q"])
+    lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+    lse2 = torch.empty_like(lse)
+    W.wise_compact_tiles(shape, dense, b.seq_lens, sup, ws)
+    W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens, dense, ws)
+    W.wise_decode_finish(shape, dense, b.seq_lens, ws, sup, out, lse)
+    W.wise_block_mass(shape, d["q"], d["k_cache"], b.page_table, b.seq_lens, disc, lse, ws)
+    W.wise_decode_finish(shape, disc, b.seq_lens, ws, sup, out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), out2.cpu()) and torch.equal(lse.cpu(), lse2.cpu())
+    o = oracle_call(b, 0, disc_np, np.zeros((R, Hkv, words(w)), np.uint32))
+    ts = W.workspace_views(shape, ws)["tile_stats"].cpu().numpy()
+    lse_np = lse.cpu().numpy()
+    for (r, h), dg in o["diag"].items():
+        nb = dg["p"].shape[0]
+        p_gpu = ts[r, h, :nb, 1] * np.exp2(ts[r, h, :nb, 0] - lse_np[r, h] / np.log(2.0))
+        assert np.max(np.abs(p_gpu - dg["p"])) < 1e-5, (r, h)
+    g = {"support": np_support(sup)}
+    assert not compare_masks(w, g["support"], o, disc_np)["fails"]
