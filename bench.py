@@ -6,7 +6,7 @@ One step = one decode step of one layer over the Ouro-1.4B-shaped batch
 through its four recurrent depths, each with its own K/V pool:
 
     depth 0  discover         compact + partial + finish
-    depth 1  union-discover   compact + partial + finish
+    depth 1  union-discover   partial + finish (the same work list as depth 0)
     depth 2  sparse           compact + partial + finish
     depth 3  sparse           partial + finish (the mask is depth 2's)
 
@@ -306,6 +306,18 @@ class Pipeline:
         def all_sparse(m):
             return all(int(x) == W.MODE_SPARSE for x in m)
 
+        def same_work_list(a, b):
+            # A compaction depends on each row's length (the same at every
+            # depth of a step), whether the row is sparse (then its mask) and
+            # whether it records tile statistics (discover or union-discover).
+            # Depths whose rows agree on both, with no sparse row, or whose
+            # rows are all sparse on a mask no depth between them rewrote,
+            # share one work list.
+            kind = lambda x: {W.MODE_DENSE: 0, W.MODE_DISCOVER: 1, W.MODE_DISCOVER_UNION: 1,
+                              W.MODE_SPARSE: 2}[int(x)]
+            ka, kb = [kind(x) for x in a], [kind(x) for x in b]
+            return ka == kb and (all(k != 2 for k in ka) or all(k == 2 for k in ka))
+
         def lse_discover_calls(modes_t, t):
             # Discovery the FlashAttention way: a dense call, the block masses
             # rebuilt from its LSE by a second read of K, then the finish's
@@ -325,7 +337,7 @@ class Pipeline:
 
         self.wise_step = []
         for t in range(w.num_depths):
-            reuse = t > 0 and all_sparse(w.depth_modes[t]) and all_sparse(w.depth_modes[t - 1])
+            reuse = t > 0 and same_work_list(w.depth_modes[t], w.depth_modes[t - 1])
             if lse_discover and all_discover(w.depth_modes[t]):
                 self.wise_step.append((t, depth_name(w.depth_modes[t]), lse_discover_calls(self.modes[t], t)))
                 continue

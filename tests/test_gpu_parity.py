@@ -470,3 +470,33 @@ def test_block_mass_from_lse_matches_oracle(Hq, Hkv, D, dtype):
         assert np.max(np.abs(p_gpu - dg["p"])) < 1e-5, (r, h)
     g = {"support": np_support(sup)}
     assert not compare_masks(w, g["support"], o, disc_np)["fails"]
+
+
+def test_union_depth_reuses_the_discover_compaction():
+    """A union-discover call over the discover call's compaction (the same
+    work list: same lengths, no sparse row, statistics recorded in both)
+    gives the results of its own compaction, bitwise."""
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    zero = np.zeros((R, 4, words(w)), np.uint32)
+    sup = dev_support(zero)
+    disc = torch.full((R,), W.MODE_DISCOVER, dtype=torch.int8, device="cuda")
+    union = torch.full((R,), W.MODE_DISCOVER_UNION, dtype=torch.int8, device="cuda")
+    W.wise_compact_tiles(shape, disc, b.seq_lens, sup, ws)
+    res = []
+    for depth, m in ((0, disc), (1, union)):
+        d = b.dev(depth)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, 4), dtype=torch.float32, device="cuda")
+        W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens, m, ws)
+        W.wise_decode_finish(shape, m, b.seq_lens, ws, sup, out, lse)
+        torch.cuda.synchronize()
+        res.append((out.cpu(), lse.cpu().numpy(), np_support(sup)))
+    g0 = gpu_call(b, 0, np.full(R, W.MODE_DISCOVER, np.int8), zero)
+    g1 = gpu_call(b, 1, np.full(R, W.MODE_DISCOVER_UNION, np.int8), g0["support"])
+    for (out, lse, s_), g in zip(res, (g0, g1)):
+        assert torch.equal(out, g["out_raw"]) and np.array_equal(lse, g["lse"])
+        assert np.array_equal(s_, g["support"])
