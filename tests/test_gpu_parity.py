@@ -16,11 +16,11 @@ pytestmark = pytest.mark.gpu
 RAGGED = np.array([1, 31, 32, 33, 300, 517, 0, 1024], np.int32)
 
 
-def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=3, n_planted=3):
+def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=3, n_planted=3, page_size=16):
     R = len(lens)
     return custom_workload("parity", R=R, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, depths=3,
                            n_planted=n_planted, seq_lens=lens, pool_factor=2, seed=seed,
-                           depth_modes=[np.zeros(R, np.int8)] * 3)
+                           depth_modes=[np.zeros(R, np.int8)] * 3, page_size=page_size)
 
 
 CASES = [(4, 4, 128, "bf16"), (4, 4, 64, "bf16"), (8, 2, 128, "bf16"), (4, 1, 64, "bf16"),
@@ -500,3 +500,23 @@ def test_union_depth_reuses_the_discover_compaction():
     for (out, lse, s_), g in zip(res, (g0, g1)):
         assert torch.equal(out, g["out_raw"]) and np.array_equal(lse, g["lse"])
         assert np.array_equal(s_, g["support"])
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 128, "bf16"), (4, 4, 64, "bf16"),
+                                            (8, 2, 128, "bf16"), (2, 2, 64, "f32")])
+def test_page_size_32(Hq, Hkv, D, dtype):
+    """32-token pages (one page per tile): every mode against the oracle, the
+    ragged lengths, padding row and NaN-filled pool included."""
+    w = _wl(Hq, Hkv, D, dtype, page_size=32, seed=31)
+    b = Batch(w)
+    R = w.num_rows
+    sup = np.zeros((R, Hkv, words(w)), np.uint32)
+    for depth, mode in enumerate((W.MODE_DISCOVER, W.MODE_DISCOVER_UNION, W.MODE_SPARSE)):
+        m = np.full(R, mode, np.int8)
+        g, o = gpu_call(b, depth, m, sup), oracle_call(b, depth, m, sup)
+        assert not compare_outputs(w, g, o)
+        assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
+        sup = o["support"]
+    m = np.zeros(R, np.int8)
+    g, o = gpu_call(b, 0, m, sup), oracle_call(b, 0, m, sup)
+    assert not compare_outputs(w, g, o)
