@@ -59,6 +59,9 @@ def parse():
                         "of K instead of recording tile statistics in the partial pass")
     p.add_argument("--head-union", action="store_true",
                    help="sparse depths attend the head union of each row's mask")
+    p.add_argument("--overlap", action="store_true",
+                   help="alternate the two slot sets and start a depth that reuses the previous "
+                        "compaction while the previous finish runs (measured: no gain at 1K)")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -234,7 +237,7 @@ class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
-                 lse_discover: bool = False):
+                 lse_discover: bool = False, overlap: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -278,12 +281,29 @@ class Pipeline:
         T = tiles_per_item or 8
         self.folded = fold and w.max_blocks <= 64 and -(-w.max_blocks // T) <= 8
 
-        def calls(modes_t, t, compact=True):
+        # overlap=True: consecutive depths alternate the workspace's two slot
+        # sets, and a depth that reuses the previous depth's compaction starts
+        # its partial pass while that depth's finish still runs
+        # (WISE_FLAG_EARLY_START: the partial reads nothing the finish writes).
+        # Measured: no gain at 1K -- the partial's CTAs need a whole SM, so
+        # they start only as the finish's CTAs leave -- hence off by default.
+        self.overlap = overlap and not fold and not lse_discover
+
+        def calls(modes_t, t, compact=True, early=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
             if compact:
                 c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, ws, nws, st)))
+            if self.overlap:
+                flags = (W.FLAG_SLOT_SET_1 if t % 2 else 0)
+                c.append(("partial", lib.wise_decode_partial_ex,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, flags | (W.FLAG_EARLY_START if early else 0), st)))
+                c.append(("finish", lib.wise_decode_finish_ex,
+                          (S, m, sl, ws, nws, flags, sup, self.out[t].data_ptr(),
+                           self.lse[t].data_ptr(), st)))
+                return c
             if self.folded:
                 c.append(("partial", lib.wise_decode_partial_finish,
                           (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
@@ -341,13 +361,16 @@ class Pipeline:
             if lse_discover and all_discover(w.depth_modes[t]):
                 self.wise_step.append((t, depth_name(w.depth_modes[t]), lse_discover_calls(self.modes[t], t)))
                 continue
-            c = calls(self.modes[t], t, compact=not reuse)
+            c = calls(self.modes[t], t, compact=not reuse, early=reuse)
             if head_union and all_sparse(w.depth_modes[t]) and not reuse:
                 # The page-granular variant: sparse depths attend the head
                 # union of the row's mask.
                 c.insert(0, ("head_union", lib.wise_support_head_union, (S, sup, st)))
             self.wise_step.append((t, depth_name(w.depth_modes[t]), c))
-        self.dense_step = [(t, "dense", calls(self.dense_modes, t)) for t in range(w.num_depths)]
+        # The dense baseline gets the same call sequence: one compaction for
+        # its four depths (they share the work list) and the same overlap.
+        self.dense_step = [(t, "dense", calls(self.dense_modes, t, compact=(t == 0), early=(t > 0)))
+                           for t in range(w.num_depths)]
         # Sparse rows of a depth that no earlier depth discovers (a mixed
         # batch) use the support of a prior discovery of the same inputs.
         if any(int(x) == W.MODE_SPARSE for x in w.depth_modes[0]):
@@ -554,7 +577,7 @@ def main_ours(args):
     # Weak scaling: every rank decodes its own batch (rows are independent).
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
-                    lse_discover=args.lse_discover)
+                    lse_discover=args.lse_discover, overlap=args.overlap)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -655,7 +678,8 @@ def main_ours(args):
                                f"page {w.page_size}, B=32, eta={w.eta}, 4 depths"
                                + (", sparse depths on the head union of the mask" if args.head_union else "")
                                + (", discovery from the LSE (second read of K)" if args.lse_discover else "")
-                               + (", finish folded into the partial pass" if pipe.folded else ""),
+                               + (", finish folded into the partial pass" if pipe.folded else "")
+                               + (", consecutive depths overlap (two slot sets, early start)" if pipe.overlap else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "

@@ -90,6 +90,7 @@ KParams make_params(const wise_shape* s) {
   const float scale = s->scale > 0.f ? s->scale : 1.f / std::sqrt((float)s->head_dim);
   kp.scale_log2 = scale * kLog2e;
   kp.eta = s->eta;
+  kp.early = 0;
   return kp;
 }
 
@@ -108,11 +109,16 @@ void compute_layout(const wise_shape* s, wise_layout* l) {
   l->partial_acc = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
   l->tile_stats = off;  off = up256(off + (size_t)kp.R * kp.Hq * kp.max_blocks * sizeof(float2));
   l->tickets = off;     off = up256(off + pairs * sizeof(int32_t));
+  l->partial_ml_1 = off;  off = up256(off + max_items * kp.G * sizeof(float2));
+  l->partial_acc_1 = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
+  l->tile_stats_1 = off;  off = up256(off + (size_t)kp.R * kp.Hq * kp.max_blocks * sizeof(float2));
   l->max_items = max_items;
   l->total_bytes = off;
 }
 
-wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v) {
+// slot_set: which of the two sets of split results and tile statistics the
+// view's partial_ml / partial_acc / tile_stats point at.
+wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v, int slot_set = 0) {
   wise_layout l;
   compute_layout(s, &l);
   if (!ws) return fail(WISE_ERR_WORKSPACE, "workspace is NULL");
@@ -126,9 +132,10 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v)
   v->queue_done = reinterpret_cast<int32_t*>(b + l.queue + 4);
   v->head_info = reinterpret_cast<int4*>(b + l.head_info);
   v->items = reinterpret_cast<int4*>(b + l.items);
-  v->partial_ml = reinterpret_cast<float2*>(b + l.partial_ml);
-  v->partial_acc = reinterpret_cast<float*>(b + l.partial_acc);
-  v->tile_stats = reinterpret_cast<float2*>(b + l.tile_stats);
+  v->partial_ml = reinterpret_cast<float2*>(b + (slot_set ? l.partial_ml_1 : l.partial_ml));
+  v->partial_acc = reinterpret_cast<float*>(b + (slot_set ? l.partial_acc_1 : l.partial_acc));
+  v->tile_stats = reinterpret_cast<float2*>(b + (slot_set ? l.tile_stats_1 : l.tile_stats));
+  v->partial_ml_other = reinterpret_cast<float2*>(b + (slot_set ? l.partial_ml : l.partial_ml_1));
   v->tickets = reinterpret_cast<int32_t*>(b + l.tickets);
   v->max_items = (int32_t)l.max_items;
   return WISE_OK;
@@ -291,11 +298,14 @@ namespace {
 wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_cache,
                          const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
                          const int8_t* modes, void* workspace, size_t workspace_bytes,
-                         const FoldArgs& fa, wise_stream_t stream) {
+                         const FoldArgs& fa, uint32_t flags, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
+  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START))
+    return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   WsView ws;
-  if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
+    return st;
   if (shape->num_rows == 0) return WISE_OK;
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !modes)
     return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -304,7 +314,8 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
   CUtensorMap tmK, tmV;
   if ((st = tensor_map(shape, k_cache, &tmK)) != WISE_OK) return st;
   if ((st = tensor_map(shape, v_cache, &tmV)) != WISE_OK) return st;
-  const KParams kp = make_params(shape);
+  KParams kp = make_params(shape);
+  kp.early = (flags & WISE_FLAG_EARLY_START) ? 1 : 0;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = shape->dtype == WISE_DTYPE_BF16
                       ? launch_partial_bf16(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, st_)
@@ -321,7 +332,15 @@ wise_status wise_decode_partial(const wise_shape* shape, const void* q, const vo
                                 const int32_t* seq_lens, const int8_t* modes, void* workspace,
                                 size_t workspace_bytes, wise_stream_t stream) {
   return partial_pass(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
-                      workspace_bytes, FoldArgs{nullptr, nullptr, nullptr}, stream);
+                      workspace_bytes, FoldArgs{nullptr, nullptr, nullptr}, 0u, stream);
+}
+
+wise_status wise_decode_partial_ex(const wise_shape* shape, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* page_table,
+                                   const int32_t* seq_lens, const int8_t* modes, void* workspace,
+                                   size_t workspace_bytes, uint32_t flags, wise_stream_t stream) {
+  return partial_pass(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                      workspace_bytes, FoldArgs{nullptr, nullptr, nullptr}, flags, stream);
 }
 
 wise_status wise_decode_partial_finish(const wise_shape* shape, const void* q,
@@ -346,16 +365,20 @@ wise_status wise_decode_partial_finish(const wise_shape* shape, const void* q,
       (!aligned(out, 16) || !aligned(lse, 4) || (support && !aligned(support, 4))))
     return fail(WISE_ERR_INVALID_ARG, "out must be 16-byte aligned, lse and support 4-byte");
   return partial_pass(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
-                      workspace_bytes, FoldArgs{support, out, lse}, stream);
+                      workspace_bytes, FoldArgs{support, out, lse}, 0u, stream);
 }
 
-wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,
-                               const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
-                               uint32_t* support, void* out, float* lse, wise_stream_t stream) {
+wise_status wise_decode_finish_ex(const wise_shape* shape, const int8_t* modes,
+                                  const int32_t* seq_lens, void* workspace,
+                                  size_t workspace_bytes, uint32_t flags, uint32_t* support,
+                                  void* out, float* lse, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
+  if (flags & ~(uint32_t)WISE_FLAG_SLOT_SET_1)
+    return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   WsView ws;
-  if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
+    return st;
   if (shape->num_rows == 0) return WISE_OK;
   if (!modes || !seq_lens || !out || !lse)
     return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -364,6 +387,13 @@ wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,
   cudaError_t e = launch_finish(shape->dtype, make_params(shape), modes, seq_lens, ws, support,
                                 out, lse, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "finish launch");
+}
+
+wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,
+                               const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                               uint32_t* support, void* out, float* lse, wise_stream_t stream) {
+  return wise_decode_finish_ex(shape, modes, seq_lens, workspace, workspace_bytes, 0u, support,
+                               out, lse, stream);
 }
 
 wise_status wise_decode(const wise_shape* shape, const void* q, const void* k_cache,

@@ -28,6 +28,7 @@ struct KParams {
   int cap_tokens;    // min(max_blocks * 32, max_pages * P)
   float scale_log2;  // softmax scale * log2(e): scores are kept in log2 units
   float eta;
+  int early;         // partial pass: start before the previous kernel has completed
 };
 
 // Device view of the caller's workspace (offsets from wise_workspace_layout).
@@ -40,6 +41,7 @@ struct WsView {
   int4* head_info;     // [R*Hkv]: first item, item count, tile count, 0
   int4* items;         // [max_items] in schedule order: rg, range, bitmap | count << 16, L | flags
   float2* partial_ml;  // [max_items, G], split s of rg in slot rg * S_max + s
+  float2* partial_ml_other;  // the other slot set's (compaction marks empty ranges in both)
   float* partial_acc;  // [max_items, G, D]
   float2* tile_stats;  // [R*Hq, max_blocks]
   int32_t* tickets;    // [R*Hkv]: items of the pair completed in the running partial

@@ -250,8 +250,10 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
     } else if (u < nunits && ui.sparse && s * kp.T < (ui.L + kTile - 1) / kTile) {
       // An empty range of a sparse row: mark its partial slot so the finish
       // pass skips it.
-      for (int h = 0; h < kp.G; ++h)
+      for (int h = 0; h < kp.G; ++h) {
         ws.partial_ml[((size_t)pair * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
+        ws.partial_ml_other[((size_t)pair * S + s) * kp.G + h] = make_float2(-INFINITY, 0.f);
+      }
     }
     if (u < nunits && s == 0 && pair % kp.Hkv == 0 && ui.raw > kp.cap_tokens)
       flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);

@@ -500,7 +500,12 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   prefetch_l2(page_table, (size_t)kp.R * kp.max_pages * sizeof(int32_t));
   prefetch_l2(q, (size_t)kp.R * kp.Hq * D * sizeof(T));
   __syncthreads();
-  grid_dependency_wait();  // compaction's items, schedule and counters
+  // Compaction's items, schedule and counters.  An early-start launch (the
+  // previous kernel writes nothing it reads and reads nothing it writes; the
+  // compaction it uses completed before that kernel began) skips the wait
+  // here and waits before it exits instead, so its completion still implies
+  // the previous kernel's.
+  if (!kp.early) grid_dependency_wait();
 
   if (warp >= C) {
     // ------------------------------------------------------------ producers
@@ -770,6 +775,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     if (folded && (d.info & 512)) fold_item_done<T>(ws, kp, fold, seq_lens, modes, d.rg, nit, lane);
   }
   }
+  if (kp.early && threadIdx.x == 0) grid_dependency_wait();  // see the prologue
 }
 
 template <typename T, int D, int G>

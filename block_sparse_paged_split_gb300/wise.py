@@ -55,7 +55,8 @@ class wise_shape(ctypes.Structure):
 class wise_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status_word", "num_items", "queue", "head_info", "items",
-        "partial_ml", "partial_acc", "tile_stats", "tickets", "max_items", "total_bytes")]
+        "partial_ml", "partial_acc", "tile_stats", "tickets", "partial_ml_1", "partial_acc_1",
+        "tile_stats_1", "max_items", "total_bytes")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -70,12 +71,15 @@ def library() -> ctypes.CDLL:
                                "`python -m block_sparse_paged_split_gb300.build`")
         lib = ctypes.CDLL(LIBRARY)
         P, S, I64, SZ = ctypes.c_void_p, ctypes.POINTER(wise_shape), ctypes.c_int64, ctypes.c_size_t
+        U32 = ctypes.c_uint32
         sigs = {
             "wise_workspace_bytes": [S, ctypes.POINTER(ctypes.c_size_t)],
             "wise_workspace_layout": [S, ctypes.POINTER(wise_layout)],
             "wise_compact_tiles": [S, P, P, P, P, SZ, P],
             "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
+            "wise_decode_partial_ex": [S, P, P, P, P, P, P, P, SZ, U32, P],
+            "wise_decode_finish_ex": [S, P, P, P, SZ, U32, P, P, P, P],
             "wise_decode_partial_finish": [S, P, P, P, P, P, P, P, SZ, P, P, P, P],
             "wise_decode": [S, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_noalloc": [S, P, P, P, P, P, P, P, P, P, P],
@@ -181,6 +185,30 @@ def wise_decode_finish(shape, modes, seq_lens, workspace, support, out, lse, str
         _stream(stream)))
 
 
+FLAG_SLOT_SET_1 = 1
+FLAG_EARLY_START = 2
+
+
+def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
+                           flags=0, stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_partial_ex(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        flags, _stream(stream)))
+
+
+def wise_decode_finish_ex(shape, modes, seq_lens, workspace, support, out, lse, flags=0,
+                          stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_finish_ex(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), flags,
+        _ptr(support, torch.int32, "support"), _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"),
+        _stream(stream)))
+
+
 def wise_decode_partial_finish(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                                support, out, lse, stream=None) -> None:
     e = _elem(shape)
@@ -267,6 +295,9 @@ def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, tor
         "partial_acc": region(lay["partial_acc"], mi * G * D, torch.float32).view(mi, G, D),
         "tile_stats": region(lay["tile_stats"], R * Hq * shape.max_blocks * 2, torch.float32).view(R, Hq, shape.max_blocks, 2),
         "tickets": region(lay["tickets"], R * Hkv, torch.int32).view(R, Hkv),
+        "partial_ml_1": region(lay["partial_ml_1"], mi * G * 2, torch.float32).view(mi, G, 2),
+        "partial_acc_1": region(lay["partial_acc_1"], mi * G * D, torch.float32).view(mi, G, D),
+        "tile_stats_1": region(lay["tile_stats_1"], R * Hq * shape.max_blocks * 2, torch.float32).view(R, Hq, shape.max_blocks, 2),
     }
 
 

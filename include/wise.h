@@ -152,6 +152,9 @@ typedef struct {
   size_t tickets;       /* int32 [R*Hkv]: items of each (row, KV head) the
                            running wise_decode_partial_finish has completed;
                            0 between calls                                    */
+  size_t partial_ml_1;  /* slot set 1 (WISE_FLAG_SLOT_SET_1): the same three   */
+  size_t partial_acc_1; /* regions again, so a partial pass can write its      */
+  size_t tile_stats_1;  /* splits while the previous call's finish reads set 0 */
   size_t max_items;     /* capacity of the item arrays                         */
   size_t total_bytes;   /* = wise_workspace_bytes                              */
 } wise_layout;
@@ -204,6 +207,38 @@ wise_status wise_decode_finish(const wise_shape *shape, const int8_t *modes,
                                const int32_t *seq_lens, void *workspace,
                                size_t workspace_bytes, uint32_t *support,
                                void *out, float *lse, wise_stream_t stream);
+
+/* Flags of the _ex calls. */
+enum {
+  /* Use the workspace's second set of split results and tile statistics
+   * (partial_ml_1, partial_acc_1, tile_stats_1).  A partial pass and the
+   * finish that reads it must use the same set. */
+  WISE_FLAG_SLOT_SET_1 = 1u,
+  /* Partial pass only: start streaming without waiting for the previous
+   * kernel in the stream to complete (the launch still completes after it).
+   * Legal when that kernel writes nothing this call reads and reads nothing
+   * it writes, and the compaction this call uses completed before that
+   * kernel began: for instance the finish of the previous depth, on the other
+   * slot set, when both calls share one compaction. */
+  WISE_FLAG_EARLY_START = 2u
+};
+
+/* wise_decode_partial with flags (WISE_FLAG_SLOT_SET_1, WISE_FLAG_EARLY_START);
+ * flags = 0 is wise_decode_partial.  Unknown flags: WISE_ERR_INVALID_ARG. */
+wise_status wise_decode_partial_ex(const wise_shape *shape, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *page_table, const int32_t *seq_lens,
+                                   const int8_t *modes, void *workspace,
+                                   size_t workspace_bytes, uint32_t flags,
+                                   wise_stream_t stream);
+
+/* wise_decode_finish with flags (WISE_FLAG_SLOT_SET_1 only); flags = 0 is
+ * wise_decode_finish. */
+wise_status wise_decode_finish_ex(const wise_shape *shape, const int8_t *modes,
+                                  const int32_t *seq_lens, void *workspace,
+                                  size_t workspace_bytes, uint32_t flags,
+                                  uint32_t *support, void *out, float *lse,
+                                  wise_stream_t stream);
 
 /* The partial pass with the finish folded in [WISE PR, "What changes": split
  * partials, then the merge and the selection for discovery rows]: the same

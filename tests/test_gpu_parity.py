@@ -520,3 +520,47 @@ def test_page_size_32(Hq, Hkv, D, dtype):
     m = np.zeros(R, np.int8)
     g, o = gpu_call(b, 0, m, sup), oracle_call(b, 0, m, sup)
     assert not compare_outputs(w, g, o)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_overlapped_depths_match_serial_calls(Hq, Hkv):
+    """The benchmark's overlapped schedule -- alternating slot sets, the union
+    and the second sparse depth reusing the previous compaction and starting
+    while the previous finish runs -- gives the serial calls' results
+    bitwise, every time over several back-to-back repetitions."""
+    w = _wl(Hq, Hkv, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    modes = [W.MODE_DISCOVER, W.MODE_DISCOVER_UNION, W.MODE_SPARSE, W.MODE_SPARSE]
+    mt = [torch.full((R,), m, dtype=torch.int8, device="cuda") for m in modes]
+    # serial reference
+    sup = np.zeros((R, Hkv, words(w)), np.uint32)
+    ref = []
+    for depth, m in enumerate(modes):
+        g = gpu_call(b, depth % 3, np.full(R, m, np.int8), sup)
+        ref.append(g)
+        sup = g["support"]
+    sup_t = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    outs = [torch.empty_like(b.dev(depth % 3)["q"]) for depth in range(4)]
+    lses = [torch.empty((R, Hq), dtype=torch.float32, device="cuda") for _ in range(4)]
+    for rep in range(5):
+        sup_t.zero_()
+        for depth in range(4):
+            d = b.dev(depth % 3)
+            reuse = depth in (1, 3)
+            flags = W.FLAG_SLOT_SET_1 if depth % 2 else 0
+            if not reuse:
+                W.wise_compact_tiles(shape, mt[depth], b.seq_lens, sup_t, ws)
+            W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, mt[depth], ws,
+                                     flags | (W.FLAG_EARLY_START if reuse else 0))
+            W.wise_decode_finish_ex(shape, mt[depth], b.seq_lens, ws, sup_t, outs[depth],
+                                    lses[depth], flags)
+        torch.cuda.synchronize()
+        for depth in range(4):
+            assert torch.equal(outs[depth].cpu(), ref[depth]["out_raw"]), (rep, depth)
+            assert np.array_equal(lses[depth].cpu().numpy(), ref[depth]["lse"]), (rep, depth)
+        assert np.array_equal(np_support(sup_t), ref[3]["support"])
+    assert int(W.workspace_views(shape, ws)["queue"].item()) == 0
