@@ -1,13 +1,15 @@
-// Compaction of support masks into tile lists and a balanced work list,
-// the standalone support union, and the batch validator.
+// Compaction of support masks into a balanced list of work items, the
+// support unions (across depths and across a row's KV heads), and the batch
+// validator.
 //
 // [WISE PR, "What changes"]: sparse rows walk only their selected tiles,
 // compacted first so the loop has no branch; programs cover about eight
 // tiles, so one long dense row does not set the latency of a launch whose
-// other rows are sparse.  The work list cuts every (row, KV head)'s tile list
-// in order into items of at most tiles_per_item tiles; the cut depends only
-// on that row's own mode, length and mask, so a row's result does not depend
-// on the rest of the batch.
+// other rows are sparse.  Every (row, KV head)'s blocks are cut into ranges
+// of tiles_per_item blocks; a range's tiles (all of them, or the selected
+// ones for a sparse row) form one work item.  The cut depends only on that
+// row's own mode, length and mask, so a row's result does not depend on the
+// rest of the batch.
 #include "internal.h"
 
 namespace wise {

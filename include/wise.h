@@ -26,6 +26,11 @@
  * One call of the path, on one CUDA stream:
  *     wise_compact_tiles -> wise_decode_partial -> wise_decode_finish
  * (wise_decode runs all three).  wise_support_union ORs masks kept per depth.
+ * Variants from the pages' FlashAttention decode path, built for comparison:
+ * wise_support_head_union (head-union masks) and wise_block_mass (block
+ * masses from the LSE by a second read of K); wise_decode_partial_finish
+ * folds the finish into the partial pass; the _ex calls take a second set of
+ * split slots and an early start, so consecutive calls can overlap.
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
