@@ -691,6 +691,7 @@ def main_ours(args):
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
+                     "frac_of_nominal_8000_gbs": round(achieved / 8000.0, 4),
                      "traffic": (round(traffic) if (traffic := recorded_traffic(R, args.workload)) else None),
                      "algorithmic_bytes_per_launch": round(
                          part_bytes / sum(1 for k in per if k[2] == "partial")),
