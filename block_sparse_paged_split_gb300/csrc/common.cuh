@@ -156,6 +156,33 @@ __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- clusters
+// Rank of this CTA in its thread-block cluster, the cluster barrier (every
+// thread of every CTA arrives; release/acquire at cluster scope), and a load
+// from another CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// An int in CTA `rank`'s shared memory at the address of `p` in this CTA's.
+__device__ __forceinline__ int load_peer(const int* p, uint32_t rank) {
+  uint32_t remote;
+  int v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // Spreads L2 prefetches of the first `bytes` (at most 4 MiB) of a buffer over
 // every thread of the grid, one 128-byte line each.
 __device__ __forceinline__ void prefetch_l2(const void* base, size_t bytes) {

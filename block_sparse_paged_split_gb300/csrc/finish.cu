@@ -1,10 +1,11 @@
 // Finish pass of WISE paged decode attention.
 //
 // [WISE PR, "What changes"]: a finish kernel merges the splits and runs the
-// selection for discovery rows.  One CTA per (row, KV head).  Rows of up to
-// 64 blocks use one warp per query head (finish_short_kernel); longer rows
-// give each query head a group of wph = min(8, 32 / G) warps, synchronised by
-// a named barrier of its own (finish_kernel).
+// selection for discovery rows.  Rows of up to 64 blocks: one CTA per (row,
+// KV head), one warp per query head (finish_short_kernel).  Longer rows: one
+// CTA of 8 warps per (row, query head), the G CTAs of a KV head forming a
+// thread-block cluster whose first CTA ORs the group's selections through
+// distributed shared memory (finish_kernel).
 //
 //   merge    M = max_i m_i, Lambda = sum_i l_i 2^(m_i - M),
 //            out = sum_i acc_i 2^(m_i - M) / Lambda, lse = (M + log2 Lambda) ln 2
@@ -20,8 +21,6 @@
 //            heads OR their choices in shared memory; the mask is written
 //            (DISCOVER) or ORed into (DISCOVER_UNION), with bits at or past
 //            the row's block count cleared.
-#include <mutex>
-
 #include "finish_short.cuh"
 #include "internal.h"
 
@@ -168,32 +167,37 @@ __device__ __forceinline__ void group_select(const float2 (&st)[E], int nb, floa
   }
 }
 
-// Long rows: one CTA per (row, KV head), a group of wph warps per query head.
-//   merge   the group's warps take the split slots round-robin, four loads
-//           in flight per lane, with an online rescale; the warps' (m, l,
-//           acc) are then combined through shared memory.
-//   select  npad = 32 * E * wph keys (npad >= max_blocks, a power of two;
-//           blocks past the row's n_b are padding) are sorted mostly in
+// Long rows: one CTA of kLongWarps warps per (row, query head); the G CTAs of
+// a KV head's group form one thread-block cluster, so their selections are
+// ORed through distributed shared memory (every SM of the group sorts one
+// head's keys, instead of one SM sorting all of them).
+//   merge   the warps take the split slots round-robin, four loads in flight
+//           per lane, with an online rescale; the warps' (m, l, acc) are then
+//           combined through shared memory.
+//   select  npad = 32 * E * kLongWarps keys (npad >= max_blocks, a power of
+//           two; blocks past the row's n_b are padding) are sorted mostly in
 //           registers (see group_bitonic_sort).
+constexpr int kLongWarps = 8;
+
 template <typename T, int E>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(kLongWarps * 32)
     finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                   const WsView ws, const KParams kp, uint32_t* __restrict__ support,
-                  T* __restrict__ out, float* __restrict__ lse, int wph, int npad_max) {
+                  T* __restrict__ out, float* __restrict__ lse) {
+  constexpr int wph = kLongWarps;
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ uint32_t smask[32];
   const int G = kp.G, D = kp.D;
-  const int gs = wph * 32;                 // threads per query head
-  const int hgrp = threadIdx.x / gs;       // query head within the KV group
-  const int th = threadIdx.x - hgrp * gs;  // thread within the head's group
-  const int lane = threadIdx.x & 31, wsub = th >> 5;
-  const int bar_id = 1 + hgrp;
-  // Shared memory: keys [G][npad_max] u64 | scratch [G][wph][D + 2] f32.
-  uint64_t* xbuf = reinterpret_cast<uint64_t*>(fsm) + (size_t)hgrp * npad_max;
-  float* scratch = reinterpret_cast<float*>(fsm + (size_t)G * npad_max * 8) +
-                   (size_t)hgrp * wph * (D + 2);
+  const int gs = wph * 32;
+  const int th = threadIdx.x;
+  const int lane = th & 31, wsub = th >> 5;
+  const int bar_id = 1;
+  // Shared memory: keys [npad] u64 | scratch [wph][D + 2] f32.
+  uint64_t* xbuf = reinterpret_cast<uint64_t*>(fsm);
+  float* scratch = reinterpret_cast<float*>(fsm + (size_t)32 * E * wph * 8);
 
-  const int rg = blockIdx.x;
+  const int hgrp = (int)cluster_rank();  // query head within the KV group
+  const int rg = blockIdx.x / G;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int h = g * G + hgrp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
@@ -207,8 +211,8 @@ __global__ void __launch_bounds__(1024)
   // Read before the dependency wait: the caller's inputs, the old mask word
   // (its last writer finished before the partial pass began) and the head
   // info (written by compaction, likewise complete).
-  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W)
-                                ? support[(size_t)rg * kp.W + threadIdx.x]
+  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && hgrp == 0 && th < kp.W)
+                                ? support[(size_t)rg * kp.W + th]
                                 : 0u;
   const int4 hi = ws.head_info[rg];
   grid_dependency_wait();    // the partial pass's results
@@ -220,7 +224,9 @@ __global__ void __launch_bounds__(1024)
     const int i = wsub * 32 * E + lane * E + e;
     st[e] = disc && i < nb ? ts[i] : make_float2(0.f, 0.f);
   }
-  if (L == 0 || hi.z == 0) {  // padding row, or a sparse row selecting nothing
+  // Padding rows and sparse rows selecting nothing: the whole cluster (one
+  // row and KV head) leaves here, before any cluster barrier.
+  if (L == 0 || hi.z == 0) {
     if (wsub == 0) {
       if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
       else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(1024)
       o[3] += used ? a[u].w * w : 0.f;
     }
   }
-  // Combine the group's warps: every warp forms M and Lambda, warp 0 the output.
+  // Combine the warps: every warp forms M and Lambda, warp 0 the output.
   {
     float* mine = scratch + wsub * (D + 2);
     if (lane == 0) {
@@ -306,21 +312,26 @@ __global__ void __launch_bounds__(1024)
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
   }
 
-  if (!disc) return;
+  if (!disc) return;  // the whole cluster
 
-  // ---- eta selection for this query head
-  if (threadIdx.x < 32) smask[threadIdx.x] = 0u;
+  // ---- eta selection for this query head, then the group's OR
+  if (th < 32) smask[th] = 0u;
   __syncthreads();
   group_select<E>(st, nb, lse2, kp.eta, lane, wsub, wph, xbuf, scratch, bar_id, smask);
   __syncthreads();
-  if ((int)threadIdx.x < kp.W) {
-    const int t = threadIdx.x;
-    const int lo = t * 32;
+  cluster_arrive();  // every head's choice is in its CTA's smask
+  cluster_wait();
+  if (hgrp == 0 && th < kp.W) {
+    const int lo = th * 32;
     const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
-    uint32_t w = smask[t] & valid;
+    uint32_t w = 0u;
+    for (int c = 0; c < G; ++c) w |= (uint32_t)load_peer(reinterpret_cast<const int*>(&smask[th]), c);
+    w &= valid;
     if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
-    support[(size_t)rg * kp.W + t] = w;
+    support[(size_t)rg * kp.W + th] = w;
   }
+  cluster_arrive();  // no CTA leaves while the group's first CTA may still read it
+  cluster_wait();
 }
 
 // ------------------------------------------------------------------ short rows
@@ -377,13 +388,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
-// short kernel (one warp per query head); longer ones a group of
-// wph = min(8, 32 / G) warps per query head (up to 1024 threads a CTA, at
-// most 8 keys a thread).
-static int finish_wph(const KParams& kp) { return kp.G >= 4 ? 32 / kp.G : 8; }
-
+// short kernel (one warp per query head); longer ones a CTA of kLongWarps
+// warps per query head, clustered by KV head (E = npad / 256 keys a thread).
 static int finish_npad(const KParams& kp) {
-  int n = 32 * finish_wph(kp);
+  int n = 32 * kLongWarps;
   while (n < kp.max_blocks) n <<= 1;
   return n;
 }
@@ -391,26 +399,24 @@ static int finish_npad(const KParams& kp) {
 template <typename T, int E>
 static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                                const WsView& ws, uint32_t* support, void* out, float* lse,
-                               cudaStream_t stream, int wph, int npad, size_t smem) {
-  // The shared-memory opt-in is set once per device and instantiation (so a
-  // call inside a stream capture issues only the launch).
-  static std::mutex mu;
-  static size_t configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (configured[dev] < smem) {
-      e = cudaFuncSetAttribute(finish_kernel<T, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e != cudaSuccess) return e;
-      configured[dev] = smem;
-    }
-  }
-  return launch_pdl(finish_kernel<T, E>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G * wph), smem, stream,
-                    modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse, wph, npad);
+                               cudaStream_t stream) {
+  const size_t smem = (size_t)32 * E * kLongWarps * 8 + (size_t)kLongWarps * (kp.D + 2) * 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kp.R * kp.Hkv * kp.G);
+  cfg.blockDim = dim3(kLongWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kp.G;  // the KV head's query heads (at most 8: portable)
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, finish_kernel<T, E>, modes, seq_lens, ws, kp, support,
+                            static_cast<T*>(out), lse);
 }
 
 template <typename T>
@@ -420,15 +426,10 @@ static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
   if (can_fold_finish(kp))
     return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
                       modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
-  const int wph = finish_wph(kp);
-  const int npad = finish_npad(kp);
-  const int E = npad / (32 * wph);  // 1, 2, 4 or 8 keys per thread
-  const size_t smem = (size_t)kp.G * npad * 8 + (size_t)kp.G * wph * (kp.D + 2) * 4;
-  switch (E) {
-    case 1: return launch_long<T, 1>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
-    case 2: return launch_long<T, 2>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
-    case 4: return launch_long<T, 4>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
-    default: return launch_long<T, 8>(kp, modes, seq_lens, ws, support, out, lse, stream, wph, npad, smem);
+  switch (finish_npad(kp) / (32 * kLongWarps)) {
+    case 1: return launch_long<T, 1>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    case 2: return launch_long<T, 2>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    default: return launch_long<T, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
   }
 }
 
