@@ -233,6 +233,25 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def pack(tensors, device):
+    """One byte buffer holding the tensors back to back (each at a 256-byte
+    aligned offset) and views of it with the tensors' shapes and dtypes (on
+    the CPU the buffer is pinned and the views hold the tensors' values)."""
+    import torch
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=device.type == "cpu")
+    views = []
+    for t, o in zip(tensors, offs):
+        v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        if device.type == "cpu":
+            v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
@@ -255,17 +274,31 @@ class Pipeline:
                                   eta=w.eta, tiles_per_item=tiles_per_item)
         dev = torch.device("cuda")
         self.host = [w.depth_inputs(t) for t in range(w.num_depths)]
-        self.depth = [{k: v.to(dev) for k, v in d.items()} for d in self.host]
-        self.page_table = torch.from_numpy(w.page_table).to(dev)
-        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
-        self.modes = [torch.from_numpy(m).to(dev) for m in w.depth_modes]
+        self.depth = [{k: v.to(dev) for k, v in d.items() if k != "q"} for d in self.host]
+        # The per-step inputs (every depth's q, the page table, the lengths,
+        # every depth's modes) live in one device buffer and the per-step
+        # outputs (every depth's out and lse, the mask) in another, so a step
+        # moves its inputs and results with one copy each way.
+        ins = ([d["q"] for d in self.host] + [torch.from_numpy(w.page_table),
+               torch.from_numpy(w.seq_lens)] + [torch.from_numpy(m) for m in w.depth_modes])
+        self.in_host, in_views = pack(ins, torch.device("cpu"))
+        self.in_dev, in_dev_views = pack(ins, dev)
+        self.in_dev.copy_(self.in_host)
+        nd = w.num_depths
+        for t in range(nd):
+            self.depth[t]["q"] = in_dev_views[t]
+        self.page_table, self.seq_lens = in_dev_views[nd], in_dev_views[nd + 1]
+        self.modes = in_dev_views[nd + 2:]
         self.dense_modes = torch.zeros(w.num_rows, dtype=torch.int8, device=dev)
-        self.support = torch.zeros((w.num_rows, w.num_kv_heads, W.mask_words(self.shape)),
-                                   dtype=torch.int32, device=dev)
+        outs = ([torch.empty(d["q"].shape, dtype=d["q"].dtype) for d in self.host] +
+                [torch.empty((w.num_rows, w.num_q_heads), dtype=torch.float32) for _ in self.host] +
+                [torch.zeros((w.num_rows, w.num_kv_heads, W.mask_words(self.shape)), dtype=torch.int32)])
+        self.out_dev, out_views = pack(outs, dev)
+        self.out_dev.zero_()
+        self.out = out_views[:nd]
+        self.lse = out_views[nd:2 * nd]
+        self.support = out_views[2 * nd]
         self.ws = W.alloc_workspace(self.shape)
-        self.out = [torch.empty_like(d["q"]) for d in self.depth]
-        self.lse = [torch.empty((w.num_rows, w.num_q_heads), dtype=torch.float32, device=dev)
-                    for _ in self.depth]
         self.stream = torch.cuda.current_stream()
         S = ctypes.byref(self.shape)
         st = self.stream.cuda_stream
@@ -479,34 +512,19 @@ def graph_region(pipe, graph, K, dist):
 
 
 def e2e_region(pipe, K):
-    """The same step through the C ABI from pinned host buffers: every step
-    copies its per-call inputs (q of each depth, page table, lengths, modes)
-    host -> device and reads the outputs (out, lse of each depth, the mask)
-    back, all inside the timed region."""
+    """The same step through the C ABI from pinned host memory: every step
+    copies its inputs (q of each depth, page table, lengths, modes: one
+    packed buffer) host -> device and reads its results (out and lse of each
+    depth, the mask: one packed buffer) back, inside the timed region."""
     import torch
-    w = pipe.w
-    pin = lambda t: t.pin_memory()
-    h_q = [pin(d["q"]) for d in pipe.host]
-    h_pt = pin(torch.from_numpy(w.page_table))
-    h_sl = pin(torch.from_numpy(w.seq_lens))
-    h_modes = [pin(torch.from_numpy(m)) for m in w.depth_modes]
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in pipe.out]
-    h_lse = [torch.empty(l.shape, dtype=l.dtype).pin_memory() for l in pipe.lse]
-    h_sup = torch.empty(pipe.support.shape, dtype=pipe.support.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_q + [h_pt, h_sl] + h_modes)
-    d2h = sum(t.numel() * t.element_size() for t in h_out + h_lse + [h_sup])
+    h_out = torch.empty(pipe.out_dev.shape, dtype=pipe.out_dev.dtype).pin_memory()
+    h2d = pipe.in_host.numel() * pipe.in_host.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def one():
-        for t in range(w.num_depths):
-            pipe.depth[t]["q"].copy_(h_q[t], non_blocking=True)
-            pipe.modes[t].copy_(h_modes[t], non_blocking=True)
-        pipe.page_table.copy_(h_pt, non_blocking=True)
-        pipe.seq_lens.copy_(h_sl, non_blocking=True)
+        pipe.in_dev.copy_(pipe.in_host, non_blocking=True)
         pipe.run(pipe.wise_step)
-        for t in range(w.num_depths):
-            h_out[t].copy_(pipe.out[t], non_blocking=True)
-            h_lse[t].copy_(pipe.lse[t], non_blocking=True)
-        h_sup.copy_(pipe.support, non_blocking=True)
+        h_out.copy_(pipe.out_dev, non_blocking=True)
 
     for _ in range(3):
         one()
