@@ -128,7 +128,7 @@ def run_oracle_sample(workload: str, rows: int, reps: int) -> dict:
 
 # ----------------------------------------------------------------------------- traffic
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_kernel_traffic.json")
-KERNEL_SOURCES = ("partial_kernel.cuh", "partial_bf16.cu", "common.cuh", "internal.h")
+KERNEL_SOURCES = ("partial_kernel.cuh", "partial_bf16.cu", "finish_short.cuh", "common.cuh", "internal.h")
 
 
 def kernel_source_hash() -> str:

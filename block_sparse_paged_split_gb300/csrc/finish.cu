@@ -54,17 +54,6 @@ __device__ __forceinline__ float group_exclusive_scan(float v, int th, int wph, 
   return before + incl - v;
 }
 
-__device__ __forceinline__ float group_max(float v, int th, int wph, float* scratch, int bar_id) {
-  const float m = warp_max(v);
-  if (wph == 1) return m;
-  if ((th & 31) == 0) scratch[th >> 5] = m;
-  group_sync(bar_id, wph * 32);
-  float r = scratch[0];
-  for (int w = 1; w < wph; ++w) r = fmaxf(r, scratch[w]);
-  group_sync(bar_id, wph * 32);
-  return r;
-}
-
 // One bitonic stage whose partner distance J (< E) stays within a thread's
 // registers; `base` is the group-wide index of the thread's key 0.
 template <int E, int J>

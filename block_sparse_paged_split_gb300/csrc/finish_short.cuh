@@ -22,7 +22,6 @@
 namespace wise {
 
 constexpr int kShortSlots = 8;    // split slots of a short row, at most
-constexpr int kShortBlocks = 64;  // blocks of a short row, at most
 
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
   uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, o);
