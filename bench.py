@@ -652,9 +652,11 @@ def main_ours(args):
     part_ms = sum(v for (tt, m, k), v in per.items() if k == "partial")
     achieved = part_bytes / (part_ms * 1e-3) / 1e9
     # Kernels launched in the timed regions: the graph replays and the eager
-    # passes, each over K WISE steps and K dense steps.
-    launches = 2 * (pipe.launches_per_step(pipe.wise_step) +
-                    pipe.launches_per_step(pipe.dense_step)) * args.steps
+    # passes, each over K WISE steps and K dense steps, and the end-to-end
+    # region's K WISE steps.
+    launches = (2 * (pipe.launches_per_step(pipe.wise_step) +
+                     pipe.launches_per_step(pipe.dense_step)) +
+                pipe.launches_per_step(pipe.wise_step)) * args.steps
 
     R = w.num_rows
     modes = {}

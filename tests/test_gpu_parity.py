@@ -565,3 +565,26 @@ def test_overlapped_depths_match_serial_calls(Hq, Hkv):
             assert np.array_equal(lses[depth].cpu().numpy(), ref[depth]["lse"]), (rep, depth)
         assert np.array_equal(np_support(sup_t), ref[3]["support"])
     assert int(W.workspace_views(shape, ws)["queue"].item()) == 0
+
+
+def test_compaction_beyond_cached_rounds():
+    """More work units than the compaction keeps in registers (40 rows x 1024
+    ranges of one block = 40,960 > 4 x 8192): the units past the cached rounds
+    are looked up again; items, masks and outputs against the oracle."""
+    rng = np.random.default_rng(23)
+    lens = np.concatenate([[32768], rng.integers(0, 500, size=39)]).astype(np.int32)
+    R = len(lens)
+    w = custom_workload("units", R=R, Hq=1, Hkv=1, D=128, dtype="bf16", depths=2, n_planted=3,
+                        seq_lens=lens, pool_factor=1, seed=29,
+                        depth_modes=[np.zeros(R, np.int8)] * 2)
+    assert w.max_blocks == 1024
+    b = Batch(w)
+    zero = np.zeros((R, 1, words(w)), np.uint32)
+    m = np.array([W.MODE_DISCOVER, W.MODE_DENSE, W.MODE_DISCOVER_UNION, W.MODE_SPARSE] * 10, np.int8)
+    prior = oracle_call(b, 1, np.full(R, W.MODE_DISCOVER, np.int8), zero)["support"]
+    sup = np.where((m == W.MODE_SPARSE)[:, None, None], prior, zero)
+    g, o = gpu_call(b, 0, m, sup, tiles_per_item=1), oracle_call(b, 0, m, sup)
+    assert not compare_outputs(w, g, o)
+    assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
+    ref = O.compact_tiles(sup, m, lens, 32, 1)
+    assert int(g["ws"]["num_items"][0]) == ref["items"].shape[0]
