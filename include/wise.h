@@ -125,7 +125,8 @@ typedef struct {
                                 a row's capacity is min(max_blocks * 32,
                                 max_pages_per_row * page_size) tokens          */
   int32_t tiles_per_item;    /* blocks per split range T: 1, 2, 4, 8 or 16;
-                                0 means 8.  Work item s of a (row, KV head)
+                                0 means 8, or 16 when max_blocks > 64.
+                                Work item s of a (row, KV head)
                                 holds its tiles in blocks [s*T, s*T + T)   */
   int32_t dtype;             /* WISE_DTYPE_* of q, k_cache, v_cache and out     */
   float scale;               /* softmax scale; 0 means 1/sqrt(head_dim)         */
