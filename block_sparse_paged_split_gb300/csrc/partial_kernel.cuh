@@ -101,7 +101,10 @@ struct PartialTune {
   static constexpr int S = UseMma<T, G>::value ? 2 : 3;
   static constexpr int STAGE_BYTES = PartialCfg<T, D, G, 1, S>::CONSUMER_BYTES;
   static constexpr int C_RAW = (222 * 1024) / STAGE_BYTES;
-  static constexpr int C = C_RAW > 12 ? 12 : (C_RAW < 1 ? 1 : C_RAW);
+  // At most 8 tensor-core consumers (their 2 x C warps keep ~128 registers
+  // a thread), 12 FMA ones.
+  static constexpr int C_MAX = UseMma<T, G>::value ? 8 : 12;
+  static constexpr int C = C_RAW > C_MAX ? C_MAX : (C_RAW < 1 ? 1 : C_RAW);
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
