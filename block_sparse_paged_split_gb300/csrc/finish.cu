@@ -156,24 +156,25 @@ __device__ __forceinline__ void group_select(const float2 (&st)[E], int nb, floa
   }
 }
 
-// Long rows: one CTA of kLongWarps warps per (row, query head); the G CTAs of
+// Long rows: one CTA of W warps per (row, query head); the G CTAs of
 // a KV head's group form one thread-block cluster, so their selections are
 // ORed through distributed shared memory (every SM of the group sorts one
 // head's keys, instead of one SM sorting all of them).
 //   merge   the warps take the split slots round-robin, four loads in flight
 //           per lane, with an online rescale; the warps' (m, l, acc) are then
 //           combined through shared memory.
-//   select  npad = 32 * E * kLongWarps keys (npad >= max_blocks, a power of
+//   select  npad = 32 * E * W keys (npad >= max_blocks, a power of
 //           two; blocks past the row's n_b are padding) are sorted mostly in
 //           registers (see group_bitonic_sort).
-constexpr int kLongWarps = 8;
+// W = 4 warps a head for up to 512 keys, 8 beyond (same-box A/B: 4 warps
+// made the 4K finish 18.7 -> 12.6 us, 8 warps stay best at 1024 keys).
 
-template <typename T, int E>
-__global__ void __launch_bounds__(kLongWarps * 32)
+template <typename T, int E, int W>
+__global__ void __launch_bounds__(W * 32)
     finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
                   const WsView ws, const KParams kp, uint32_t* __restrict__ support,
                   T* __restrict__ out, float* __restrict__ lse) {
-  constexpr int wph = kLongWarps;
+  constexpr int wph = W;
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ uint32_t smask[32];
   const int G = kp.G, D = kp.D;
@@ -377,22 +378,24 @@ __global__ void __launch_bounds__(256)
 }
 
 // Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
-// short kernel (one warp per query head); longer ones a CTA of kLongWarps
-// warps per query head, clustered by KV head (E = npad / 256 keys a thread).
+// short kernel (one warp per query head); longer ones a CTA of W warps per
+// query head, clustered by KV head (E = npad / (32 W) keys a thread).
+static int finish_warps(const KParams& kp) { return kp.max_blocks <= 512 ? 4 : 8; }
+
 static int finish_npad(const KParams& kp) {
-  int n = 32 * kLongWarps;
+  int n = 32 * finish_warps(kp);
   while (n < kp.max_blocks) n <<= 1;
   return n;
 }
 
-template <typename T, int E>
+template <typename T, int E, int W>
 static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                                const WsView& ws, uint32_t* support, void* out, float* lse,
                                cudaStream_t stream) {
-  const size_t smem = (size_t)32 * E * kLongWarps * 8 + (size_t)kLongWarps * (kp.D + 2) * 4;
+  const size_t smem = (size_t)32 * E * W * 8 + (size_t)W * (kp.D + 2) * 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kp.R * kp.Hkv * kp.G);
-  cfg.blockDim = dim3(kLongWarps * 32);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -404,7 +407,7 @@ static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, finish_kernel<T, E>, modes, seq_lens, ws, kp, support,
+  return cudaLaunchKernelEx(&cfg, finish_kernel<T, E, W>, modes, seq_lens, ws, kp, support,
                             static_cast<T*>(out), lse);
 }
 
@@ -415,10 +418,19 @@ static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
   if (can_fold_finish(kp))
     return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
                       modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
-  switch (finish_npad(kp) / (32 * kLongWarps)) {
-    case 1: return launch_long<T, 1>(kp, modes, seq_lens, ws, support, out, lse, stream);
-    case 2: return launch_long<T, 2>(kp, modes, seq_lens, ws, support, out, lse, stream);
-    default: return launch_long<T, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
+  const int w = finish_warps(kp);
+  const int e = finish_npad(kp) / (32 * w);
+  if (w == 4) {
+    switch (e) {  // npad <= 512: e <= 4
+      case 1: return launch_long<T, 1, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
+      case 2: return launch_long<T, 2, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
+      default: return launch_long<T, 4, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    }
+  }
+  switch (e) {  // npad = 1024 with 8 warps: e = 4
+    case 1: return launch_long<T, 1, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    case 2: return launch_long<T, 2, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    default: return launch_long<T, 4, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
   }
 }
 

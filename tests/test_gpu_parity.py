@@ -312,15 +312,15 @@ def test_seq_len_above_capacity_is_clamped_and_flagged():
     assert int(v["head_info"][0, 0, 2].item()) == -(-cap // 32)
 
 
-# Long rows take the multi-warp finish kernel: one CTA of 8 warps per query
-# head, the KV head's query heads as one thread-block cluster; its sort keeps
-# E = (padded block count) / 256 keys per thread.  One case per layout and
-# cluster size.
+# Long rows take the multi-warp finish kernel: one CTA of W warps per query
+# head (4 up to 512 blocks, 8 beyond), the KV head's query heads as one
+# thread-block cluster; its sort keeps E = (padded block count) / (32 W) keys
+# per thread.  One case per layout and cluster size.
 LONG_CASES = [
-    (2, 2, np.array([3000, 100, 0, 2049], np.int32)),         # G=1, 94 blocks -> E=1
-    (4, 2, np.array([10000, 5000, 1, 33], np.int32)),         # G=2, 313 blocks -> E=2
-    (4, 1, np.array([20000, 700, 9999], np.int32)),           # G=4, 625 blocks -> E=4
-    (8, 1, np.array([20000, 3000, 700, 100, 17000], np.int32)),  # G=8 (cluster of 8), E=4
+    (2, 2, np.array([3000, 100, 0, 2049], np.int32)),         # G=1, 94 blocks: W=4, E=1
+    (4, 2, np.array([10000, 5000, 1, 33], np.int32)),         # G=2, 313 blocks: W=4, E=4
+    (4, 1, np.array([20000, 700, 9999], np.int32)),           # G=4, 625 blocks: W=8, E=4
+    (8, 1, np.array([20000, 3000, 700, 100, 17000], np.int32)),  # G=8 (cluster of 8): W=8, E=4
 ]
 
 
