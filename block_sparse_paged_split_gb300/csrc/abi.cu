@@ -82,9 +82,16 @@ KParams make_params(const wise_shape* s) {
   kp.num_pages = s->num_pages;
   kp.max_blocks = s->max_blocks;
   kp.W = (s->max_blocks + 31) / 32;
-  // Default split: 8 tiles; 16 when rows can exceed 64 blocks (fewer claims
-  // and split slots; measured faster at 4K-32K tokens, slower at 1K).
-  kp.T = s->tiles_per_item ? s->tiles_per_item : (s->max_blocks > 64 ? 16 : 8);
+  // Default split: 8 tiles; 16 when rows can exceed 64 blocks and the batch
+  // still gives ~4 items of 16 tiles per consumer of a GB300 (fewer claims
+  // and split slots: measured faster at 4K-32K tokens over 8-64 rows; with
+  // fewer items the longer ones leave consumers idle at the end).
+  if (s->tiles_per_item) {
+    kp.T = s->tiles_per_item;
+  } else {
+    const int64_t items16 = (int64_t)s->num_rows * s->num_kv_heads * ((s->max_blocks + 15) / 16);
+    kp.T = (s->max_blocks > 64 && items16 >= 4096) ? 16 : 8;
+  }
   kp.S_max = (s->max_blocks + kp.T - 1) / kp.T;
   const int64_t cap_a = (int64_t)s->max_blocks * kTile;
   const int64_t cap_b = (int64_t)s->max_pages_per_row * s->page_size;

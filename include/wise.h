@@ -125,7 +125,9 @@ typedef struct {
                                 a row's capacity is min(max_blocks * 32,
                                 max_pages_per_row * page_size) tokens          */
   int32_t tiles_per_item;    /* blocks per split range T: 1, 2, 4, 8 or 16;
-                                0 means 8, or 16 when max_blocks > 64.
+                                0 means 8, or 16 when max_blocks > 64 and
+                                num_rows * num_kv_heads * ceil(max_blocks /
+                                16) >= 4096.
                                 Work item s of a (row, KV head)
                                 holds its tiles in blocks [s*T, s*T + T)   */
   int32_t dtype;             /* WISE_DTYPE_* of q, k_cache, v_cache and out     */
