@@ -511,11 +511,13 @@ def graph_region(pipe, graph, K, dist):
     return s.elapsed_time(e)
 
 
-def e2e_region(pipe, K):
+def e2e_region(pipe, K, graph=None):
     """The same step through the C ABI from pinned host memory: every step
     copies its inputs (q of each depth, page table, lengths, modes: one
     packed buffer) host -> device and reads its results (out and lse of each
-    depth, the mask: one packed buffer) back, inside the timed region."""
+    depth, the mask: one packed buffer) back, inside the timed region.  The
+    step's ABI calls run from `graph` (their capture, as an engine replays
+    its decode step) or, without one, one by one."""
     import torch
     h_out = torch.empty(pipe.out_dev.shape, dtype=pipe.out_dev.dtype).pin_memory()
     h2d = pipe.in_host.numel() * pipe.in_host.element_size()
@@ -523,7 +525,10 @@ def e2e_region(pipe, K):
 
     def one():
         pipe.in_dev.copy_(pipe.in_host, non_blocking=True)
-        pipe.run(pipe.wise_step)
+        if graph is not None:
+            graph.replay()
+        else:
+            pipe.run(pipe.wise_step)
         h_out.copy_(pipe.out_dev, non_blocking=True)
 
     for _ in range(3):
@@ -652,11 +657,11 @@ def main_ours(args):
     part_ms = sum(v for (tt, m, k), v in per.items() if k == "partial")
     achieved = part_bytes / (part_ms * 1e-3) / 1e9
     # Kernels launched in the timed regions: the graph replays and the eager
-    # passes, each over K WISE steps and K dense steps, and the end-to-end
-    # region's K WISE steps.
+    # passes, each over K WISE steps and K dense steps, and the two end-to-end
+    # regions' K WISE steps each.
     launches = (2 * (pipe.launches_per_step(pipe.wise_step) +
                      pipe.launches_per_step(pipe.dense_step)) +
-                pipe.launches_per_step(pipe.wise_step)) * args.steps
+                2 * pipe.launches_per_step(pipe.wise_step)) * args.steps
 
     R = w.num_rows
     modes = {}
@@ -682,9 +687,10 @@ def main_ours(args):
                       "step_ms_graph": round(ms_dense_graph / args.steps, 4)}
 
 
-    e2e_ms, h2d, d2h = e2e_region(pipe, args.steps)
+    e2e_ms, h2d, d2h = e2e_region(pipe, args.steps, graph)
+    e2e_eager_ms, _, _ = e2e_region(pipe, args.steps)
     rows_per_step = R * w.num_depths
-    e2e_ms = max_over_ranks([e2e_ms], dist, "cuda")[0]
+    e2e_ms, e2e_eager_ms = max_over_ranks([e2e_ms, e2e_eager_ms], dist, "cuda")
     value = whole_job_rate(world, rows_per_step, args.steps, ms)
     e2e_value = whole_job_rate(world, rows_per_step, args.steps, e2e_ms)
 
@@ -719,7 +725,11 @@ def main_ours(args):
                                 if pipe.folded else "partial_kernel (split-KV partial pass, all four depths)"),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "note": "per step: one packed host->device copy of the inputs, the step's C-ABI "
+                        "calls replayed from their CUDA graph, one packed device->host copy",
+                "eager_calls_value": round(whole_job_rate(world, rows_per_step, args.steps,
+                                                          e2e_eager_ms), 1)},
         "eager": {"ms_per_step": round(ms_eager / args.steps, 4),
                   "rows_per_s": round(whole_job_rate(world, rows_per_step, args.steps, ms_eager), 1),
                   "note": "every launch bracketed by CUDA events"},
