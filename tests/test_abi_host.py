@@ -116,3 +116,37 @@ def test_zero_rows_is_a_no_op(lib):
     assert lib.wise_decode_partial(ctypes.byref(s), None, None, None, None, None, None,
                                    P(4096), n, None) == 0
     assert lib.wise_decode_finish(ctypes.byref(s), None, None, P(4096), n, None, None, None, None) == 0
+
+
+def test_flag_checks(lib):
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    P = ctypes.c_void_p
+    # unknown partial flags, and a partial-only flag given to the finish
+    st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
+                                    P(4096), n, ctypes.c_uint32(8), None)
+    assert st == 1 and b"flags" in lib.wise_last_error()
+    st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                   ctypes.c_uint32(W.FLAG_EARLY_START), P(16), P(16), P(16), None)
+    assert st == 1
+    lay = W.wise_workspace_layout(s)
+    # the second slot set: three more aligned regions after the first set
+    second = [lay[k] for k in ("partial_ml_1", "partial_acc_1", "tile_stats_1")]
+    assert all(o % 256 == 0 for o in second) and min(second) > lay["tile_stats"]
+    assert lay["total_bytes"] > max(second)
+
+
+def test_default_split_size(lib):
+    # short rows: 8 blocks a range
+    s = _shape(num_rows=64, num_q_heads=16, num_kv_heads=16, max_blocks=32, max_pages_per_row=64)
+    assert W.wise_workspace_layout(s)["max_items"] == 64 * 16 * 4
+    # rows past 64 blocks with >= 4096 ranges of 16 blocks: 16 blocks a range
+    s = _shape(num_rows=64, num_q_heads=16, num_kv_heads=16, max_blocks=128, max_pages_per_row=256)
+    assert W.wise_workspace_layout(s)["max_items"] == 64 * 16 * 8
+    # a small batch of long rows keeps 8 (enough items for every consumer)
+    s = _shape(num_rows=2, num_q_heads=32, num_kv_heads=8, max_blocks=1024, max_pages_per_row=2048)
+    assert W.wise_workspace_layout(s)["max_items"] == 2 * 8 * 128
+    # an explicit split size wins
+    s = _shape(num_rows=2, num_q_heads=32, num_kv_heads=8, max_blocks=1024, max_pages_per_row=2048,
+               tiles_per_item=16)
+    assert W.wise_workspace_layout(s)["max_items"] == 2 * 8 * 64
