@@ -1,0 +1,53 @@
+"""The benchmark's one-line JSON contract: the CPU reference arm (the oracle
+on a bounded sample) and, on a GPU, a short run of the GPU arm."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, timeout=600):
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                         capture_output=True, text=True, timeout=timeout, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+BASE_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config")
+
+
+def test_reference_arm_line():
+    out = _run("--impl", "reference", "--steps", "1", "--warmup", "1")
+    for k in BASE_KEYS + ("impl", "cpu_baseline", "e2e"):
+        assert k in out, k
+    assert out["impl"] == "reference" and out["value"] > 0 and out["higher_is_better"]
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] >= 1
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
+    assert "workload" in out["config"]
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line():
+    out = _run("--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    for k in BASE_KEYS + ("roofline", "e2e", "gpu_launches", "clocks", "modes"):
+        assert k in out, k
+    assert out["n_gpus"] == 1 and out["steps"] == 3 and out["warmup"] == 3
+    assert out["value"] > 0 and out["ms_per_step"] > 0 and out["scaling"] == "weak"
+    roof = out["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in roof, k
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert 0 < roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
+    e2e = out["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert e2e["value"] < out["value"] * 1.05  # the copies cost something
+    assert out["gpu_launches"] > 0
+    assert set(out["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert out["config"]["workload"].startswith("ouro1.4b_1k")
