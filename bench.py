@@ -471,6 +471,23 @@ class Pipeline:
             total += int((bits * valid[None, :]).sum()) * per_head_token
         return total
 
+    def support_density(self, modes) -> float:
+        """Block density of the mask the sparse rows attend: set bits over
+        the causal blocks, summed over the sparse rows' (row, KV head) pairs
+        (the reused-union density of [WISE PR, "Response to review", item 4])."""
+        np, w, W = self.np, self.w, self.W
+        sup = self.support.cpu().numpy().view(np.uint32)
+        kept = causal = 0
+        for r in range(w.num_rows):
+            if int(modes[r]) != W.MODE_SPARSE:
+                continue
+            nb = -(-int(w.seq_lens[r]) // 32)
+            bits = np.unpackbits(sup[r].view(np.uint8).reshape(w.num_kv_heads, -1), axis=1,
+                                 bitorder="little")[:, :nb]
+            kept += int(bits.sum())
+            causal += nb * w.num_kv_heads
+        return kept / causal if causal else 0.0
+
     def small_bytes(self) -> int:
         w = self.w
         es = 2 if w.dtype == "bf16" else 4
@@ -617,6 +634,7 @@ def main_ours(args):
     sparse_depths = [t for t, mode, _ in pipe.wise_step if mode == "sparse"]
     density = (pipe.kv_bytes(w.depth_modes[sparse_depths[0]]) /
                pipe.kv_bytes(np.zeros(w.num_rows, np.int8))) if sparse_depths else None
+    block_density = pipe.support_density(w.depth_modes[sparse_depths[0]]) if sparse_depths else None
 
     # The step and the dense baseline step, each captured once as a CUDA graph.
     graph = pipe.graph(pipe.wise_step)
@@ -713,7 +731,8 @@ def main_ours(args):
                    "timing": "value: CUDA-graph replay of the step, CUDA events around the K "
                              "replays; modes and roofline: eager launches with CUDA events "
                              "around every launch on the launching stream",
-                   "union_density": round(density, 4) if density else None},
+                   "union_density": round(density, 4) if density else None,
+                   "support_density_blocks": round(block_density, 4) if block_density else None},
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),

@@ -51,3 +51,4 @@ def test_gpu_arm_line():
     assert out["gpu_launches"] > 0
     assert set(out["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert out["config"]["workload"].startswith("ouro1.4b_1k")
+    assert 0 < out["config"]["support_density_blocks"] <= 1
