@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--rows", type=int, default=None,
                    help="fewer rows of the same workload (small profiling case)")
+    p.add_argument("--eta", type=float, default=None,
+                   help="selection threshold (default: the workload's, 0.95)")
     p.add_argument("--tiles-per-item", type=int, default=0,
                    help="split work-item size (0: the library default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -81,7 +83,7 @@ def oracle_sample_main(spec_json: str) -> None:
     from oracle import wise_oracle as O
 
     spec = json.loads(spec_json)
-    w = make_workload(spec["workload"], num_rows=spec["rows"])
+    w = make_workload(spec["workload"], num_rows=spec["rows"], **eta_kw(spec.get("eta")))
     inputs = []
     for t in range(w.num_depths):
         d = w.depth_inputs(t)
@@ -103,6 +105,10 @@ def oracle_sample_main(spec_json: str) -> None:
     print(json.dumps({"seconds": el, "row_calls": reps * w.num_rows * w.num_depths}))
 
 
+def eta_kw(eta) -> dict:
+    return {} if eta is None else {"eta": eta}
+
+
 def torch_int16():
     import torch
     return torch.int16
@@ -113,10 +119,10 @@ def bf16():
     return torch.bfloat16
 
 
-def run_oracle_sample(workload: str, rows: int, reps: int) -> dict:
+def run_oracle_sample(workload: str, rows: int, reps: int, eta=None) -> dict:
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    spec = json.dumps({"workload": workload, "rows": rows, "reps": reps})
+    spec = json.dumps({"workload": workload, "rows": rows, "reps": reps, "eta": eta})
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", spec],
                          capture_output=True, text=True, env=env, check=True)
     out = json.loads(res.stdout.strip().splitlines()[-1])
@@ -615,7 +621,7 @@ def main_ours(args):
     from block_sparse_paged_split_gb300.workload import make_workload
     build_library()
     # Weak scaling: every rank decodes its own batch (rows are independent).
-    w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank))
+    w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank), **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
                     lse_discover=args.lse_discover, overlap=args.overlap)
 
@@ -758,7 +764,7 @@ def main_ours(args):
         "wall_s_timed": round(wall, 2),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, reps=36)
+        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, reps=36, eta=args.eta)
     if rank == 0:
         print(json.dumps(result))
     if dist:
@@ -773,9 +779,9 @@ def main_reference(args):
     # Each step: the oracle on a 2-row sample of the workload through the 4
     # depths (about a second of CPU); warm-up steps are not timed.
     rows = 2
-    run_oracle_sample(args.workload, rows=rows, reps=max(1, min(Wm, 1)))
+    run_oracle_sample(args.workload, rows=rows, reps=max(1, min(Wm, 1)), eta=args.eta)
     t0 = time.perf_counter()
-    res = run_oracle_sample(args.workload, rows=rows, reps=K)
+    res = run_oracle_sample(args.workload, rows=rows, reps=K, eta=args.eta)
     value = res["value"]
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
            "n_gpus": 1, "steps": K, "warmup": Wm,

@@ -59,6 +59,32 @@ def test_modes_match_oracle(Hq, Hkv, D, dtype):
     assert np.array_equal(g["support"], s1)  # sparse leaves the mask alone
 
 
+@pytest.mark.parametrize("eta", [0.5, 0.8, 0.9, 0.99, 1.0])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4)])
+def test_eta_range(Hq, Hkv, eta):
+    """The selection across the threshold range of the GQA long-context
+    workload (0.8-0.99) and its ends: eta = 1 keeps every causal block."""
+    w = _wl(Hq, Hkv, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, Hkv, words(w)), np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, zero, eta=eta), oracle_call(b, 0, m, zero, eta=eta)
+    assert not compare_outputs(w, g, o)
+    cm = compare_masks(w, g["support"], o, m)
+    assert not cm["fails"] and cm["checked"] >= cm["excluded"], cm
+    if eta >= 1.0:
+        full = np.zeros_like(zero)
+        for r in range(R):
+            nb = -(-int(w.seq_lens[r]) // 32)
+            for blk in range(nb):
+                full[r, :, blk >> 5] |= np.uint32(1 << (blk & 31))
+        assert np.array_equal(g["support"], full)
+    m = np.full(R, W.MODE_SPARSE, np.int8)
+    g, o = gpu_call(b, 1, m, o["support"], eta=eta), oracle_call(b, 1, m, o["support"], eta=eta)
+    assert not compare_outputs(w, g, o)
+
+
 def test_tile_stats_match_oracle():
     """Discover rows' per-tile max and exp-sum (the workspace intermediates)."""
     w = _wl(4, 4, 128, "bf16")
