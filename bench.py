@@ -66,6 +66,10 @@ def parse():
                         "compaction while the previous finish runs (measured: no gain at 1K)")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
+    p.add_argument("--sparse-scaling", action="store_true",
+                   help="time one sparse call (64 rows, 16 heads MHA, D=128) at contexts "
+                        "1K-32K with 8 selected tiles per (row, head), and at 8K with 1-256 "
+                        "selected tiles; prints one JSON line with the table")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     p.add_argument("--record-traffic", default=None, metavar="RAW_CSV",
                    help="store the DRAM bytes of the partial-kernel launches in an ncu "
@@ -76,11 +80,13 @@ def parse():
 
 # ----------------------------------------------------------------------------- oracle leg
 def oracle_sample_main(spec_json: str) -> None:
-    """Runs in a child process with BLAS pinned to one thread: times the CPU
-    oracle on `rows` rows of the workload through the 4-depth schedule."""
+    """Runs in a child process (no CUDA context): times the C++ fp32 oracle on
+    `rows` rows of the workload through the 4-depth schedule, on every host
+    thread and on one, each for at least its target seconds (or a fixed number
+    of passes when `reps` is given)."""
     import numpy as np
     from block_sparse_paged_split_gb300.workload import make_workload
-    from oracle import wise_oracle as O
+    from oracle.cpp_oracle import CppOracle
 
     spec = json.loads(spec_json)
     w = make_workload(spec["workload"], num_rows=spec["rows"], **eta_kw(spec.get("eta")))
@@ -92,17 +98,31 @@ def oracle_sample_main(spec_json: str) -> None:
             conv[k] = v.view(torch_int16()).numpy().view(np.uint16) if v.dtype == bf16() else v.numpy()
         inputs.append(conv)
     sup = np.zeros((w.num_rows, w.num_kv_heads, -(-w.max_blocks // 32)), np.uint32)
-    reps = spec["reps"]
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def one_pass(O):
         s = sup
         for t in range(w.num_depths):
             d = inputs[t]
-            res = O.decode_layer(d["q"], d["k_cache"], d["v_cache"], w.page_table, w.seq_lens,
-                                 w.depth_modes[t], s, eta=w.eta, tile_tokens=w.tile_tokens)
-            s = res["support"]
-    el = time.perf_counter() - t0
-    print(json.dumps({"seconds": el, "row_calls": reps * w.num_rows * w.num_depths}))
+            s = O.decode_layer(d["q"], d["k_cache"], d["v_cache"], w.page_table, w.seq_lens,
+                               w.depth_modes[t], s, eta=w.eta, tile_tokens=w.tile_tokens,
+                               diagnostics=False)["support"]
+
+    report = {"row_calls_per_pass": w.num_rows * w.num_depths}
+    for key, threads, target in (("all", 0, spec["seconds"]), ("one", 1, spec["seconds_1t"])):
+        if target <= 0:
+            continue
+        O = CppOracle("f32", threads=threads)
+        for _ in range(max(1, spec.get("warmup", 1))):  # untimed: page-in, thread start
+            one_pass(O)
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            one_pass(O)
+            passes += 1
+            el = time.perf_counter() - t0
+            if (spec.get("reps") and passes >= spec["reps"]) or (not spec.get("reps") and el >= target):
+                break
+        report[key] = {"seconds": el, "passes": passes, "threads": O.last_threads}
+    print(json.dumps(report))
 
 
 def eta_kw(eta) -> dict:
@@ -119,17 +139,29 @@ def bf16():
     return torch.bfloat16
 
 
-def run_oracle_sample(workload: str, rows: int, reps: int, eta=None) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    spec = json.dumps({"workload": workload, "rows": rows, "reps": reps, "eta": eta})
+def run_oracle_sample(workload: str, rows: int, seconds: float = 10.0, seconds_1t: float = 3.0,
+                      reps: int = 0, warmup: int = 1, eta=None) -> dict:
+    """The CPU baseline: the C++ fp32 oracle (the definition the kernels are
+    checked against, untuned) on `rows` rows of the workload, in a child
+    process with no GPU visible."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    spec = json.dumps({"workload": workload, "rows": rows, "seconds": seconds,
+                       "seconds_1t": seconds_1t, "reps": reps, "warmup": warmup, "eta": eta})
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", spec],
                          capture_output=True, text=True, env=env, check=True)
     out = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": out["row_calls"] / out["seconds"], "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"{rows} rows of {workload} (same recipe), {reps}x the 4-depth schedule, "
-                      f"numpy float64, BLAS pinned to 1 thread; {out['seconds']:.1f} s"}
+    per = out["row_calls_per_pass"]
+    a = out["all"]
+    value = per * a["passes"] / a["seconds"]
+    sample = (f"{rows} rows of {workload} (same recipe), {a['passes']}x the 4-depth schedule "
+              f"through the C++ fp32 oracle on {a['threads']} host threads ({a['seconds']:.1f} s)")
+    result = {"value": value, "unit": UNIT, "cores": a["threads"], "kind": "oracle"}
+    if "one" in out:
+        o = out["one"]
+        result["value_1_thread"] = round(per * o["passes"] / o["seconds"], 3)
+        sample += f"; 1 thread: {o['passes']}x ({o['seconds']:.1f} s)"
+    result["sample"] = sample
+    return result
 
 
 # ----------------------------------------------------------------------------- traffic
@@ -764,11 +796,106 @@ def main_ours(args):
         "wall_s_timed": round(wall, 2),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, reps=36, eta=args.eta)
+        result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, eta=args.eta)
     if rank == 0:
         print(json.dumps(result))
     if dist:
         dist.destroy_process_group()
+
+
+def sparse_scaling_main(args):
+    """Sparse-mode time against the selected tiles and against the context.
+
+    Each point is one sparse call over 64 rows x 16 heads (MHA, D=128, bf16):
+    compaction, partial pass and finish, timed with CUDA events on the
+    launching stream (median of 30 calls, the L2 flushed by a 512 MiB write
+    before each).  Sweep 1 holds 8 selected tiles per (row, head) and grows the
+    context 1K -> 32K; sweep 2 holds the context at 8K and grows the selected
+    tiles 1 -> 256 (every block).  The dense call at each context is timed the
+    same way for contrast."""
+    import numpy as np
+    import torch
+    import block_sparse_paged_split_gb300 as W
+    from block_sparse_paged_split_gb300 import wise
+    from block_sparse_paged_split_gb300.build import build_library
+    from block_sparse_paged_split_gb300.workload import sparse_scaling_inputs
+
+    build_library()
+    lib = wise.library()
+    torch.cuda.set_device(0)
+    R, H, D, reps = 64, 16, 128, 30
+    peak, peak_kind = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768)] +
+              [(8192, k, False) for k in (1, 2, 4, 16, 32, 64, 128, 256)])
+    rows = []
+    for L, k, with_dense in points:
+        d = sparse_scaling_inputs(R, H, D, L, k, seed=4242 + L + k)
+        shape = W.make_shape(num_rows=R, num_q_heads=H, num_kv_heads=H, head_dim=D, page_size=16,
+                             max_pages_per_row=d["page_table"].shape[1], num_pages=d["num_pages"],
+                             max_blocks=d["max_blocks"], dtype=W.DTYPE_BF16, eta=0.95)
+        ws = W.alloc_workspace(shape)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, H), dtype=torch.float32, device="cuda")
+        S = ctypes.byref(shape)
+        st = stream.cuda_stream
+        args_common = (d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                       d["page_table"].data_ptr(), d["seq_lens"].data_ptr())
+
+        def call(modes_t, sup):
+            m = modes_t.data_ptr()
+            t = []
+            for fn, a in ((lib.wise_compact_tiles, (S, m, args_common[4], sup.data_ptr(),
+                                                    ws.data_ptr(), ws.numel(), st)),
+                          (lib.wise_decode_partial, (S,) + args_common + (m, ws.data_ptr(),
+                                                                          ws.numel(), st)),
+                          (lib.wise_decode_finish, (S, m, args_common[4], ws.data_ptr(), ws.numel(),
+                                                    sup.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                                    st))):
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                t.append(e)
+                rc = fn(*a)
+                if rc != 0:
+                    raise RuntimeError(lib.wise_last_error().decode())
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            t.append(e)
+            return t
+
+        def timed(modes_t, sup):
+            calls, parts = [], []
+            for i in range(reps + 3):
+                flush.fill_(i & 0xFF)
+                t = call(modes_t, sup)
+                torch.cuda.synchronize()
+                if i >= 3:
+                    calls.append(t[0].elapsed_time(t[3]) * 1e3)
+                    parts.append(t[1].elapsed_time(t[2]) * 1e3)
+            return statistics.median(calls), statistics.median(parts)
+
+        sparse = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
+        call_us, part_us = timed(sparse, d["support"])
+        tiles = R * H * min(k, d["max_blocks"])
+        sel_bytes = tiles * 32 * D * 2 * 2
+        row = {"context": L, "selected_tiles_per_head": min(k, d["max_blocks"]),
+               "sparse_call_us": round(call_us, 2), "sparse_partial_us": round(part_us, 2),
+               "selected_kv_bytes": sel_bytes,
+               "partial_gbs": round(sel_bytes / (part_us * 1e-6) / 1e9, 1),
+               "partial_frac": round(sel_bytes / (part_us * 1e-6) / 1e9 / peak, 3)}
+        if with_dense:
+            dense = torch.zeros((R,), dtype=torch.int8, device="cuda")
+            dense_call, dense_part = timed(dense, torch.zeros_like(d["support"]))
+            dense_bytes = R * H * L * D * 2 * 2
+            row.update({"dense_call_us": round(dense_call, 2),
+                        "dense_partial_frac": round(dense_bytes / (dense_part * 1e-6) / 1e9 / peak, 3)})
+        rows.append(row)
+        del d, ws, out, lse
+        torch.cuda.empty_cache()
+    print(json.dumps({"sparse_scaling": rows, "rows": R, "heads": H, "head_dim": D,
+                      "peak_gbs": peak, "peak_kind": peak_kind, "reps": reps,
+                      "l2": "flushed by a 512 MiB write before every call"}))
 
 
 def main_reference(args):
@@ -776,20 +903,21 @@ def main_reference(args):
     if rank != 0:
         return
     K, Wm = args.steps, args.warmup
-    # Each step: the oracle on a 2-row sample of the workload through the 4
-    # depths (about a second of CPU); warm-up steps are not timed.
-    rows = 2
-    run_oracle_sample(args.workload, rows=rows, reps=max(1, min(Wm, 1)), eta=args.eta)
+    # Each step: the C++ fp32 oracle on a 16-row sample of the workload through
+    # the 4 depths on every host thread (tens of milliseconds); the warm-up
+    # passes run untimed inside the child before the K timed ones.
+    rows = 16
     t0 = time.perf_counter()
-    res = run_oracle_sample(args.workload, rows=rows, reps=K, eta=args.eta)
+    res = run_oracle_sample(args.workload, rows=rows, seconds_1t=0.0, reps=K, warmup=Wm,
+                            eta=args.eta)
     value = res["value"]
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
            "n_gpus": 1, "steps": K, "warmup": Wm,
            "ms_per_step": round(1e3 * rows * 4 / value, 3), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"{args.workload} (oracle sample of {rows} rows per step)"},
-           "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                            "sample": res["sample"]},
+           "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": res["cores"],
+                            "kind": "oracle", "sample": res["sample"]},
            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0},
            "wall_s": round(time.perf_counter() - t0, 1)}
@@ -802,6 +930,8 @@ if __name__ == "__main__":
         oracle_sample_main(a.oracle_sample)
     elif a.record_traffic is not None:
         record_traffic(a.record_traffic, a.rows or 64, a.workload)
+    elif a.sparse_scaling:
+        sparse_scaling_main(a)
     elif a.impl == "reference":
         main_reference(a)
     else:

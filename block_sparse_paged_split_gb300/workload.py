@@ -245,3 +245,36 @@ def make_workload(name: str, *, num_rows: Optional[int] = None, context: Optiona
 
 
 WORKLOADS = tuple(BASE_SEEDS)
+
+
+def sparse_scaling_inputs(R: int, H: int, D: int, L: int, k: int, seed: int,
+                          device="cuda", page_size: int = 16, tile_tokens: int = 32):
+    """Inputs of the sparse-scaling measurement, drawn on the device (timing
+    only; no parity check reads them): R rows of L tokens, H heads MHA, bf16
+    q/K/V ~ N(0,1) from a seeded device generator, each row's pages at a
+    seeded permutation of a pool exactly the batch's size, and per (row, head)
+    k distinct blocks drawn uniformly without replacement from the row's
+    L / tile_tokens blocks (a seeded host draw).  Returns q, k_cache, v_cache,
+    page_table, seq_lens and the mask [R, H, W] (int32 words)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    npg = -(-L // page_size)
+    num_pages = R * npg
+    q = torch.randn((R, H, D), generator=gen, device=device).to(torch.bfloat16)
+    k_cache = torch.randn((num_pages, page_size, H, D), generator=gen, device=device,
+                          dtype=torch.bfloat16)
+    v_cache = torch.randn((num_pages, page_size, H, D), generator=gen, device=device,
+                          dtype=torch.bfloat16)
+    perm = torch.randperm(num_pages, generator=gen, device=device).to(torch.int32)
+    page_table = perm.view(R, npg).contiguous()
+    seq_lens = torch.full((R,), L, dtype=torch.int32, device=device)
+    nb = -(-L // tile_tokens)
+    W = -(-nb // 32)
+    rng = _rng(seed, 0, _TENSOR_IDS["plant"])
+    chosen = np.argsort(rng.random((R, H, nb)), axis=-1)[..., :min(k, nb)]
+    bits = np.zeros((R, H, 32 * W), dtype=bool)
+    np.put_along_axis(bits, chosen, True, axis=-1)
+    words = np.packbits(bits, axis=-1, bitorder="little").view(np.int32).reshape(R, H, W)
+    support = torch.from_numpy(words.copy()).to(device)
+    return {"q": q, "k_cache": k_cache, "v_cache": v_cache, "page_table": page_table,
+            "seq_lens": seq_lens, "support": support, "num_pages": num_pages, "max_blocks": nb}

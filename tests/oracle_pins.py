@@ -70,6 +70,25 @@ def random_support(w, seed, density=0.4) -> np.ndarray:
         w.num_rows, w.num_kv_heads, W).copy()
 
 
+# Float64 tolerances.  An oracle that computes in float32 carries its own
+# `TOLERANCES` (the same keys), derived from its measured distance to float64.
+TOLERANCES = {"out_rtol": 1e-10, "out_atol": 1e-12, "lse": 1e-10, "mass": 1e-12,
+              "tile_max": 1e-12, "mass_sum": 1e-12, "tile_lse": 1e-10, "cutoff_band": 1e-9}
+
+
+# For the fp32 oracle: measured against the float64 oracle on MHA and GQA
+# batches up to 4096 tokens, its worst errors are 1.4e-6 (output), 2.4e-6 (LSE),
+# 9e-7 (block mass), 2.2e-6 (tile max), 1.9e-6 (sum of masses - 1); each bound
+# below leaves about ten times that.  A cumulative fp32 sum of masses carries
+# up to ~1e-6, so selections whose cutoff lies that close to eta are skipped.
+F32_TOLERANCES = {"out_rtol": 1e-5, "out_atol": 2e-5, "lse": 2e-5, "mass": 1e-5,
+                  "tile_max": 2e-5, "mass_sum": 2e-5, "tile_lse": 2e-5, "cutoff_band": 2e-6}
+
+
+def tol(O, key: str) -> float:
+    return getattr(O, "TOLERANCES", TOLERANCES)[key]
+
+
 def library_bits(words: np.ndarray, nb: int) -> np.ndarray:
     """Mask bits decoded by numpy's unpackbits (little-endian words)."""
     return np.unpackbits(np.ascontiguousarray(words, dtype="<u4").view(np.uint8),
@@ -109,9 +128,10 @@ def pin_dense_sdpa(O) -> List[str]:
                 q, K, V = _ref_row(d, r, h // G, h)
                 o = _sdpa(q, K, V, scale).numpy()
                 lse = torch.logsumexp(scale * torch.mv(K, q), 0).item()
-                if not np.allclose(res["out"][r, h], o, rtol=1e-10, atol=1e-12):
+                if not np.allclose(res["out"][r, h], o, rtol=tol(O, "out_rtol"),
+                                   atol=tol(O, "out_atol")):
                     fails.append(f"dense out differs r={r} h={h}")
-                if abs(res["lse"][r, h] - lse) > 1e-10:
+                if abs(res["lse"][r, h] - lse) > tol(O, "lse"):
                     fails.append(f"dense lse differs r={r} h={h}")
     return fails
 
@@ -142,9 +162,10 @@ def pin_sparse_masked_sdpa(O) -> List[str]:
                 o = _sdpa(q, K, V, scale, mask).numpy()
                 s = scale * torch.mv(K, q)
                 lse = torch.logsumexp(s[torch.from_numpy(mask)], 0).item()
-                if not np.allclose(res["out"][r, h], o, rtol=1e-10, atol=1e-12):
+                if not np.allclose(res["out"][r, h], o, rtol=tol(O, "out_rtol"),
+                                   atol=tol(O, "out_atol")):
                     fails.append(f"sparse out differs r={r} h={h}")
-                if abs(res["lse"][r, h] - lse) > 1e-10:
+                if abs(res["lse"][r, h] - lse) > tol(O, "lse"):
                     fails.append(f"sparse lse differs r={r} h={h}")
     return fails
 
@@ -203,17 +224,17 @@ def pin_block_masses(O) -> List[str]:
         nb = -(-L // B)
         for b in range(nb):
             blk = slice(b * B, min((b + 1) * B, L))
-            if abs(dg["p"][b] - prob[blk].sum().item()) > 1e-12:
+            if abs(dg["p"][b] - prob[blk].sum().item()) > tol(O, "mass"):
                 fails.append(f"p_b != softmax block sum r={r} h={h} b={b}")
-            if abs(dg["m_b"][b] - torch.amax(s[blk]).item()) > 1e-12:
+            if abs(dg["m_b"][b] - torch.amax(s[blk]).item()) > tol(O, "tile_max"):
                 fails.append(f"m_b != amax r={r} h={h} b={b}")
             lse_mass = dg["l_b"][b] * math.exp(dg["m_b"][b] - res["lse"][r, h])
-            if abs(lse_mass - dg["p"][b]) > 1e-12:
+            if abs(lse_mass - dg["p"][b]) > tol(O, "mass"):
                 fails.append(f"LSE-derived mass differs r={r} h={h} b={b}")
-        if abs(dg["p"].sum() - 1.0) > 1e-12:
+        if abs(dg["p"].sum() - 1.0) > tol(O, "mass_sum"):
             fails.append(f"masses do not sum to 1 r={r} h={h}")
         blk_lse = torch.logsumexp(torch.tensor(dg["m_b"] + np.log(dg["l_b"])), 0).item()
-        if abs(blk_lse - res["lse"][r, h]) > 1e-10:
+        if abs(blk_lse - res["lse"][r, h]) > tol(O, "tile_lse"):
             fails.append(f"logsumexp of tile stats != lse r={r} h={h}")
     return fails
 
@@ -237,7 +258,7 @@ def pin_selection_bruteforce(O) -> List[str]:
         p = rng.dirichlet(np.full(n, rng.uniform(0.2, 3.0))).astype(np.float32).astype(np.float64)
         eta = float(rng.uniform(0.05, 0.999))
         C = np.cumsum(np.sort(p)[::-1])
-        if np.any(np.abs(C - eta) < 1e-9):
+        if np.any(np.abs(C - eta) < tol(O, "cutoff_band")):
             continue
         k, best = _brute_force_k(p, eta)
         got = O.select_blocks(p, eta)
