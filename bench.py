@@ -70,6 +70,8 @@ def parse():
                    help="time one sparse call (64 rows, 16 heads MHA, D=128) at contexts "
                         "1K-32K with 8 selected tiles per (row, head), and at 8K with 1-256 "
                         "selected tiles; prints one JSON line with the table")
+    p.add_argument("--point", default=None, metavar="CONTEXT:TILES",
+                   help="with --sparse-scaling: time only this point (e.g. 8192:1)")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     p.add_argument("--record-traffic", default=None, metavar="RAW_CSV",
                    help="store the DRAM bytes of the partial-kernel launches in an ncu "
@@ -806,9 +808,9 @@ def main_ours(args):
 def sparse_scaling_main(args):
     """Sparse-mode time against the selected tiles and against the context.
 
-    Each point is one sparse call over 64 rows x 16 heads (MHA, D=128, bf16):
+    Each point is one sparse call over 64 rows (--rows) x 16 heads (MHA, D=128, bf16):
     compaction, partial pass and finish, timed with CUDA events on the
-    launching stream (median of 30 calls, the L2 flushed by a 512 MiB write
+    launching stream (mean of 30 calls, the L2 flushed by a 512 MiB write
     before each).  Sweep 1 holds 8 selected tiles per (row, head) and grows the
     context 1K -> 32K; sweep 2 holds the context at 8K and grows the selected
     tiles 1 -> 256 (every block).  The dense call at each context is timed the
@@ -823,12 +825,15 @@ def sparse_scaling_main(args):
     build_library()
     lib = wise.library()
     torch.cuda.set_device(0)
-    R, H, D, reps = 64, 16, 128, 30
+    R, H, D, reps = args.rows or 64, 16, 128, 30
     peak, peak_kind = peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768)] +
               [(8192, k, False) for k in (1, 2, 4, 16, 32, 64, 128, 256)])
+    if args.point:
+        L, k = (int(x) for x in args.point.split(":"))
+        points = [(L, k, False)]
     rows = []
     for L, k, with_dense in points:
         d = sparse_scaling_inputs(R, H, D, L, k, seed=4242 + L + k)
@@ -865,28 +870,34 @@ def sparse_scaling_main(args):
             return t
 
         def timed(modes_t, sup):
-            calls, parts = [], []
+            calls, comp, parts, fin = [], [], [], []
             for i in range(reps + 3):
                 flush.fill_(i & 0xFF)
                 t = call(modes_t, sup)
                 torch.cuda.synchronize()
                 if i >= 3:
                     calls.append(t[0].elapsed_time(t[3]) * 1e3)
+                    comp.append(t[0].elapsed_time(t[1]) * 1e3)
                     parts.append(t[1].elapsed_time(t[2]) * 1e3)
-            return statistics.median(calls), statistics.median(parts)
+                    fin.append(t[2].elapsed_time(t[3]) * 1e3)
+            # Means: event timestamps step in about 2 us on GB300, and the mean of
+            # many calls averages that quantisation out where a median keeps it.
+            return (statistics.fmean(calls), statistics.fmean(parts), statistics.fmean(comp),
+                    statistics.fmean(fin))
 
         sparse = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
-        call_us, part_us = timed(sparse, d["support"])
+        call_us, part_us, comp_us, fin_us = timed(sparse, d["support"])
         tiles = R * H * min(k, d["max_blocks"])
         sel_bytes = tiles * 32 * D * 2 * 2
         row = {"context": L, "selected_tiles_per_head": min(k, d["max_blocks"]),
                "sparse_call_us": round(call_us, 2), "sparse_partial_us": round(part_us, 2),
+               "sparse_compact_us": round(comp_us, 2), "sparse_finish_us": round(fin_us, 2),
                "selected_kv_bytes": sel_bytes,
                "partial_gbs": round(sel_bytes / (part_us * 1e-6) / 1e9, 1),
                "partial_frac": round(sel_bytes / (part_us * 1e-6) / 1e9 / peak, 3)}
         if with_dense:
             dense = torch.zeros((R,), dtype=torch.int8, device="cuda")
-            dense_call, dense_part = timed(dense, torch.zeros_like(d["support"]))
+            dense_call, dense_part, _, _ = timed(dense, torch.zeros_like(d["support"]))
             dense_bytes = R * H * L * D * 2 * 2
             row.update({"dense_call_us": round(dense_call, 2),
                         "dense_partial_frac": round(dense_bytes / (dense_part * 1e-6) / 1e9 / peak, 3)})

@@ -124,10 +124,11 @@ def test_tiny_schedule_f32():
 
 def test_compaction_matches_oracle():
     """Work items (tiles as bitmaps over their block range) and per-head
-    counts, against the oracle's lists and items: bit-exact."""
+    counts, against the oracle's lists and items: bit-exact, over rows of up
+    to four mask words."""
     rng = np.random.default_rng(5)
     for T in (1, 2, 4, 8, 16):
-        lens = rng.integers(0, 700, size=9).astype(np.int32)
+        lens = rng.integers(0, 4000, size=9).astype(np.int32)
         w = _wl(4, 2, 64, "bf16", lens=lens, seed=9)
         R = w.num_rows
         bits = rng.random((R, 2, words(w) * 32)) < 0.3

@@ -35,3 +35,22 @@ def test_workload_is_deterministic_and_poisoned_outside_rows():
         if L % P:
             last = a.page_table[r, L // P]
             assert da["k_cache"][last, L % P:].float().isnan().all()
+
+
+def test_sparse_scaling_inputs():
+    """The sparse-scaling inputs: every (row, head) mask holds exactly k
+    distinct blocks below the row's block count, the page table is a
+    permutation of the pool, and a seed fixes the draw."""
+    from block_sparse_paged_split_gb300.workload import sparse_scaling_inputs
+    for L, k in ((1000, 5), (4096, 8), (2048, 64), (96, 9)):
+        d = sparse_scaling_inputs(3, 2, 64, L, k, seed=11, device="cpu")
+        nb = -(-L // 32)
+        words = d["support"].numpy().view(np.uint32)
+        bits = np.unpackbits(words.view(np.uint8), axis=-1, bitorder="little")
+        assert np.all(bits.sum(-1) == min(k, nb))
+        assert not bits[..., nb:].any()
+        pt = d["page_table"].numpy().ravel()
+        assert np.array_equal(np.sort(pt), np.arange(d["num_pages"]))
+        assert d["max_blocks"] == nb and d["k_cache"].shape[0] == d["num_pages"]
+        again = sparse_scaling_inputs(3, 2, 64, L, k, seed=11, device="cpu")
+        assert torch.equal(again["support"], d["support"]) and torch.equal(again["k_cache"], d["k_cache"])
