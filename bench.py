@@ -296,7 +296,7 @@ class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
-                 lse_discover: bool = False, overlap: bool = False):
+                 lse_discover: bool = False, overlap: bool = False, share=None):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -313,8 +313,15 @@ class Pipeline:
                                   dtype=W.DTYPE_BF16 if w.dtype == "bf16" else W.DTYPE_F32,
                                   eta=w.eta, tiles_per_item=tiles_per_item)
         dev = torch.device("cuda")
-        self.host = [w.depth_inputs(t) for t in range(w.num_depths)]
-        self.depth = [{k: v.to(dev) for k, v in d.items() if k != "q"} for d in self.host]
+        if share is None:
+            self.host = [w.depth_inputs(t) for t in range(w.num_depths)]
+            self.depth = [{k: v.to(dev) for k, v in d.items() if k != "q"} for d in self.host]
+        else:
+            # A second buffer set over the same resident K/V (the pipelined
+            # end-to-end region alternates two): its own step inputs, outputs,
+            # mask and workspace.
+            self.host = share.host
+            self.depth = [{k: v for k, v in d.items() if k != "q"} for d in share.depth]
         # The per-step inputs (every depth's q, the page table, the lengths,
         # every depth's modes) live in one device buffer and the per-step
         # outputs (every depth's out and lse, the mask) in another, so a step
@@ -601,6 +608,61 @@ def e2e_region(pipe, K, graph=None):
     return s.elapsed_time(e), h2d, d2h
 
 
+def e2e_pipelined(pipes, graphs, K):
+    """The end-to-end region as an engine runs it: two buffer sets over the
+    same resident K/V, so step i+1's host->device input copy and step i-1's
+    device->host result copy (each on its own copy stream) run while step i
+    computes.  Every step still moves its own inputs from pinned host memory
+    and its own results back; the region runs from before the first input
+    copy to after the last result copy."""
+    import torch
+    compute = pipes[0].stream
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    h_out = [torch.empty(p.out_dev.shape, dtype=p.out_dev.dtype).pin_memory() for p in pipes]
+    h2d = pipes[0].in_host.numel() * pipes[0].in_host.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    ev = lambda: torch.cuda.Event()
+
+    def run(n, timed):
+        computed = [None, None]   # compute of the set's last step done
+        read_back = [None, None]  # result copy of the set's last step done
+        start = torch.cuda.Event(enable_timing=True) if timed else None
+        end = torch.cuda.Event(enable_timing=True) if timed else None
+        if timed:
+            start.record(compute)
+        up.wait_stream(compute)
+        down.wait_stream(compute)
+        for i in range(n):
+            j = i % 2
+            p = pipes[j]
+            with torch.cuda.stream(up):
+                if computed[j] is not None:
+                    up.wait_event(computed[j])     # the set's inputs are consumed
+                p.in_dev.copy_(p.in_host, non_blocking=True)
+                landed = ev()
+                landed.record(up)
+            compute.wait_event(landed)
+            if read_back[j] is not None:
+                compute.wait_event(read_back[j])   # the set's results are read
+            graphs[j].replay()
+            computed[j] = ev()
+            computed[j].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[j])
+                h_out[j].copy_(p.out_dev, non_blocking=True)
+                read_back[j] = ev()
+                read_back[j].record(down)
+        compute.wait_stream(up)
+        compute.wait_stream(down)
+        if timed:
+            end.record(compute)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) if timed else None
+
+    run(4, False)
+    return run(K, True), h2d, d2h
+
+
 # ----------------------------------------------------------------------------- ranks
 def rank_env():
     """(world size, rank, local rank) from the torchrun environment."""
@@ -715,11 +777,11 @@ def main_ours(args):
     part_ms = sum(v for (tt, m, k), v in per.items() if k == "partial")
     achieved = part_bytes / (part_ms * 1e-3) / 1e9
     # Kernels launched in the timed regions: the graph replays and the eager
-    # passes, each over K WISE steps and K dense steps, and the two end-to-end
-    # regions' K WISE steps each.
+    # passes, each over K WISE steps and K dense steps, and the three
+    # end-to-end regions' K WISE steps each.
     launches = (2 * (pipe.launches_per_step(pipe.wise_step) +
                      pipe.launches_per_step(pipe.dense_step)) +
-                2 * pipe.launches_per_step(pipe.wise_step)) * args.steps
+                3 * pipe.launches_per_step(pipe.wise_step)) * args.steps
 
     R = w.num_rows
     modes = {}
@@ -745,10 +807,18 @@ def main_ours(args):
                       "step_ms_graph": round(ms_dense_graph / args.steps, 4)}
 
 
-    e2e_ms, h2d, d2h = e2e_region(pipe, args.steps, graph)
+    # End to end: the pipelined region (two buffer sets, copies overlapping
+    # the compute), then the same steps with each step's copies in line.
+    pipe_b = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold,
+                      head_union=args.head_union, lse_discover=args.lse_discover,
+                      overlap=args.overlap, share=pipe)
+    graph_b = pipe_b.graph(pipe_b.wise_step)
+    e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
+    e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)
     e2e_eager_ms, _, _ = e2e_region(pipe, args.steps)
     rows_per_step = R * w.num_depths
-    e2e_ms, e2e_eager_ms = max_over_ranks([e2e_ms, e2e_eager_ms], dist, "cuda")
+    e2e_ms, e2e_serial_ms, e2e_eager_ms = max_over_ranks([e2e_ms, e2e_serial_ms, e2e_eager_ms],
+                                                         dist, "cuda")
     value = whole_job_rate(world, rows_per_step, args.steps, ms)
     e2e_value = whole_job_rate(world, rows_per_step, args.steps, e2e_ms)
 
@@ -786,9 +856,15 @@ def main_ours(args):
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "per step: one packed host->device copy of the inputs, the step's C-ABI "
-                        "calls replayed from their CUDA graph, one packed device->host copy",
+                        "calls replayed from their CUDA graph, one packed device->host copy of "
+                        "the results; two buffer sets, so step i+1's input copy and step i-1's "
+                        "result copy (own copy streams) overlap step i's compute",
+                "serial_value": round(whole_job_rate(world, rows_per_step, args.steps,
+                                                     e2e_serial_ms), 1),
                 "eager_calls_value": round(whole_job_rate(world, rows_per_step, args.steps,
-                                                          e2e_eager_ms), 1)},
+                                                          e2e_eager_ms), 1),
+                "variants": "serial_value: each step's copies in line with it, one buffer set; "
+                            "eager_calls_value: the same with the C-ABI calls made one by one"},
         "eager": {"ms_per_step": round(ms_eager / args.steps, 4),
                   "rows_per_s": round(whole_job_rate(world, rows_per_step, args.steps, ms_eager), 1),
                   "note": "every launch bracketed by CUDA events"},
