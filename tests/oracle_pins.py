@@ -205,6 +205,31 @@ def pin_paging_invariance(O) -> List[str]:
     return fails
 
 
+def pin_page_size_invariance(O) -> List[str]:
+    """The same logical rows paged in 16-token and in 32-token pages (each a
+    seeded permutation of its own pool) give bitwise the same outputs, LSEs
+    and masks in every mode: the page size only changes where a token is
+    stored, never the arithmetic."""
+    fails = []
+    lens = np.array([70, 33, 96, 1, 0, 64], np.int32)
+    modes = np.array([MODE_DENSE, MODE_DISCOVER, MODE_SPARSE, MODE_DISCOVER_UNION, MODE_SPARSE,
+                      MODE_DISCOVER], np.int8)
+    res = []
+    for P in (16, 32):
+        w = custom_workload(R=len(lens), Hq=4, Hkv=2, D=64, dtype="f32", depths=1, n_planted=1,
+                            seq_lens=lens, pool_factor=2, seed=43, page_size=P,
+                            depth_modes=[modes])
+        d = w.depth_inputs(0)
+        sup = random_support(w, 7, density=0.5)
+        res.append(O.decode_layer(as_oracle_array(d["q"]), as_oracle_array(d["k_cache"]),
+                                  as_oracle_array(d["v_cache"]), w.page_table, w.seq_lens, modes,
+                                  sup, eta=0.9, tile_tokens=32))
+    for key in ("out", "lse", "support"):
+        if not np.array_equal(res[0][key], res[1][key]):
+            fails.append(f"page size 16 vs 32 changed {key}")
+    return fails
+
+
 def pin_block_masses(O) -> List[str]:
     """Per-tile stats and block masses against library softmax/logsumexp:
     m_b = amax over the tile; p_b = sum of the tile's softmax probabilities;
@@ -436,6 +461,6 @@ def pin_compaction(O) -> List[str]:
 
 
 ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_all_blocks_sparse_is_dense,
-            pin_paging_invariance, pin_block_masses, pin_selection_bruteforce,
+            pin_paging_invariance, pin_page_size_invariance, pin_block_masses, pin_selection_bruteforce,
             pin_selection_golden, pin_selection_limits, pin_union, pin_density_example,
             pin_compaction, pin_head_union]

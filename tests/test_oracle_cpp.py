@@ -129,6 +129,8 @@ MUTANTS = [
      "while (i < c && lst[i] <= (s + 1) * T) ++i;"),
     ("head_union_skips_last_head", "for (int g = 0; g < kv_heads; ++g)\n        any = any ||",
      "for (int g = 0; g + 1 < kv_heads; ++g)\n        any = any ||"),
+    ("page_size_fixed_at_16", "const int B = P.tile_tokens, PS = P.page_size;",
+     "const int B = P.tile_tokens, PS = 16;"),
     ("padding_row_gets_output", "if (L <= 0) return;  // padding row",
      "if (L <= 0) { out[0] = 1.0; return; }"),
 ]
