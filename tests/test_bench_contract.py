@@ -52,3 +52,21 @@ def test_gpu_arm_line():
     assert set(out["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert out["config"]["workload"].startswith("ouro1.4b_1k")
     assert 0 < out["config"]["support_density_blocks"] <= 1
+
+
+@pytest.mark.gpu
+def test_sparse_scaling_point():
+    """One point of the sparse-scaling measurement (8 rows, 4K context, 8
+    selected tiles per head): per-kernel times that add up to the call, and
+    selected bytes equal to rows x heads x tiles x 32 tokens x 512 B."""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--sparse-scaling",
+                          "--point", "4096:8", "--rows", "8"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    out = json.loads([l for l in res.stdout.splitlines() if l.startswith("{")][-1])
+    (pt,) = out["sparse_scaling"]
+    assert pt["context"] == 4096 and pt["selected_tiles_per_head"] == 8 and out["rows"] == 8
+    assert pt["selected_kv_bytes"] == 8 * 16 * 8 * 32 * 512
+    parts = pt["sparse_compact_us"] + pt["sparse_partial_us"] + pt["sparse_finish_us"]
+    assert 0 < parts <= pt["sparse_call_us"] * 1.01
+    assert 0 < pt["partial_frac"] < 1.5
