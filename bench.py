@@ -82,6 +82,8 @@ def parse():
                         "selected tiles; prints one JSON line with the table")
     p.add_argument("--point", default=None, metavar="CONTEXT:TILES",
                    help="with --sparse-scaling: time only this point (e.g. 8192:1)")
+    p.add_argument("--shared-blocks", action="store_true",
+                   help="with --sparse-scaling: every head of a row selects the same blocks")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     p.add_argument("--record-traffic", default=None, metavar="RAW_CSV",
                    help="store the DRAM bytes of the partial-kernel launches in an ncu "
@@ -618,6 +620,39 @@ def e2e_region(pipe, K, graph=None):
     return s.elapsed_time(e), h2d, d2h
 
 
+def partial_in_step_ms(pipe, base_ms, depth, K, dist):
+    """What one partial launch of `depth` costs inside the captured step: the
+    step is captured again with one more launch of that depth's partial just
+    before it, and the extra time per replay over the plain step is the
+    answer.  The extra launch reads a private copy of the depth's K/V pool
+    (same values, same items, its own addresses; nothing else reads it), so
+    neither it nor the real launch finds the other's tiles in L2, and the
+    real launch then rewrites the same splits.  Unlike the eager per-launch
+    events, this keeps the programmatic-dependent-launch overlap with the
+    neighbouring kernels that the step itself has."""
+    torch = pipe.torch
+    cold = [pipe.depth[depth]["k_cache"].clone(), pipe.depth[depth]["v_cache"].clone()]
+    step = []
+    for t, mode, calls in pipe.wise_step:
+        if t == depth:
+            doubled = []
+            for c in calls:
+                if c[0] == "partial":
+                    args = list(c[2])
+                    args[2], args[3] = cold[0].data_ptr(), cold[1].data_ptr()
+                    doubled.append(("partial", c[1], tuple(args)))
+                doubled.append(c)
+            calls = doubled
+        step.append((t, mode, calls))
+    g = pipe.graph(step)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    extra = (graph_region(pipe, g, K, dist) - base_ms) / K
+    del g, cold
+    return extra
+
+
 def e2e_pipelined(pipes, graphs, K):
     """The end-to-end region as an engine runs it: two buffer sets over the
     same resident K/V, so step i+1's host->device input copy and step i-1's
@@ -765,6 +800,13 @@ def main_ours(args):
     # around every launch (per-mode times and the roofline of the partial pass).
     ms_eager, events = timed_region(pipe, pipe.wise_step, args.steps, dist)
     ms_dense, events_dense = timed_region(pipe, pipe.dense_step, args.steps, dist)
+    # One partial of the first discover depth and of the first sparse depth,
+    # timed inside the captured step (marginal cost).
+    in_step = {}
+    for t, mode, calls in pipe.wise_step:
+        if mode in ("discover", "sparse") and mode not in {m for _, m in in_step} and \
+                any(c[0] == "partial" for c in calls):
+            in_step[(t, mode)] = partial_in_step_ms(pipe, ms, t, args.steps, dist)
     clocks = clock.stop()
     wall = time.time() - wall0
 
@@ -787,11 +829,13 @@ def main_ours(args):
     part_ms = sum(v for (tt, m, k), v in per.items() if k == "partial")
     achieved = part_bytes / (part_ms * 1e-3) / 1e9
     # Kernels launched in the timed regions: the graph replays and the eager
-    # passes, each over K WISE steps and K dense steps, and the three
-    # end-to-end regions' K WISE steps each.
+    # passes, each over K WISE steps and K dense steps, the three end-to-end
+    # regions' K WISE steps each, and the in-step partial timings' K steps
+    # with one extra partial each.
     launches = (2 * (pipe.launches_per_step(pipe.wise_step) +
                      pipe.launches_per_step(pipe.dense_step)) +
-                3 * pipe.launches_per_step(pipe.wise_step)) * args.steps
+                3 * pipe.launches_per_step(pipe.wise_step) +
+                len(in_step) * (pipe.launches_per_step(pipe.wise_step) + 1)) * args.steps
 
     R = w.num_rows
     modes = {}
@@ -806,6 +850,15 @@ def main_ours(args):
             "partial_gbs": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9, 1),
             "partial_frac_of_measured_hbm": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9 / peak, 3),
             "algorithmic_bytes": kv[(tt, m)]}
+        if (tt, m) in in_step:
+            t_in = max_over_ranks([in_step[(tt, m)]], dist, "cuda")[0]
+            modes[f"depth{tt}_{m}"].update({
+                "partial_in_step_us": round(t_in * 1e3, 2),
+                "partial_in_step_frac_of_measured_hbm": round(kv[(tt, m)] / (t_in * 1e-3) / 1e9 / peak, 3),
+                "in_step_note": "marginal time of one more such partial launch (over a private "
+                                "copy of the K/V pool, so no L2 reuse) inside the captured "
+                                "step, whose launches overlap the previous kernel; partial_us "
+                                "above is the eager launch bracketed by events"})
     dense_call = sum(per_dense.values()) / w.num_depths
     dense_part = statistics.mean(v for (tt, m, k), v in per_dense.items() if k == "partial")
     modes["dense"] = {"call_us": round(dense_call * 1e3, 2), "partial_us": round(dense_part * 1e3, 2),
@@ -923,7 +976,8 @@ def sparse_scaling_main(args):
         points = [(L, k, False)]
     rows = []
     for L, k, with_dense in points:
-        d = sparse_scaling_inputs(R, H, D, L, k, seed=4242 + L + k)
+        d = sparse_scaling_inputs(R, H, D, L, k, seed=4242 + L + k,
+                                  shared_blocks=args.shared_blocks)
         shape = W.make_shape(num_rows=R, num_q_heads=H, num_kv_heads=H, head_dim=D, page_size=16,
                              max_pages_per_row=d["page_table"].shape[1], num_pages=d["num_pages"],
                              max_blocks=d["max_blocks"], dtype=W.DTYPE_BF16, eta=0.95)
@@ -992,6 +1046,7 @@ def sparse_scaling_main(args):
         del d, ws, out, lse
         torch.cuda.empty_cache()
     print(json.dumps({"sparse_scaling": rows, "rows": R, "heads": H, "head_dim": D,
+                      "blocks": "shared by a row's heads" if args.shared_blocks else "per head",
                       "peak_gbs": peak, "peak_kind": peak_kind, "reps": reps,
                       "l2": "flushed by a 512 MiB write before every call"}))
 

@@ -248,13 +248,15 @@ WORKLOADS = tuple(BASE_SEEDS)
 
 
 def sparse_scaling_inputs(R: int, H: int, D: int, L: int, k: int, seed: int,
-                          device="cuda", page_size: int = 16, tile_tokens: int = 32):
+                          device="cuda", page_size: int = 16, tile_tokens: int = 32,
+                          shared_blocks: bool = False):
     """Inputs of the sparse-scaling measurement, drawn on the device (timing
     only; no parity check reads them): R rows of L tokens, H heads MHA, bf16
     q/K/V ~ N(0,1) from a seeded device generator, each row's pages at a
     seeded permutation of a pool exactly the batch's size, and per (row, head)
     k distinct blocks drawn uniformly without replacement from the row's
-    L / tile_tokens blocks (a seeded host draw).  Returns q, k_cache, v_cache,
+    L / tile_tokens blocks (a seeded host draw; with shared_blocks, one draw per
+    row that all its heads share).  Returns q, k_cache, v_cache,
     page_table, seq_lens and the mask [R, H, W] (int32 words)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
@@ -271,7 +273,8 @@ def sparse_scaling_inputs(R: int, H: int, D: int, L: int, k: int, seed: int,
     nb = -(-L // tile_tokens)
     W = -(-nb // 32)
     rng = _rng(seed, 0, _TENSOR_IDS["plant"])
-    chosen = np.argsort(rng.random((R, H, nb)), axis=-1)[..., :min(k, nb)]
+    draws = rng.random((R, 1 if shared_blocks else H, nb))
+    chosen = np.broadcast_to(np.argsort(draws, axis=-1)[..., :min(k, nb)], (R, H, min(k, nb)))
     bits = np.zeros((R, H, 32 * W), dtype=bool)
     np.put_along_axis(bits, chosen, True, axis=-1)
     words = np.packbits(bits, axis=-1, bitorder="little").view(np.int32).reshape(R, H, W)
