@@ -70,3 +70,39 @@ def test_sparse_scaling_point():
     parts = pt["sparse_compact_us"] + pt["sparse_partial_us"] + pt["sparse_finish_us"]
     assert 0 < parts <= pt["sparse_call_us"] * 1.01
     assert 0 < pt["partial_frac"] < 1.5
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun only rank 0 runs the reference arm; the others print
+    nothing and exit 0."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert not [l for l in res.stdout.splitlines() if l.startswith("{")]
+
+
+def test_traffic_record_round_trip(tmp_path, monkeypatch):
+    """An ncu '--page raw --csv' export (header row, units row, one row per
+    launch) becomes per-launch DRAM bytes keyed by the kernel's source hash;
+    the bench scales them to its own rows and drops them once the kernel's
+    source or the workload differs."""
+    import bench
+    raw = tmp_path / "raw.csv"
+    raw.write_text(
+        '"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+        '"","","Mbyte","Kbyte"\n'
+        '"0","void wise::partial_kernel<...>(...)","100","500"\n'
+        '"1","void wise::finish_short_kernel<...>(...)","7","7"\n'
+        '"2","void wise::partial_kernel<...>(...)","1,000","0"\n')
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "traffic.json"))
+    bench.record_traffic(str(raw), 32, "ouro1.4b_1k")
+    rec = json.loads((tmp_path / "traffic.json").read_text())
+    assert rec["per_launch_bytes"] == [100.5e6, 1000e6]
+    assert rec["kernel_source_sha256"] == bench.kernel_source_hash()
+    assert bench.recorded_traffic(64, "ouro1.4b_1k") == pytest.approx((100.5e6 + 1000e6) / 2 * 2)
+    assert bench.recorded_traffic(64, "gqa_32k") is None
+    rec["kernel_source_sha256"] = "0" * 64
+    (tmp_path / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic(64, "ouro1.4b_1k") is None
