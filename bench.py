@@ -113,13 +113,23 @@ def oracle_sample_main(spec_json: str) -> None:
         inputs.append(conv)
     sup = np.zeros((w.num_rows, w.num_kv_heads, -(-w.max_blocks // 32)), np.uint32)
 
+    mode_names = {0: "dense", 1: "discover", 2: "discover_union", 3: "sparse"}
+
+    def depth_name(m):
+        u = {int(x) for x in m}
+        return mode_names[u.pop()] if len(u) == 1 else "mixed"
+
+    per_depth = [0.0] * w.num_depths
+
     def one_pass(O):
         s = sup
         for t in range(w.num_depths):
             d = inputs[t]
+            t0 = time.perf_counter()
             s = O.decode_layer(d["q"], d["k_cache"], d["v_cache"], w.page_table, w.seq_lens,
                                w.depth_modes[t], s, eta=w.eta, tile_tokens=w.tile_tokens,
                                diagnostics=False)["support"]
+            per_depth[t] += time.perf_counter() - t0
 
     report = {"row_calls_per_pass": w.num_rows * w.num_depths}
     for key, threads, target in (("all", 0, spec["seconds"]), ("one", 1, spec["seconds_1t"])):
@@ -128,6 +138,7 @@ def oracle_sample_main(spec_json: str) -> None:
         O = CppOracle("f32", threads=threads)
         for _ in range(max(1, spec.get("warmup", 1))):  # untimed: page-in, thread start
             one_pass(O)
+        per_depth[:] = [0.0] * w.num_depths
         passes, t0 = 0, time.perf_counter()
         while True:
             one_pass(O)
@@ -135,7 +146,10 @@ def oracle_sample_main(spec_json: str) -> None:
             el = time.perf_counter() - t0
             if (spec.get("reps") and passes >= spec["reps"]) or (not spec.get("reps") and el >= target):
                 break
-        report[key] = {"seconds": el, "passes": passes, "threads": O.last_threads}
+        report[key] = {"seconds": el, "passes": passes, "threads": O.last_threads,
+                       "per_mode": {f"depth{t}_{depth_name(w.depth_modes[t])}":
+                                    round(w.num_rows * passes / per_depth[t], 1)
+                                    for t in range(w.num_depths)}}
     print(json.dumps(report))
 
 
@@ -169,7 +183,8 @@ def run_oracle_sample(workload: str, rows: int, seconds: float = 10.0, seconds_1
     value = per * a["passes"] / a["seconds"]
     sample = (f"{rows} rows of {workload} (same recipe), {a['passes']}x the 4-depth schedule "
               f"through the C++ fp32 oracle on {a['threads']} host threads ({a['seconds']:.1f} s)")
-    result = {"value": value, "unit": UNIT, "cores": a["threads"], "kind": "oracle"}
+    result = {"value": value, "unit": UNIT, "cores": a["threads"], "kind": "oracle",
+              "per_mode_rows_per_s": a["per_mode"]}
     if "one" in out:
         o = out["one"]
         result["value_1_thread"] = round(per * o["passes"] / o["seconds"], 3)
@@ -1070,7 +1085,8 @@ def main_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"{args.workload} (oracle sample of {rows} rows per step)"},
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": res["cores"],
-                            "kind": "oracle", "sample": res["sample"]},
+                            "kind": "oracle", "sample": res["sample"],
+                            "per_mode_rows_per_s": res["per_mode_rows_per_s"]},
            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0},
            "wall_s": round(time.perf_counter() - t0, 1)}
