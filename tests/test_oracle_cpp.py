@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 
 from block_sparse_paged_split_gb300.workload import (MODE_DISCOVER, MODE_DISCOVER_UNION,
-                                                     MODE_SPARSE, custom_workload)
+                                                     MODE_SPARSE, custom_workload, make_workload)
 from oracle import cpp_oracle
 from oracle import wise_oracle as numpy_oracle
 from tests import oracle_pins
@@ -40,6 +40,10 @@ def test_cpp_oracle_pin(pin, precision):
 
 
 def _schedule_case(name):
+    if name == "tiny":
+        # 4 x 256 tokens, 2 heads, D=64, fp32 storage; rows run [dense,
+        # discover, sparse, sparse] then [dense, union-discover, sparse, sparse]
+        return make_workload("tiny")
     if name == "mha_1k":
         lens = np.array([1024, 1024, 1000, 0], np.int32)
         w = custom_workload(R=4, Hq=16, Hkv=16, D=128, dtype="bf16", depths=4, n_planted=4,
@@ -57,7 +61,7 @@ def _schedule_case(name):
     return w
 
 
-@pytest.mark.parametrize("case", ["mha_1k", "gqa_4k"])
+@pytest.mark.parametrize("case", ["tiny", "mha_1k", "gqa_4k"])
 def test_f32_against_float64_oracle(case):
     """The 4-depth schedule; both oracles start every depth from the float64
     oracle's mask (sparse parity is checked on the same mask)."""
