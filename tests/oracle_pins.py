@@ -170,6 +170,46 @@ def pin_sparse_masked_sdpa(O) -> List[str]:
     return fails
 
 
+def pin_sparse_bruteforce_loops(O) -> List[str]:
+    """Sparse (and dense) attention written out token by token in plain
+    Python floats on tiny inputs: s_j = scale * sum_d q_d k_jd over the
+    tokens of the selected blocks only, m = max s_j, Z = sum exp(s_j - m),
+    o_d = sum exp(s_j - m) v_jd / Z, lse = m + log Z [WISE PR, Tests: sparse
+    output matches masked attention]."""
+    fails = []
+    lens = [70, 33, 96]
+    w, d = make_case(2, 1, 16, "f32", lens, 27)
+    sup = random_support(w, 3, density=0.5)
+    for mode in (MODE_SPARSE, MODE_DENSE):
+        res = run(O, w, d, [mode] * len(lens), sup)
+        scale = 1.0 / math.sqrt(16)
+        for r, L in enumerate(lens):
+            K = d["k_rows"][r][:, 0, :].tolist()
+            V = d["v_rows"][r][:, 0, :].tolist()
+            words = [int(x) for x in sup[r, 0]]
+            active = [mode == MODE_DENSE or (words[(j // 32) // 32] >> ((j // 32) % 32)) & 1
+                      for j in range(L)]
+            for h in range(2):
+                q = d["q"][r, h].tolist()
+                s = [scale * sum(q[i] * K[j][i] for i in range(16)) for j in range(L)]
+                act = [j for j in range(L) if active[j]]
+                if not act:
+                    if res["lse"][r, h] != -math.inf:
+                        fails.append(f"empty selection r={r} h={h} has an LSE")
+                    continue
+                m = max(s[j] for j in act)
+                e = {j: math.exp(s[j] - m) for j in act}
+                Z = sum(e[j] for j in act)
+                o = [sum(e[j] * V[j][i] for j in act) / Z for i in range(16)]
+                lse = m + math.log(Z)
+                if max(abs(a - b) for a, b in zip(o, res["out"][r, h])) > tol(O, "out_atol") + \
+                        tol(O, "out_rtol") * max(abs(x) for x in o):
+                    fails.append(f"mode {mode} out differs from the loops r={r} h={h}")
+                if abs(lse - res["lse"][r, h]) > tol(O, "lse"):
+                    fails.append(f"mode {mode} lse differs from the loops r={r} h={h}")
+    return fails
+
+
 def pin_all_blocks_sparse_is_dense(O) -> List[str]:
     """Every block selected: sparse equals dense bitwise [WISE PR, Tests:
     compaction with every block selected is bitwise dense]."""
@@ -460,7 +500,8 @@ def pin_compaction(O) -> List[str]:
     return fails
 
 
-ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_all_blocks_sparse_is_dense,
+ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_sparse_bruteforce_loops,
+            pin_all_blocks_sparse_is_dense,
             pin_paging_invariance, pin_page_size_invariance, pin_block_masses, pin_selection_bruteforce,
             pin_selection_golden, pin_selection_limits, pin_union, pin_density_example,
             pin_compaction, pin_head_union]
