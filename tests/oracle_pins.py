@@ -7,13 +7,17 @@ plant a mistake in a private copy of the oracle and confirm some pin catches it.
 What the pins compare against:
   * library routines in float64 (torch scaled_dot_product_attention, softmax,
     logsumexp, amax; numpy unpackbits);
+  * attention written out token by token in plain Python floats (tiny inputs);
   * brute force over every subset of block masses;
   * exact closed-form selections (tests/golden/selection_cases.json);
   * the pages' density example (tests/golden/union_density_example.json);
   * a hand-worked head-union example (tests/golden/head_union_example.json);
   * invariances the pages state: all-blocks sparse is dense bitwise, block
     masses from the LSE equal softmax block sums, the union equals the OR of
-    per-depth selections; and the page layout cannot matter.
+    per-depth selections; and the page layout and the page size cannot matter.
+
+An oracle that computes in float32 carries its own TOLERANCES (see
+F32_TOLERANCES); the float64 oracles use the module's.
 """
 from __future__ import annotations
 
