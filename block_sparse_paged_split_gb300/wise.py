@@ -87,6 +87,7 @@ def library() -> ctypes.CDLL:
             "wise_support_head_union": [S, P, P],
             "wise_block_mass": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_validate": [S, P, P, P, P, P, P],
+            "wise_selftest_wait_timeout": [P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -272,6 +273,13 @@ def wise_validate(shape, page_table, seq_lens, modes, support, err_word, stream=
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(modes, torch.int8, "modes"),
         _ptr(support, torch.int32, "support"), _ptr(err_word, torch.int32, "err_word"),
         _stream(stream)))
+
+
+def wise_selftest_wait_timeout(status_word: torch.Tensor, stream=None) -> None:
+    """Run the bounded-wait self-test (see include/wise.h): about 500 ms later
+    the device int32 `status_word` has DEVERR_WAIT_TIMEOUT set."""
+    _check(library().wise_selftest_wait_timeout(_ptr(status_word, torch.int32, "status_word"),
+                                                 _stream(stream)))
 
 
 def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, torch.Tensor]:

@@ -338,6 +338,18 @@ wise_status wise_decode_noalloc(const wise_shape *shape, const void *q,
                                 const int8_t *modes, uint32_t *support, void *out,
                                 float *lse, wise_stream_t stream);
 
+/* Self-test of the failure path (the pages have no counterpart; it computes
+ * nothing of the method).  Every mbarrier wait in this library's kernels is
+ * bounded by %globaltimer (500 ms) and, when it runs out, sets
+ * WISE_DEVERR_WAIT_TIMEOUT in a status word and returns instead of hanging.
+ * This call launches one CTA that waits, through the same bounded wait, on a
+ * barrier nothing ever arrives on: after about 500 ms it ORs
+ * WISE_DEVERR_WAIT_TIMEOUT into *status_word and returns, with nothing in
+ * flight and the context usable.  status_word: a 4-byte aligned device
+ * int32 the caller owns (zero it first to read the bit).  Asynchronous on
+ * `stream`; a NULL or misaligned pointer returns WISE_ERR_INVALID_ARG. */
+wise_status wise_selftest_wait_timeout(int32_t *status_word, wise_stream_t stream);
+
 /* Static name of a status code. */
 const char *wise_status_string(wise_status status);
 

@@ -150,3 +150,10 @@ def test_default_split_size(lib):
     s = _shape(num_rows=2, num_q_heads=32, num_kv_heads=8, max_blocks=1024, max_pages_per_row=2048,
                tiles_per_item=16)
     assert W.wise_workspace_layout(s)["max_items"] == 2 * 8 * 64
+
+
+def test_selftest_rejects_a_bad_status_pointer(lib):
+    P = ctypes.c_void_p
+    assert lib.wise_selftest_wait_timeout(None, None) == 1
+    assert lib.wise_selftest_wait_timeout(P(4098), None) == 1
+    assert b"status_word" in lib.wise_last_error()
