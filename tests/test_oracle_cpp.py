@@ -110,6 +110,9 @@ def test_thread_count_never_changes_results():
 
 # ----------------------------------------------------------------------------- mutants
 # (name, text in wise_oracle.cpp, replacement); each text occurs exactly once.
+# Every mutant keeps its memory accesses inside the arrays it is given: a
+# mutant library that read out of bounds could take the test process down
+# instead of failing a pin.
 MUTANTS = [
     ("scale_squared", "s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
     ("slot_off_by_one", "const size_t krow = ((size_t(page) * PS + j % PS) * Hkv + g) * D;",
@@ -117,7 +120,7 @@ MUTANTS = [
     ("value_of_wrong_kv_head", "const size_t vrow = ((size_t(page) * PS + j % PS) * Hkv + g) * D;",
      "const size_t vrow = ((size_t(page) * PS + j % PS) * Hkv + (g + 1) % Hkv) * D;"),
     ("query_of_wrong_head", "static_cast<T>(stored(q, bf16, pair * D + d))",
-     "static_cast<T>(stored(q, bf16, (pair ^ 1) * D + d))"),
+     "static_cast<T>(stored(q, bf16, (size_t(r) * Hq + (h + 1) % Hq) * D + d))"),
     ("tile_sum_without_max", "lb += std::exp(s[j] - mb);", "lb += std::exp(s[j]);"),
     ("mass_not_normalised", "pm[b] = eb / Z;", "pm[b] = eb;"),
     ("last_token_dropped", "for (int j = lo; j < hi; ++j) {", "for (int j = lo; j + 1 < hi; ++j) {"),
@@ -133,8 +136,8 @@ MUTANTS = [
      "while (i < c && lst[i] <= (s + 1) * T) ++i;"),
     ("head_union_skips_last_head", "for (int g = 0; g < kv_heads; ++g)\n        any = any ||",
      "for (int g = 0; g + 1 < kv_heads; ++g)\n        any = any ||"),
-    ("page_size_fixed_at_16", "const int B = P.tile_tokens, PS = P.page_size;",
-     "const int B = P.tile_tokens, PS = 16;"),
+    ("slot_ignores_page_size", "const size_t krow = ((size_t(page) * PS + j % PS) * Hkv + g) * D;",
+     "const size_t krow = ((size_t(page) * PS + (j % PS) % 16) * Hkv + g) * D;"),
     ("padding_row_gets_output", "if (L <= 0) return;  // padding row",
      "if (L <= 0) { out[0] = 1.0; return; }"),
 ]
