@@ -146,6 +146,18 @@ class CppOracle:
         support = np.ascontiguousarray(support, np.uint32)
         W = support.shape[2]
         NB = 32 * W
+        # The C++ code trusts its indices: check them here so a bad input
+        # raises instead of reading out of bounds.
+        if page_table.shape[0] != R or seq_lens.shape[0] != R or modes.shape[0] != R or \
+                support.shape[:2] != (R, Hkv) or Hq % Hkv:
+            raise ValueError("inconsistent batch shapes")
+        for r in range(R):
+            L = int(seq_lens[r])
+            if L < 0 or L > page_table.shape[1] * P or -(-L // tile_tokens) > NB:
+                raise ValueError(f"row {r}: length {L} exceeds its pages or its mask")
+            used = page_table[r, :-(-L // P)]
+            if used.size and (used.min() < 0 or used.max() >= num_pages):
+                raise ValueError(f"row {r}: page id outside the pool")
         prob = _Problem(R, Hq, Hkv, D, P, tile_tokens, page_table.shape[1], num_pages, W, bf16,
                         float(scale), float(eta))
         out = np.zeros((R, Hq, D))
