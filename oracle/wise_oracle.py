@@ -3,7 +3,9 @@
 TEST INFRASTRUCTURE ONLY.  This module is the plain, slow definition that the
 CUDA library is checked against.  Only the tests, the smoke check and the
 benchmark's CPU-baseline leg may import it; the library never does, and it
-imports nothing from the library.  Arithmetic is numpy float64.
+imports nothing from the library.  Arithmetic is numpy float64.  Its sibling
+wise_oracle.cpp states the same definition in plain C++ with fp32 math; the
+same pins check both.
 
 Source: the vllm-rlt pull request "WISE working-set decode" (PR #143),
 cited below as [WISE PR, <section>].  What it fixes:
