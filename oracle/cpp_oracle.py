@@ -104,8 +104,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.wise_oracle_head_union.restype = None
     lib.wise_oracle_union_density.argtypes = [vp, vp, i32, i32, i32, i32]
     lib.wise_oracle_union_density.restype = dbl
-    lib.wise_oracle_compact.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64]
-    lib.wise_oracle_compact.restype = i64
+    lib.wise_oracle_compact.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+    lib.wise_oracle_compact.restype = None
     return lib
 
 
@@ -231,7 +231,7 @@ class CppOracle:
         return float(self.lib.wise_oracle_union_density(_ptr(sup), _ptr(lens), R, Hkv, W, B))
 
     # ------------------------------------------------------------------ compaction
-    def compact_tiles(self, support, modes, seq_lens, B: int, tiles_per_item: int):
+    def compact_tiles(self, support, modes, seq_lens, B: int):
         sup = np.ascontiguousarray(support, np.uint32)
         modes = np.ascontiguousarray(modes, np.int8)
         lens = np.ascontiguousarray(seq_lens, np.int32)
@@ -239,13 +239,8 @@ class CppOracle:
         NB = 32 * W
         lists = np.zeros((R, Hkv, NB), np.int32)
         counts = np.zeros((R, Hkv), np.int32)
-        cap = max(1, R * Hkv * NB)
-        items = np.zeros((cap, 5), np.int32)
-        n = self.lib.wise_oracle_compact(_ptr(sup), _ptr(modes), _ptr(lens), R, Hkv, W, B,
-                                         tiles_per_item, _ptr(lists), _ptr(counts), _ptr(items),
-                                         cap)
-        if n < 0:
-            raise RuntimeError("item capacity exceeded")
+        self.lib.wise_oracle_compact(_ptr(sup), _ptr(modes), _ptr(lens), R, Hkv, W, B,
+                                     _ptr(lists), _ptr(counts))
         return {"lists": [[lists[r, g, :counts[r, g]].copy() for g in range(Hkv)]
                           for r in range(R)],
-                "items": items[:n].copy()}
+                "counts": counts}

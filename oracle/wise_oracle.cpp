@@ -379,20 +379,17 @@ double wise_oracle_union_density(const uint32_t* support, const int32_t* seq_len
   return causal ? double(sel) / double(causal) : 0.0;
 }
 
-/* Tile lists and work items [WISE PR, "What changes": sparse rows attend only
- * their selected tiles, compacted first so the loop has no branch; programs
- * cover about eight tiles each].  Per (row, KV head) the list is the
- * ascending selected blocks below the row's block count (sparse rows) or
- * every block (other modes), written to lists [R, Hkv, 32W] with its length
- * in counts [R, Hkv].  Item s of a pair holds the list's tiles whose block
- * lies in [s*T, s*T + T); a range with no tile has no item.  Items, ordered
- * by (row, head, s), are (row, head, s, first index in the list, tile count)
- * rows of items [capacity, 5].  Returns the item count, or -1 past capacity. */
-int64_t wise_oracle_compact(const uint32_t* support, const int8_t* modes, const int32_t* seq_lens,
-                            int rows, int kv_heads, int words, int tile_tokens, int tiles_per_item,
-                            int32_t* lists, int32_t* counts, int32_t* items, int64_t capacity) {
-  const int NB = 32 * words, T = tiles_per_item;
-  int64_t n = 0;
+/* The compacted tile lists [WISE PR, "What changes": sparse rows attend only
+ * their selected tiles, compacted first so the loop has no branch].  Per
+ * (row, KV head) the list is the ascending selected blocks below the row's
+ * block count (sparse rows) or every block (other modes), written to
+ * lists [R, Hkv, 32W] with its length in counts [R, Hkv].  How the lists are
+ * cut into work items is the kernel's scheduling choice, not part of the
+ * definition. */
+void wise_oracle_compact(const uint32_t* support, const int8_t* modes, const int32_t* seq_lens,
+                         int rows, int kv_heads, int words, int tile_tokens, int32_t* lists,
+                         int32_t* counts) {
+  const int NB = 32 * words;
   for (int r = 0; r < rows; ++r) {
     const int nb = seq_lens[r] > 0 ? (seq_lens[r] + tile_tokens - 1) / tile_tokens : 0;
     for (int g = 0; g < kv_heads; ++g) {
@@ -402,22 +399,8 @@ int64_t wise_oracle_compact(const uint32_t* support, const int8_t* modes, const 
       for (int b = 0; b < nb; ++b)
         if (modes[r] != SPARSE || mask_bit(w, b)) lst[c++] = b;
       counts[size_t(r) * kv_heads + g] = c;
-      int i = 0;
-      for (int s = 0; s * T < nb; ++s) {
-        const int first = i;
-        while (i < c && lst[i] < (s + 1) * T) ++i;
-        if (i == first) continue;
-        if (n >= capacity) return -1;
-        int32_t* it = items + 5 * n++;
-        it[0] = r;
-        it[1] = g;
-        it[2] = s;
-        it[3] = first;
-        it[4] = i - first;
-      }
     }
   }
-  return n;
 }
 
 }  // extern "C"

@@ -216,21 +216,21 @@ def union_density(support: np.ndarray, seq_lens: np.ndarray, B: int) -> float:
 
 
 # --------------------------------------------------------------------------- compaction
-def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray, B: int,
-                  tiles_per_item: int) -> Dict[str, object]:
-    """Tile lists and the work list [WISE PR, "What changes": sparse rows
-    attend only their selected tiles, compacted first so the loop has no
-    branch; programs cover about eight tiles each].
+def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray,
+                  B: int) -> Dict[str, object]:
+    """The compacted tile lists [WISE PR, "What changes": sparse rows attend
+    only their selected tiles, compacted first so the loop has no branch].
 
-    Per (row, KV head): the list is the ascending selected blocks b < n_b for
-    sparse rows and 0..n_b-1 otherwise.  Work item s of the pair holds the
-    list's tiles whose blocks lie in [s*T, s*T + T) (T = tiles_per_item); a
-    range with no tile has no item.  Items are ordered by (row, head, s) and
-    given as (row, head, s, first index in the list, tile count)."""
+    Per (row, KV head): the ascending block indices b < n_b whose mask bit is
+    set for sparse rows, and every block 0..n_b-1 for the other modes.  How a
+    list is cut into work items for the GPU's programs ("about eight tiles"
+    each) is a scheduling choice the pages leave open, so it is not defined
+    here; the tests check the kernel's items against these lists by their
+    properties.  Returns dict(lists=[R][Hkv] int32 arrays, counts=int32
+    [R, Hkv])."""
     R, Hkv, _ = support.shape
-    T = tiles_per_item
     lists: List[List[np.ndarray]] = []
-    items = []
+    counts = np.zeros((R, Hkv), dtype=np.int32)
     for r in range(R):
         nb = -(-int(seq_lens[r]) // B)
         per = []
@@ -240,12 +240,9 @@ def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray, 
             else:
                 lst = np.arange(nb, dtype=np.int32)
             per.append(lst)
-            for s in range(-(-nb // T)):
-                in_range = np.nonzero((lst >= s * T) & (lst < (s + 1) * T))[0]
-                if in_range.size:
-                    items.append((r, g, s, int(in_range[0]), int(in_range.size)))
+            counts[r, g] = lst.shape[0]
         lists.append(per)
-    return {"lists": lists, "items": np.array(items, dtype=np.int32).reshape(-1, 5)}
+    return {"lists": lists, "counts": counts}
 
 
 # --------------------------------------------------------------------------- one call

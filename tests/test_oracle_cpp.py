@@ -132,8 +132,8 @@ MUTANTS = [
     ("sparse_ignores_mask", "return mode != SPARSE || mask_bit(words, j / B);", "return true;"),
     ("bit_order_reversed", "return (words[b >> 5] >> (b & 31)) & 1u;",
      "return (words[b >> 5] >> (31 - (b & 31))) & 1u;"),
-    ("compaction_range_overlap", "while (i < c && lst[i] < (s + 1) * T) ++i;",
-     "while (i < c && lst[i] <= (s + 1) * T) ++i;"),
+    ("compaction_drops_last_block", "if (modes[r] != SPARSE || mask_bit(w, b)) lst[c++] = b;",
+     "if ((modes[r] != SPARSE || mask_bit(w, b)) && b + 1 < nb) lst[c++] = b;"),
     ("head_union_skips_last_head", "for (int g = 0; g < kv_heads; ++g)\n        any = any ||",
      "for (int g = 0; g + 1 < kv_heads; ++g)\n        any = any ||"),
     ("slot_ignores_page_size", "const size_t krow = ((size_t(page) * PS + j % PS) * Hkv + g) * D;",

@@ -130,22 +130,21 @@ def m_mask_bit_order_reversed(O):
     O.mask_bits = mask_bits
 
 
-def m_compaction_split_off_by_one(O):
+def m_compaction_drops_last_block(O):
     orig = O.compact_tiles
 
-    def compact_tiles(support, modes, seq_lens, B, T):
-        return orig(support, modes, seq_lens, B, T + 1)
+    def compact_tiles(support, modes, seq_lens, B):
+        res = orig(support, modes, seq_lens, B)
+        lists = [[lst[:-1] for lst in per] for per in res["lists"]]
+        return {"lists": lists, "counts": np.maximum(res["counts"] - 1, 0)}
     O.compact_tiles = compact_tiles
 
 
-def m_compaction_first_index_shifted(O):
+def m_compaction_ignores_mode(O):
     orig = O.compact_tiles
 
-    def compact_tiles(support, modes, seq_lens, B, T):
-        res = orig(support, modes, seq_lens, B, T)
-        items = res["items"].copy()
-        items[:, 3] = np.maximum(items[:, 3] - 1, 0)
-        return {**res, "items": items}
+    def compact_tiles(support, modes, seq_lens, B):
+        return orig(support, np.full_like(np.asarray(modes), oracle_pins.MODE_SPARSE), seq_lens, B)
     O.compact_tiles = compact_tiles
 
 
@@ -162,8 +161,8 @@ def m_head_union_skips_last_head(O):
 MUTANTS = [m_scale_squared, m_slot_off_by_one, m_page_order_reversed, m_wrong_kv_head, m_unnormalised_output,
            m_tile_sum_without_max, m_masses_drop_partial_block, m_ties_to_higher_index,
            m_strict_cutoff, m_one_extra_block, m_union_overwrites, m_mask_ignored,
-           m_mask_bit_order_reversed, m_compaction_split_off_by_one,
-           m_compaction_first_index_shifted, m_head_union_skips_last_head]
+           m_mask_bit_order_reversed, m_compaction_drops_last_block,
+           m_compaction_ignores_mode, m_head_union_skips_last_head]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
