@@ -74,6 +74,12 @@ def parse():
     p.add_argument("--overlap", action="store_true",
                    help="alternate the two slot sets and start a depth that reuses the previous "
                         "compaction while the previous finish runs (measured: no gain at 1K)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="measure only the headline workload (the default run also measures "
+                        "the 4K, mixed 8K and 32K grouped-query workloads)")
+    p.add_argument("--no-sparse-list", action="store_true",
+                   help="sparse depths get their own compaction instead of the work list the "
+                        "previous depth's finish builds")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--sparse-scaling", action="store_true",
@@ -323,7 +329,8 @@ class Pipeline:
     """The 4-depth WISE step with all ctypes arguments bound once."""
 
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
-                 lse_discover: bool = False, overlap: bool = False, share=None):
+                 lse_discover: bool = False, overlap: bool = False, share=None,
+                 sparse_list: bool = True, device_inputs: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -340,7 +347,15 @@ class Pipeline:
                                   dtype=W.DTYPE_BF16 if w.dtype == "bf16" else W.DTYPE_F32,
                                   eta=w.eta, tiles_per_item=tiles_per_item)
         dev = torch.device("cuda")
-        if share is None:
+        if share is None and device_inputs:
+            # K/V drawn on the device with the same recipe (Workload.
+            # depth_inputs_device): the long workloads' host draws take
+            # minutes, and timing does not depend on the values.
+            drawn = [w.depth_inputs_device(t) for t in range(w.num_depths)]
+            self.host = [{"q": d["q"]} for d in drawn]
+            self.depth = [{k: v for k, v in d.items() if k != "q"} for d in drawn]
+            del drawn
+        elif share is None:
             self.host = [w.depth_inputs(t) for t in range(w.num_depths)]
             self.depth = [{k: v.to(dev) for k, v in d.items() if k != "q"} for d in self.host]
         else:
@@ -396,12 +411,35 @@ class Pipeline:
         # they start only as the finish's CTAs leave -- hence off by default.
         self.overlap = overlap and not fold and not lse_discover
 
-        def calls(modes_t, t, compact=True, early=False):
+        # sparse_list=True: the finish of the depth before a run of all-sparse
+        # depths also writes their work list (WISE_FLAG_BUILD_SPARSE_LIST), and
+        # those depths run on it (WISE_FLAG_SPARSE_LIST) with no compaction
+        # launch.  The variants above keep a compaction per sparse depth.
+        self.sparse_list = sparse_list and not (fold or overlap or head_union or lse_discover)
+
+        def calls(modes_t, t, compact=True, early=False, build=False, on_list=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
+            if on_list:
+                f = W.FLAG_SPARSE_LIST
+                c.append(("partial", lib.wise_decode_partial_ex,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, f, st)))
+                c.append(("finish", lib.wise_decode_finish_ex,
+                          (S, m, sl, ws, nws, f, sup, self.out[t].data_ptr(),
+                           self.lse[t].data_ptr(), st)))
+                return c
             if compact:
                 c.append(("compact", lib.wise_compact_tiles, (S, m, sl, sup, ws, nws, st)))
+            if build:
+                c.append(("partial", lib.wise_decode_partial,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, st)))
+                c.append(("finish", lib.wise_decode_finish_ex,
+                          (S, m, sl, ws, nws, W.FLAG_BUILD_SPARSE_LIST, sup,
+                           self.out[t].data_ptr(), self.lse[t].data_ptr(), st)))
+                return c
             if self.overlap:
                 flags = (W.FLAG_SLOT_SET_1 if t % 2 else 0)
                 c.append(("partial", lib.wise_decode_partial_ex,
@@ -463,10 +501,21 @@ class Pipeline:
             return all(int(x) in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION) for x in m)
 
         self.wise_step = []
+        listed = False  # list 1 holds the work list of an all-sparse depth on the current mask
         for t in range(w.num_depths):
-            reuse = t > 0 and same_work_list(w.depth_modes[t], w.depth_modes[t - 1])
-            if lse_discover and all_discover(w.depth_modes[t]):
-                self.wise_step.append((t, depth_name(w.depth_modes[t]), lse_discover_calls(self.modes[t], t)))
+            dm = w.depth_modes
+            reuse = t > 0 and same_work_list(dm[t], dm[t - 1])
+            if lse_discover and all_discover(dm[t]):
+                self.wise_step.append((t, depth_name(dm[t]), lse_discover_calls(self.modes[t], t)))
+                continue
+            on_list = self.sparse_list and listed and all_sparse(dm[t])
+            build = (self.sparse_list and not all_sparse(dm[t]) and t + 1 < w.num_depths and
+                     all_sparse(dm[t + 1]))
+            listed = build or on_list
+            if on_list or build:
+                self.wise_step.append((t, depth_name(dm[t]),
+                                       calls(self.modes[t], t, compact=not reuse, build=build,
+                                             on_list=on_list)))
                 continue
             c = calls(self.modes[t], t, compact=not reuse, early=reuse)
             if head_union and all_sparse(w.depth_modes[t]) and not reuse:
@@ -761,6 +810,124 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def summarize_events(evts):
+    """Mean duration (ms) of each (depth, mode, kernel) over the timed steps."""
+    per = {}
+    for (tt, mode, kind, e0, e1) in evts:
+        per.setdefault((tt, mode, kind), []).append(e0.elapsed_time(e1))
+    return {k: statistics.mean(v) for k, v in per.items()}
+
+
+def mode_table(per, per_dense, kv, R, num_depths, peak):
+    """Per depth of the WISE step: call time (every launch of the depth) and
+    its partial launch, each as GB/s over the bytes the depth's partial pass
+    must read and as a fraction of the measured and of the nominal 8 TB/s HBM
+    bandwidth; then the dense baseline's mean call."""
+    def rates(nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return round(gbs, 1), round(gbs / peak, 3), round(gbs / 8000.0, 3)
+
+    modes = {}
+    for (tt, m, k) in sorted(per):
+        if k != "partial":
+            continue
+        call_ms = sum(v for (t2, m2, k2), v in per.items() if t2 == tt)
+        p_gbs, p_frac, p_nom = rates(kv[(tt, m)], per[(tt, m, k)])
+        c_gbs, c_frac, c_nom = rates(kv[(tt, m)], call_ms)
+        modes[f"depth{tt}_{m}"] = {
+            "call_us": round(call_ms * 1e3, 2), "partial_us": round(per[(tt, m, k)] * 1e3, 2),
+            "kernels_us": {k2: round(v * 1e3, 2) for (t2, m2, k2), v in per.items() if t2 == tt},
+            "rows_per_s": round(R / (call_ms * 1e-3), 1),
+            "partial_gbs": p_gbs, "partial_frac_of_measured_hbm": p_frac,
+            "partial_frac_of_nominal_8000_gbs": p_nom,
+            "call_gbs": c_gbs, "call_frac_of_measured_hbm": c_frac,
+            "call_frac_of_nominal_8000_gbs": c_nom,
+            "algorithmic_bytes": kv[(tt, m)]}
+    dense_call = sum(per_dense.values()) / num_depths
+    dense_part = statistics.mean(v for (tt, m, k), v in per_dense.items() if k == "partial")
+    p_gbs, p_frac, p_nom = rates(kv[(0, "dense")], dense_part)
+    c_gbs, c_frac, c_nom = rates(kv[(0, "dense")], dense_call)
+    modes["dense"] = {"call_us": round(dense_call * 1e3, 2), "partial_us": round(dense_part * 1e3, 2),
+                      "rows_per_s": round(R / (dense_call * 1e-3), 1),
+                      "partial_gbs": p_gbs, "partial_frac_of_measured_hbm": p_frac,
+                      "partial_frac_of_nominal_8000_gbs": p_nom,
+                      "call_gbs": c_gbs, "call_frac_of_measured_hbm": c_frac,
+                      "call_frac_of_nominal_8000_gbs": c_nom,
+                      "algorithmic_bytes": kv[(0, "dense")]}
+    return modes
+
+
+def algorithmic_bytes(pipe, w):
+    import numpy as np
+    kv = {}
+    for t, mode, _ in pipe.wise_step:
+        kv[(t, mode)] = pipe.kv_bytes(w.depth_modes[t]) + pipe.small_bytes()
+    for t, mode, _ in pipe.dense_step:
+        kv[(t, mode)] = pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) + pipe.small_bytes()
+    return kv
+
+
+# Workloads the default run measures after its headline, each on its own
+# K/V drawn on the device: the metric is quoted per mode at 1K, 4K and 8K
+# context, and the 32K grouped-query workload exercises the tensor-core path.
+SWEEP = ("ouro1.4b_4k", "mixed_8k", "gqa_32k")
+
+
+def sweep_workload(name, args, steps, peak):
+    """One workload of the default run's sweep: the WISE step and the dense
+    step, each captured as a CUDA graph and replayed `steps` times (CUDA
+    events around the replays), then launched eagerly with events around
+    every launch for the per-mode table."""
+    import numpy as np
+    import torch
+    from block_sparse_paged_split_gb300.workload import make_workload
+    t0 = time.time()
+    w = make_workload(name, **eta_kw(args.eta))
+    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
+                    device_inputs=True)
+    for _ in range(3):
+        pipe.run(pipe.wise_step)
+        pipe.run(pipe.dense_step)
+    torch.cuda.synchronize()
+    kv = algorithmic_bytes(pipe, w)
+    sparse_t = [t for t in range(w.num_depths) if any(int(x) == 3 for x in w.depth_modes[t])]
+    density = pipe.support_density(w.depth_modes[sparse_t[0]]) if sparse_t else None
+    g, gd = pipe.graph(pipe.wise_step), pipe.graph(pipe.dense_step)
+    for _ in range(3):
+        g.replay()
+        gd.replay()
+    ms = graph_region(pipe, g, steps, None)
+    ms_dense = graph_region(pipe, gd, steps, None)
+    _, ev = timed_region(pipe, pipe.wise_step, steps, None)
+    _, ev_dense = timed_region(pipe, pipe.dense_step, steps, None)
+    R = w.num_rows
+    rows_per_step = R * w.num_depths
+    out = {"workload": f"{R} rows x {int(w.seq_lens.min())}-{int(w.seq_lens.max())} tokens, "
+                       f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, D={w.head_dim}, "
+                       f"{w.num_depths} depth(s): " +
+                       ", ".join(pipe_depth_names(pipe)),
+           "step_ms": round(ms / steps, 4),
+           "rows_per_s": round(rows_per_step * steps / (ms * 1e-3), 1),
+           "dense_step_ms": round(ms_dense / steps, 4),
+           "speedup_vs_dense": round(ms_dense / ms, 3),
+           "support_density_blocks": round(density, 4) if density is not None else None,
+           "modes": mode_table(summarize_events(ev), summarize_events(ev_dense), kv, R,
+                               w.num_depths, peak),
+           "launches_per_step": pipe.launches_per_step(pipe.wise_step),
+           "dense_launches_per_step": pipe.launches_per_step(pipe.dense_step),
+           "steps": steps, "inputs": "K/V drawn on the device (same recipe, seeded)",
+           "wall_s": None}
+    del g, gd, pipe
+    torch.cuda.empty_cache()
+    out["wall_s"] = round(time.time() - t0, 1)
+    return out
+
+
+def pipe_depth_names(pipe):
+    return [f"{mode}" + ("" if not any(c[0] == "compact" for c in calls) else "+compact")
+            for _, mode, calls in pipe.wise_step]
+
+
 def main_ours(args):
     import numpy as np
     import torch
@@ -779,7 +946,8 @@ def main_ours(args):
     # Weak scaling: every rank decodes its own batch (rows are independent).
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank), **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
-                    lse_discover=args.lse_discover, overlap=args.overlap)
+                    lse_discover=args.lse_discover, overlap=args.overlap,
+                    sparse_list=not args.no_sparse_list)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -788,11 +956,7 @@ def main_ours(args):
 
     # Algorithmic bytes of each depth's partial launch (the mask is the same
     # every step: the inputs do not change).
-    kv = {}
-    for t, mode, _ in pipe.wise_step:
-        kv[(t, mode)] = pipe.kv_bytes(w.depth_modes[t]) + pipe.small_bytes()
-    for t, mode, _ in pipe.dense_step:
-        kv[(t, mode)] = pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) + pipe.small_bytes()
+    kv = algorithmic_bytes(pipe, w)
     sparse_depths = [t for t, mode, _ in pipe.wise_step if mode == "sparse"]
     density = (pipe.kv_bytes(w.depth_modes[sparse_depths[0]]) /
                pipe.kv_bytes(np.zeros(w.num_rows, np.int8))) if sparse_depths else None
@@ -829,14 +993,8 @@ def main_ours(args):
     ms, ms_dense_graph, ms_eager, ms_dense = max_over_ranks(
         [ms, ms_dense_graph, ms_eager, ms_dense], dist, "cuda")
 
-    def summarize(evts):
-        per = {}
-        for (tt, mode, kind, e0, e1) in evts:
-            per.setdefault((tt, mode, kind), []).append(e0.elapsed_time(e1))
-        return {k: statistics.mean(v) for k, v in per.items()}
-
-    per = summarize(events)
-    per_dense = summarize(events_dense)
+    per = summarize_events(events)
+    per_dense = summarize_events(events_dense)
     peak, peak_kind = peaks()
 
     # Dominant kernel: the split partial pass (all depths of the WISE step).
@@ -853,43 +1011,24 @@ def main_ours(args):
                 len(in_step) * (pipe.launches_per_step(pipe.wise_step) + 1)) * args.steps
 
     R = w.num_rows
-    modes = {}
-    for (tt, m, k) in sorted(per):
-        if k != "partial":
-            continue
-        call_ms = sum(v for (t2, m2, k2), v in per.items() if t2 == tt)
-        modes[f"depth{tt}_{m}"] = {
-            "call_us": round(call_ms * 1e3, 2), "partial_us": round(per[(tt, m, k)] * 1e3, 2),
-            "kernels_us": {k2: round(v * 1e3, 2) for (t2, m2, k2), v in per.items() if t2 == tt},
-            "rows_per_s": round(R / (call_ms * 1e-3), 1),
-            "partial_gbs": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9, 1),
-            "partial_frac_of_measured_hbm": round(kv[(tt, m)] / (per[(tt, m, k)] * 1e-3) / 1e9 / peak, 3),
-            "algorithmic_bytes": kv[(tt, m)]}
-        if (tt, m) in in_step:
-            t_in = max_over_ranks([in_step[(tt, m)]], dist, "cuda")[0]
-            modes[f"depth{tt}_{m}"].update({
-                "partial_in_step_us": round(t_in * 1e3, 2),
-                "partial_in_step_frac_of_measured_hbm": round(kv[(tt, m)] / (t_in * 1e-3) / 1e9 / peak, 3),
-                "in_step_note": "marginal time of one more such partial launch (over a private "
-                                "copy of the K/V pool, so no L2 reuse) inside the captured "
-                                "step, whose launches overlap the previous kernel; partial_us "
-                                "above is the eager launch bracketed by events"})
-    dense_call = sum(per_dense.values()) / w.num_depths
-    dense_part = statistics.mean(v for (tt, m, k), v in per_dense.items() if k == "partial")
-    modes["dense"] = {"call_us": round(dense_call * 1e3, 2), "partial_us": round(dense_part * 1e3, 2),
-                      "rows_per_s": round(R / (dense_call * 1e-3), 1),
-                      "partial_gbs": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9, 1),
-                      "partial_frac_of_measured_hbm": round(kv[(0, "dense")] / (dense_part * 1e-3) / 1e9 / peak, 3),
-                      "algorithmic_bytes": kv[(0, "dense")],
-                      "step_ms_eager": round(ms_dense / args.steps, 4),
-                      "step_ms_graph": round(ms_dense_graph / args.steps, 4)}
-
+    modes = mode_table(per, per_dense, kv, R, w.num_depths, peak)
+    for (tt, m) in in_step:
+        t_in = max_over_ranks([in_step[(tt, m)]], dist, "cuda")[0]
+        modes[f"depth{tt}_{m}"].update({
+            "partial_in_step_us": round(t_in * 1e3, 2),
+            "partial_in_step_frac_of_measured_hbm": round(kv[(tt, m)] / (t_in * 1e-3) / 1e9 / peak, 3),
+            "in_step_note": "marginal time of one more such partial launch (over a private "
+                            "copy of the K/V pool, so no L2 reuse) inside the captured "
+                            "step, whose launches overlap the previous kernel; partial_us "
+                            "above is the eager launch bracketed by events"})
+    modes["dense"].update({"step_ms_eager": round(ms_dense / args.steps, 4),
+                           "step_ms_graph": round(ms_dense_graph / args.steps, 4)})
 
     # End to end: the pipelined region (two buffer sets, copies overlapping
     # the compute), then the same steps with each step's copies in line.
     pipe_b = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold,
                       head_union=args.head_union, lse_discover=args.lse_discover,
-                      overlap=args.overlap, share=pipe)
+                      overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list)
     graph_b = pipe_b.graph(pipe_b.wise_step)
     e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
     e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)
@@ -899,6 +1038,23 @@ def main_ours(args):
                                                          dist, "cuda")
     value = whole_job_rate(world, rows_per_step, args.steps, ms)
     e2e_value = whole_job_rate(world, rows_per_step, args.steps, e2e_ms)
+
+    # The default run also measures the metric's other contexts (4K, the
+    # ragged 8K mixed batch) and the 32K grouped-query workload, each with
+    # fewer steps, on one GPU.
+    sweep = None
+    variant = args.fold or args.head_union or args.lse_discover or args.overlap
+    if (not args.no_sweep and world == 1 and args.workload == WORKLOAD and args.rows is None
+            and not variant):
+        del pipe_b, graph_b
+        torch.cuda.empty_cache()
+        sweep_steps = max(5, min(args.steps, 50))
+        sclock = ClockSampler(local)
+        sweep = {name: sweep_workload(name, args, sweep_steps, peak) for name in SWEEP}
+        sweep_clocks = sclock.stop()
+        for name, res in sweep.items():
+            launches += 2 * sweep_steps * res.pop("launches_per_step")
+            launches += 2 * sweep_steps * res.pop("dense_launches_per_step")
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -911,7 +1067,9 @@ def main_ours(args):
                                + (", sparse depths on the head union of the mask" if args.head_union else "")
                                + (", discovery from the LSE (second read of K)" if args.lse_discover else "")
                                + (", finish folded into the partial pass" if pipe.folded else "")
-                               + (", consecutive depths overlap (two slot sets, early start)" if pipe.overlap else ""),
+                               + (", consecutive depths overlap (two slot sets, early start)" if pipe.overlap else "")
+                               + (", sparse depths on the work list the union depth's finish "
+                                  "builds (no compaction launch)" if pipe.sparse_list else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "
@@ -952,6 +1110,13 @@ def main_ours(args):
         "clocks": clocks,
         "wall_s_timed": round(wall, 2),
     }
+    if sweep is not None:
+        result["modes_by_workload"] = sweep
+        result["modes_by_workload_clocks"] = sweep_clocks
+        result["config"]["sweep"] = (f"after the headline: {', '.join(SWEEP)}, each with its WISE "
+                                     f"and dense steps replayed from CUDA graphs "
+                                     f"({sweep_steps} steps) and launched eagerly for the "
+                                     f"per-mode table; K/V drawn on the device")
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, eta=args.eta)
     if rank == 0:

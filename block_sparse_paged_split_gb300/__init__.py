@@ -9,14 +9,16 @@ from .wise import (MODE_DENSE, MODE_DISCOVER, MODE_DISCOVER_UNION, MODE_SPARSE, 
                    DTYPE_F32, WiseError, alloc_workspace, make_shape, mask_words,
                    wise_block_mass, wise_compact_tiles, wise_decode, wise_decode_finish, wise_decode_partial,
                    wise_decode_partial_finish, wise_decode_partial_ex, wise_decode_finish_ex,
-                   FLAG_SLOT_SET_1, FLAG_EARLY_START,
+                   FLAG_SLOT_SET_1, FLAG_EARLY_START, FLAG_BUILD_SPARSE_LIST, FLAG_SPARSE_LIST,
                    wise_support_head_union, wise_support_union, wise_validate, wise_workspace_bytes,
-                   wise_workspace_layout, workspace_views)
+                   wise_workspace_layout, workspace_views, wise_mask, make_mask,
+                   wise_compact_tiles_m, wise_decode_finish_m, wise_decode_m, wise_validate_m)
 
 __all__ = ["MODE_DENSE", "MODE_DISCOVER", "MODE_DISCOVER_UNION", "MODE_SPARSE", "DTYPE_BF16",
            "DTYPE_F32", "WiseError", "alloc_workspace", "make_shape", "mask_words",
            "wise_block_mass", "wise_compact_tiles", "wise_decode", "wise_decode_finish", "wise_decode_partial",
            "wise_decode_partial_finish", "wise_decode_partial_ex", "wise_decode_finish_ex",
-           "FLAG_SLOT_SET_1", "FLAG_EARLY_START",
+           "FLAG_SLOT_SET_1", "FLAG_EARLY_START", "FLAG_BUILD_SPARSE_LIST", "FLAG_SPARSE_LIST",
            "wise_support_head_union", "wise_support_union", "wise_validate", "wise_workspace_bytes",
-           "wise_workspace_layout", "workspace_views"]
+           "wise_workspace_layout", "workspace_views", "wise_mask", "make_mask",
+           "wise_compact_tiles_m", "wise_decode_finish_m", "wise_decode_m", "wise_validate_m"]

@@ -100,6 +100,8 @@ KParams make_params(const wise_shape* s) {
   kp.scale_log2 = scale * kLog2e;
   kp.eta = s->eta;
   kp.early = 0;
+  kp.list1 = 0;
+  kp.build = 0;
   return kp;
 }
 
@@ -121,6 +123,9 @@ void compute_layout(const wise_shape* s, wise_layout* l) {
   l->partial_ml_1 = off;  off = up256(off + max_items * kp.G * sizeof(float2));
   l->partial_acc_1 = off; off = up256(off + max_items * kp.G * kp.D * sizeof(float));
   l->tile_stats_1 = off;  off = up256(off + (size_t)kp.R * kp.Hq * kp.max_blocks * sizeof(float2));
+  l->head_info_1 = off;   off = up256(off + pairs * sizeof(int4));
+  l->items_1 = off;       off = up256(off + (size_t)kp.T * max_items * sizeof(int4));
+  l->list1 = 128;
   l->max_items = max_items;
   l->total_bytes = off;
 }
@@ -147,6 +152,24 @@ wise_status make_view(const wise_shape* s, void* ws, size_t ws_bytes, WsView* v,
   v->partial_ml_other = reinterpret_cast<float2*>(b + (slot_set ? l.partial_ml : l.partial_ml_1));
   v->tickets = reinterpret_cast<int32_t*>(b + l.tickets);
   v->max_items = (int32_t)l.max_items;
+  v->l1_counter = reinterpret_cast<int32_t*>(b + l.list1);
+  v->head_info_1 = reinterpret_cast<int4*>(b + l.head_info_1);
+  v->items_1 = reinterpret_cast<int4*>(b + l.items_1);
+  return WISE_OK;
+}
+
+wise_status mask_view(const wise_shape* s, const wise_mask* m, MaskView* v) {
+  if (!m) return fail(WISE_ERR_INVALID_ARG, "mask descriptor is NULL");
+  const int64_t head_words = (int64_t)s->num_kv_heads * ((s->max_blocks + 31) / 32);
+  if (m->words && !aligned(m->words, 4)) return fail(WISE_ERR_INVALID_ARG, "mask words misaligned");
+  if (m->row_slot && !aligned(m->row_slot, 4))
+    return fail(WISE_ERR_INVALID_ARG, "row_slot misaligned");
+  if (m->num_slots < 0) return fail(WISE_ERR_INVALID_ARG, "num_slots < 0");
+  if (m->slot_stride < 0 || (m->slot_stride != 0 && m->slot_stride < head_words))
+    return fail(WISE_ERR_INVALID_ARG, "slot_stride must be 0 or at least num_kv_heads * W = %lld",
+                (long long)head_words);
+  *v = MaskView{m->words, m->row_slot, (long long)(m->slot_stride ? m->slot_stride : head_words),
+                m->num_slots};
   return WISE_OK;
 }
 
@@ -284,19 +307,30 @@ wise_status wise_workspace_layout(const wise_shape* shape, wise_layout* layout) 
   return WISE_OK;
 }
 
-wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
-                               const int32_t* seq_lens, const uint32_t* support,
-                               void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+wise_status wise_compact_tiles_m(const wise_shape* shape, const int8_t* modes,
+                                 const int32_t* seq_lens, const wise_mask* mask,
+                                 void* workspace, size_t workspace_bytes, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
   if (shape->num_rows > 0 && (!modes || !seq_lens))
     return fail(WISE_ERR_INVALID_ARG, "modes and seq_lens must not be NULL");
-  if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
-  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, support, ws,
+  MaskView mv;
+  if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
+  cudaError_t e = launch_compact(make_params(shape), modes, seq_lens, mv, ws,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "compact launch");
+}
+
+wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
+                               const int32_t* seq_lens, const uint32_t* support,
+                               void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
+  const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
+  return wise_compact_tiles_m(shape, modes, seq_lens, &m, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
@@ -310,13 +344,16 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
                          const FoldArgs& fa, uint32_t flags, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
-  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START))
+  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START | WISE_FLAG_SPARSE_LIST))
     return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((flags & WISE_FLAG_SPARSE_LIST) && fa.out)
+    return fail(WISE_ERR_INVALID_ARG, "the folded finish takes no WISE_FLAG_SPARSE_LIST");
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
     return st;
   if (shape->num_rows == 0) return WISE_OK;
-  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !modes)
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens ||
+      (!modes && !(flags & WISE_FLAG_SPARSE_LIST)))
     return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return fail(WISE_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
@@ -325,6 +362,7 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
   if ((st = tensor_map(shape, v_cache, &tmV)) != WISE_OK) return st;
   KParams kp = make_params(shape);
   kp.early = (flags & WISE_FLAG_EARLY_START) ? 1 : 0;
+  kp.list1 = (flags & WISE_FLAG_SPARSE_LIST) ? 1 : 0;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = shape->dtype == WISE_DTYPE_BF16
                       ? launch_partial_bf16(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, st_)
@@ -377,25 +415,48 @@ wise_status wise_decode_partial_finish(const wise_shape* shape, const void* q,
                       workspace_bytes, FoldArgs{support, out, lse}, 0u, stream);
 }
 
+wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
+                                 const int32_t* seq_lens, void* workspace,
+                                 size_t workspace_bytes, uint32_t flags, const wise_mask* mask,
+                                 void* out, float* lse, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_BUILD_SPARSE_LIST | WISE_FLAG_SPARSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  WsView ws;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
+    return st;
+  if (shape->num_rows == 0) return WISE_OK;
+  if ((!modes && !(flags & WISE_FLAG_SPARSE_LIST)) || !seq_lens || !out || !lse)
+    return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
+  MaskView mv;
+  if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
+  if ((flags & WISE_FLAG_BUILD_SPARSE_LIST) && !mv.words)
+    return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_BUILD_SPARSE_LIST needs the support mask");
+  if ((flags & WISE_FLAG_BUILD_SPARSE_LIST) && (flags & WISE_FLAG_SPARSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG,
+                "a call on list 1 leaves the mask as it is; it cannot build list 1 again");
+  if (!aligned(out, 16) || !aligned(lse, 4))
+    return fail(WISE_ERR_INVALID_ARG, "out must be 16-byte aligned, lse 4-byte");
+  KParams kp = make_params(shape);
+  kp.build = (flags & WISE_FLAG_BUILD_SPARSE_LIST) ? 1 : 0;
+  kp.list1 = (flags & WISE_FLAG_SPARSE_LIST) ? 1 : 0;
+  cudaError_t e = launch_finish(shape->dtype, kp, modes, seq_lens, ws, mv, out, lse,
+                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "finish launch");
+}
+
 wise_status wise_decode_finish_ex(const wise_shape* shape, const int8_t* modes,
                                   const int32_t* seq_lens, void* workspace,
                                   size_t workspace_bytes, uint32_t flags, uint32_t* support,
                                   void* out, float* lse, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
-  if (flags & ~(uint32_t)WISE_FLAG_SLOT_SET_1)
-    return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-  WsView ws;
-  if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
-    return st;
-  if (shape->num_rows == 0) return WISE_OK;
-  if (!modes || !seq_lens || !out || !lse)
-    return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!aligned(out, 16) || !aligned(lse, 4) || (support && !aligned(support, 4)))
+  if (support && !aligned(support, 4))
     return fail(WISE_ERR_INVALID_ARG, "out must be 16-byte aligned, lse and support 4-byte");
-  cudaError_t e = launch_finish(shape->dtype, make_params(shape), modes, seq_lens, ws, support,
-                                out, lse, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "finish launch");
+  const wise_mask m{support, nullptr, 0, 0};
+  return wise_decode_finish_m(shape, modes, seq_lens, workspace, workspace_bytes, flags, &m, out,
+                              lse, stream);
 }
 
 wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,
@@ -405,18 +466,30 @@ wise_status wise_decode_finish(const wise_shape* shape, const int8_t* modes,
                                out, lse, stream);
 }
 
-wise_status wise_decode(const wise_shape* shape, const void* q, const void* k_cache,
-                        const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
-                        const int8_t* modes, uint32_t* support, void* out, float* lse,
-                        void* workspace, size_t workspace_bytes, wise_stream_t stream) {
-  wise_status st = wise_compact_tiles(shape, modes, seq_lens, support, workspace,
-                                      workspace_bytes, stream);
+wise_status wise_decode_m(const wise_shape* shape, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
+                          const int8_t* modes, const wise_mask* mask, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = wise_compact_tiles_m(shape, modes, seq_lens, mask, workspace, workspace_bytes,
+                                        stream);
   if (st != WISE_OK) return st;
   st = wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                            workspace_bytes, stream);
   if (st != WISE_OK) return st;
-  return wise_decode_finish(shape, modes, seq_lens, workspace, workspace_bytes, support, out, lse,
-                            stream);
+  return wise_decode_finish_m(shape, modes, seq_lens, workspace, workspace_bytes, 0u, mask, out,
+                              lse, stream);
+}
+
+wise_status wise_decode(const wise_shape* shape, const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* page_table, const int32_t* seq_lens,
+                        const int8_t* modes, uint32_t* support, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
+  const wise_mask m{support, nullptr, 0, 0};
+  return wise_decode_m(shape, q, k_cache, v_cache, page_table, seq_lens, modes, &m, out, lse,
+                       workspace, workspace_bytes, stream);
 }
 
 wise_status wise_support_union(uint32_t* dst, const uint32_t* src, int64_t n_words,
@@ -458,18 +531,27 @@ wise_status wise_support_head_union(const wise_shape* shape, uint32_t* support,
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "head union launch");
 }
 
-wise_status wise_validate(const wise_shape* shape, const int32_t* page_table,
-                          const int32_t* seq_lens, const int8_t* modes, const uint32_t* support,
-                          int32_t* err_word, wise_stream_t stream) {
+wise_status wise_validate_m(const wise_shape* shape, const int32_t* page_table,
+                            const int32_t* seq_lens, const int8_t* modes, const wise_mask* mask,
+                            int32_t* err_word, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   if (!err_word) return fail(WISE_ERR_INVALID_ARG, "err_word is NULL");
+  MaskView mv;
+  if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
   if (shape->num_rows == 0) return WISE_OK;
   if (!page_table || !seq_lens || !modes)
     return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
-  cudaError_t e = launch_validate(make_params(shape), page_table, seq_lens, modes, support,
-                                  err_word, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_validate(make_params(shape), page_table, seq_lens, modes, mv, err_word,
+                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "validate launch");
+}
+
+wise_status wise_validate(const wise_shape* shape, const int32_t* page_table,
+                          const int32_t* seq_lens, const int8_t* modes, const uint32_t* support,
+                          int32_t* err_word, wise_stream_t stream) {
+  const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
+  return wise_validate_m(shape, page_table, seq_lens, modes, &m, err_word, stream);
 }
 
 }  // extern "C"

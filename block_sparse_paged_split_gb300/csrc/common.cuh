@@ -13,6 +13,7 @@
 namespace wise {
 
 constexpr int kTile = 32;             // block / tile size B in tokens
+constexpr int kMaxT = 16;             // largest tiles_per_item
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -29,6 +30,9 @@ struct KParams {
   float scale_log2;  // softmax scale * log2(e): scores are kept in log2 units
   float eta;
   int early;         // partial pass: start before the previous kernel has completed
+  int list1;         // partial and finish: the work list is list 1 (built by an
+                     // earlier finish), every row sparse
+  int build;         // finish: also build list 1 from the mask this call leaves
 };
 
 // Device view of the caller's workspace (offsets from wise_workspace_layout).
@@ -47,11 +51,41 @@ struct WsView {
   int32_t* tickets;    // [R*Hkv]: items of the pair completed in the running partial
                        // pass (zeroed by compaction and by the pair's finisher)
   int32_t max_items;
+  // List 1: the work list of a following all-sparse call, written by a finish
+  // (its items bucketed by tile count, bucket n-1 at items_1 + (n-1) * max_items).
+  int32_t* l1_counter;  // [kMaxT]: items of list 1 with n tiles at [n-1]
+  int4* head_info_1;    // [R*Hkv]: as head_info, for list 1
+  int4* items_1;        // [kMaxT * max_items]
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
-// Work item record, fourth field: row length (bits 0-23) and mode flags.
+// Where each row's support mask lives [WISE PR, "What changes", wise.py
+// bullet: per-request slots hold a [slot, layer, head, block] bitmask]: the W
+// words of (row r, KV head g) are at words + slot(r) * slot_stride + g * W,
+// with slot(r) = row_slot[r], or r itself when row_slot is null.  A row whose
+// slot is negative (or >= num_slots when num_slots > 0) has no mask.
+struct MaskView {
+  uint32_t* words;          // slot 0's mask at the call's layer; null: no mask at all
+  const int32_t* row_slot;  // [R] or null
+  long long slot_stride;    // words from one slot's mask to the next
+  int num_slots;            // 0: not checked
+};
+
+__device__ __forceinline__ int mask_slot(const MaskView& m, int r) {
+  if (!m.words) return -1;
+  if (!m.row_slot) return r;
+  const int s = m.row_slot[r];
+  return (s < 0 || (m.num_slots > 0 && s >= m.num_slots)) ? -1 : s;
+}
+
+__device__ __forceinline__ uint32_t* mask_of(const MaskView& m, int slot, int g, int W) {
+  return slot < 0 ? nullptr : m.words + (long long)slot * m.slot_stride + (long long)g * W;
+}
+
+// Work item record: x = row * Hkv + KV head, y = block range s | partial slot
+// k << 16 (the item writes its split to slot rg * S_max + k), z = tile bitmap
+// over the range | tile count << 16, w = row length (bits 0-23) | mode flags.
 constexpr int kItemSparse = 1 << 24;
 constexpr int kItemDiscover = 1 << 25;
 constexpr int kItemLenMask = (1 << 24) - 1;

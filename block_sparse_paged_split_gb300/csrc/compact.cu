@@ -16,7 +16,6 @@ namespace wise {
 
 constexpr int kCompactThreads = 1024;
 constexpr int kCompactCluster = 8;  // CTAs of the one cluster the kernel runs as
-constexpr int kMaxT = 16;           // largest tiles_per_item
 
 // Work items are block ranges: item (rg, s) holds the tiles of (row, KV head)
 // rg that lie in blocks [s*T, s*T + T) -- all of them for dense and discover
@@ -26,8 +25,9 @@ constexpr int kMaxT = 16;           // largest tiles_per_item
 // Item (rg, s) writes its partial output to slot rg * S_max + s.
 //
 // An item record carries its compacted tiles as a bitmap over its range:
-// x = rg, y = s, z = tile bitmap (bit i: block s*T + i) | tile count << 16,
-// w = row length | sparse << 24 | discover << 25.  The partial pass walks the
+// x = rg, y = s | s << 16 (range, and the partial slot it writes), z = tile
+// bitmap (bit i: block s*T + i) | tile count << 16, w = row length | sparse
+// << 24 | discover << 25.  The partial pass walks the
 // set bits in order (the k-th tile is the k-th set bit), so its inner loop
 // has no branch and needs no list in memory.
 //
@@ -60,39 +60,38 @@ struct UnitInfo {
 // dependency wait; the mask word may come from the previous call's finish
 // pass and is read after it.
 struct UnitLoad {
-  int mode, raw;
+  int mode, raw, slot;
   uint32_t word;
 };
 
 __device__ __forceinline__ void unit_load_inputs(UnitLoad& l, int u, int nunits,
                                                  const int8_t* __restrict__ modes,
                                                  const int32_t* __restrict__ seq_lens,
-                                                 const KParams& kp) {
-  l = UnitLoad{-1, 0, 0u};
+                                                 const MaskView& mv, const KParams& kp) {
+  l = UnitLoad{-1, 0, -1, 0u};
   if (u < nunits) {
     const int r = u / kp.S_max / kp.Hkv;
     l.mode = modes[r];
     l.raw = seq_lens[r];
+    l.slot = mask_slot(mv, r);
   }
 }
 
 __device__ __forceinline__ void unit_load_mask(UnitLoad& l, int u, int nunits,
-                                               const uint32_t* __restrict__ support,
-                                               const KParams& kp) {
-  if (u < nunits && support) {
+                                               const MaskView& mv, const KParams& kp) {
+  if (u < nunits && l.slot >= 0) {
     const int pair = u / kp.S_max, s = u - pair * kp.S_max;
     // s * T < max_blocks <= 32 W: the word is inside the pair's mask.
-    l.word = support[(size_t)pair * kp.W + ((s * kp.T) >> 5)];
+    l.word = mask_of(mv, l.slot, pair % kp.Hkv, kp.W)[(s * kp.T) >> 5];
   }
 }
 
 __device__ __forceinline__ UnitLoad unit_load(int u, int nunits, const int8_t* __restrict__ modes,
                                               const int32_t* __restrict__ seq_lens,
-                                              const uint32_t* __restrict__ support,
-                                              const KParams& kp) {
+                                              const MaskView& mv, const KParams& kp) {
   UnitLoad l;
-  unit_load_inputs(l, u, nunits, modes, seq_lens, kp);
-  unit_load_mask(l, u, nunits, support, kp);
+  unit_load_inputs(l, u, nunits, modes, seq_lens, mv, kp);
+  unit_load_mask(l, u, nunits, mv, kp);
   return l;
 }
 
@@ -118,7 +117,7 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const UnitLoad& l, const KP
 
 __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompactThreads)
     compact_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                   const uint32_t* __restrict__ support, const WsView ws, const KParams kp) {
+                   const MaskView mv, const WsView ws, const KParams kp) {
   __shared__ int hist[kMaxT + 1];                     // this CTA's items of each size
   __shared__ int next[kMaxT + 1];                     // its next schedule slot of each size
   const int lane = threadIdx.x & 31;
@@ -135,30 +134,31 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
   UnitLoad ld[kCached];
 #pragma unroll
   for (int c = 0; c < kCached; ++c) {
-    ld[c] = UnitLoad{-1, 0, 0u};
-    if (c < rounds) unit_load_inputs(ld[c], c * nthreads + gt, nunits, modes, seq_lens, kp);
+    ld[c] = UnitLoad{-1, 0, -1, 0u};
+    if (c < rounds) unit_load_inputs(ld[c], c * nthreads + gt, nunits, modes, seq_lens, mv, kp);
   }
   grid_dependency_wait();    // the previous call's mask
   grid_dependents_launch();  // the partial pass may start its prologue now
 #pragma unroll
   for (int c = 0; c < kCached; ++c)
-    if (c < rounds) unit_load_mask(ld[c], c * nthreads + gt, nunits, support, kp);
+    if (c < rounds) unit_load_mask(ld[c], c * nthreads + gt, nunits, mv, kp);
   if (gt == 0) {
     *ws.status = 0;
     *ws.queue = 0;
     *ws.queue_done = 0;
   }
+  if (gt < kMaxT) ws.l1_counter[gt] = 0;  // a finish building list 1 appends from 0
   if (threadIdx.x <= kMaxT) hist[threadIdx.x] = 0;
   __syncthreads();
   auto unit = [&](int i, int u) {
     if (i < kCached) {
-      UnitLoad l{-1, 0, 0u};
+      UnitLoad l{-1, 0, -1, 0u};
 #pragma unroll
       for (int c = 0; c < kCached; ++c)
         if (c == i) l = ld[c];
       return unit_info(u, l, kp);
     }
-    return unit_info(u, unit_load(u, nunits, modes, seq_lens, support, kp), kp);
+    return unit_info(u, unit_load(u, nunits, modes, seq_lens, mv, kp), kp);
   };
 
   // Phase A: this CTA's histogram of item sizes; head info from each pair's
@@ -221,7 +221,7 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
     slot = __shfl_sync(kFull, slot, leader);
     if (n > 0) {
       ws.items[slot + __popc(same & ((1u << lane) - 1u))] =
-          make_int4(pair, s, (int)(ui.bits | ((uint32_t)n << 16)), ui.L | ui.flags);
+          make_int4(pair, s | (s << 16), (int)(ui.bits | ((uint32_t)n << 16)), ui.L | ui.flags);
       if (ui.sparse) {
         atomicAdd(&ws.head_info[pair].z, n);
         atomicAdd(&ws.head_info[pair].w, 1);
@@ -241,9 +241,9 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
 }
 
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const WsView& ws, cudaStream_t stream) {
+                           const MaskView& mv, const WsView& ws, cudaStream_t stream) {
   return launch_pdl(compact_kernel, dim3(kCompactCluster), dim3(kCompactThreads), 0, stream, modes,
-                    seq_lens, support, ws, kp);
+                    seq_lens, mv, ws, kp);
 }
 
 // ------------------------------------------------------------------ union
@@ -309,15 +309,18 @@ cudaError_t launch_head_union(const KParams& kp, uint32_t* support, cudaStream_t
 // --------------------------------------------------------------- validate
 __global__ void validate_kernel(const int32_t* __restrict__ page_table,
                                 const int32_t* __restrict__ seq_lens,
-                                const int8_t* __restrict__ modes,
-                                const uint32_t* __restrict__ support, int32_t* err,
-                                const KParams kp) {
+                                const int8_t* __restrict__ modes, const MaskView mv,
+                                int32_t* err, const KParams kp) {
   const int r = blockIdx.x;
   const int raw = seq_lens[r];
   const int mode = modes[r];
   if (threadIdx.x == 0) {
     if (mode < 0 || mode > 3) atomicOr(err, WISE_BAD_MODE);
     if (raw < 0 || raw > kp.cap_tokens) atomicOr(err, WISE_BAD_SEQ_LEN);
+    if (mv.row_slot) {
+      const int sl = mv.row_slot[r];
+      if (sl < -1 || (mv.num_slots > 0 && sl >= mv.num_slots)) atomicOr(err, WISE_BAD_SLOT);
+    }
   }
   const int L = clamp_len(raw, kp.cap_tokens);
   const int npg = (L + kp.P - 1) / kp.P;
@@ -328,10 +331,11 @@ __global__ void validate_kernel(const int32_t* __restrict__ page_table,
   }
   if (mode == WISE_MODE_SPARSE && L > 0) {
     const int nb = (L + kTile - 1) / kTile;
+    const int slot = mask_slot(mv, r);
     for (int g = threadIdx.x; g < kp.Hkv; g += blockDim.x) {
       bool any = false;
-      if (support != nullptr) {
-        const uint32_t* words = support + ((size_t)r * kp.Hkv + g) * kp.W;
+      if (slot >= 0) {
+        const uint32_t* words = mask_of(mv, slot, g, kp.W);
         for (int w = 0; w * 32 < nb; ++w) {
           const int lo = w * 32;
           any |= (words[w] & (lo + 32 <= nb ? 0xffffffffu : (1u << (nb - lo)) - 1u)) != 0;
@@ -343,10 +347,10 @@ __global__ void validate_kernel(const int32_t* __restrict__ page_table,
 }
 
 cudaError_t launch_validate(const KParams& kp, const int32_t* page_table,
-                            const int32_t* seq_lens, const int8_t* modes,
-                            const uint32_t* support, int32_t* err_word, cudaStream_t stream) {
+                            const int32_t* seq_lens, const int8_t* modes, const MaskView& mv,
+                            int32_t* err_word, cudaStream_t stream) {
   if (kp.R == 0) return cudaSuccess;
-  validate_kernel<<<kp.R, 128, 0, stream>>>(page_table, seq_lens, modes, support, err_word, kp);
+  validate_kernel<<<kp.R, 128, 0, stream>>>(page_table, seq_lens, modes, mv, err_word, kp);
   return cudaGetLastError();
 }
 

@@ -23,6 +23,7 @@
 //            the row's block count cleared.
 #include "finish_short.cuh"
 #include "internal.h"
+#include "list1.cuh"
 
 namespace wise {
 
@@ -169,14 +170,16 @@ __device__ __forceinline__ void group_select(const float2 (&st)[E], int nb, floa
 // W = 4 warps a head for up to 512 keys, 8 beyond (same-box A/B: 4 warps
 // made the 4K finish 18.7 -> 12.6 us, 8 warps stay best at 1024 keys).
 
-template <typename T, int E, int W>
+template <typename T, int E, int W, bool kBuild>
 __global__ void __launch_bounds__(W * 32)
     finish_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                  const WsView ws, const KParams kp, uint32_t* __restrict__ support,
+                  const WsView ws, const KParams kp, const MaskView mv,
                   T* __restrict__ out, float* __restrict__ lse) {
   constexpr int wph = W;
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ uint32_t smask[32];
+  __shared__ uint32_t fwords[32];  // the mask the call leaves (list 1 is built from it)
+  __shared__ List1Smem l1sm;
   const int G = kp.G, D = kp.D;
   const int gs = wph * 32;
   const int th = threadIdx.x;
@@ -191,22 +194,25 @@ __global__ void __launch_bounds__(W * 32)
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int h = g * G + hgrp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
-  const int mode = modes[r];
+  const int mode = kp.list1 ? (int)WISE_MODE_SPARSE : (int)modes[r];
   const int nb = (L + kTile - 1) / kTile;
-  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
+  uint32_t* const mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // the pair's mask, or null
+  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
   const int dpl = D >> 5;  // 2 or 4 dims per lane
   T* orow = out + ((size_t)r * kp.Hq + h) * D + lane * dpl;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 
-  // Read before the dependency wait: the caller's inputs, the old mask word
-  // (its last writer finished before the partial pass began) and the head
-  // info (written by compaction, likewise complete).
-  const uint32_t old_word = (disc && mode == WISE_MODE_DISCOVER_UNION && hgrp == 0 && th < kp.W)
-                                ? support[(size_t)rg * kp.W + th]
-                                : 0u;
-  const int4 hi = ws.head_info[rg];
+  // Read before the dependency wait: the caller's inputs and the head info
+  // (written by compaction or by the finish that built list 1, both complete
+  // before the partial pass began).
+  const int4 hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
+  // The mask words the call starts from (the group's first CTA): union-discover
+  // rows OR into them, and a list build takes them as they are for rows this
+  // call does not select.
+  const bool need_old = (disc && mode == WISE_MODE_DISCOVER_UNION) || (kBuild && !disc);
+  const uint32_t old_word = (need_old && mw && hgrp == 0 && th < kp.W) ? mw[th] : 0u;
   float2 st[E];
   const float2* ts = ws.tile_stats + (size_t)(r * kp.Hq + h) * kp.max_blocks;
 #pragma unroll
@@ -215,20 +221,23 @@ __global__ void __launch_bounds__(W * 32)
     st[e] = disc && i < nb ? ts[i] : make_float2(0.f, 0.f);
   }
   // Padding rows and sparse rows selecting nothing: the whole cluster (one
-  // row and KV head) leaves here, before any cluster barrier.
+  // row and KV head) leaves here, before any cluster barrier.  Their masks
+  // select nothing, so a list build gives them no item.
   if (L == 0 || hi.z == 0) {
     if (wsub == 0) {
       if (dpl == 4) Elem<T>::template store_global<4>(orow, o);
       else Elem<T>::template store_global<2>(orow, reinterpret_cast<const float(&)[2]>(o));
       if (lane == 0) lse[(size_t)r * kp.Hq + h] = -INFINITY;
     }
+    if (kBuild && hgrp == 0 && th == 0) list1_empty_pair(ws, kp, rg);
     return;
   }
 
-  // ---- merge the block ranges' partial results
-  const float2* ml = ws.partial_ml + (size_t)hi.x * G + hgrp;  // slot s at ml[s * G]
-  const float* acc = ws.partial_acc + ((size_t)hi.x * G + hgrp) * D + lane * dpl;
-  const int n = hi.y;
+  // ---- merge the pair's split slots (hi.y of them from hi.x)
+  const size_t slot0 = (size_t)rg * kp.S_max;  // = hi.x
+  const float2* ml = ws.partial_ml + slot0 * G + hgrp;  // slot s at ml[s * G]
+  const float* acc = ws.partial_acc + (slot0 * G + hgrp) * D + lane * dpl;
+  const int n = min(max(hi.y, 0), kp.S_max);
   float m_w = -INFINITY, lam = 0.f;
   for (int s0 = wsub; s0 < n; s0 += 4 * wph) {
     float2 t[4];
@@ -302,7 +311,14 @@ __global__ void __launch_bounds__(W * 32)
     if (lane == 0) lse[(size_t)r * kp.Hq + h] = lse2 * kLn2;
   }
 
-  if (!disc) return;  // the whole cluster
+  if (!disc) {  // the whole cluster
+    if (kBuild && hgrp == 0) {
+      if (th < kp.W) fwords[th] = old_word;
+      __syncthreads();
+      list1_build_pair(ws, kp, rg, L, fwords, l1sm);
+    }
+    return;
+  }
 
   // ---- eta selection for this query head, then the group's OR
   if (th < 32) smask[th] = 0u;
@@ -318,47 +334,56 @@ __global__ void __launch_bounds__(W * 32)
     for (int c = 0; c < G; ++c) w |= (uint32_t)load_peer(reinterpret_cast<const int*>(&smask[th]), c);
     w &= valid;
     if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
-    support[(size_t)rg * kp.W + th] = w;
+    mw[th] = w;
+    fwords[th] = w;
   }
   cluster_arrive();  // no CTA leaves while the group's first CTA may still read it
   cluster_wait();
+  if (kBuild && hgrp == 0) list1_build_pair(ws, kp, rg, L, fwords, l1sm);
 }
 
 // ------------------------------------------------------------------ short rows
 // Rows of at most 64 blocks and 8 split slots: one warp per query head, the
 // merge in each lane over all slots, the sort in registers with shuffles
 // (finish_short.cuh); the group's selections are ORed in shared memory.
-template <typename T>
+template <typename T, bool kBuild>
 __global__ void __launch_bounds__(256)
     finish_short_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
-                        const WsView ws, const KParams kp, uint32_t* __restrict__ support,
+                        const WsView ws, const KParams kp, const MaskView mv,
                         T* __restrict__ out, float* __restrict__ lse) {
   __shared__ uint32_t smask[2];
+  __shared__ uint32_t fwords[2];  // the mask the call leaves (list 1 is built from it)
+  __shared__ List1Smem l1sm;
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h = g * kp.G + warp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
-  const int mode = modes[r];
+  const int mode = kp.list1 ? (int)WISE_MODE_SPARSE : (int)modes[r];
   const int nb = (L + kTile - 1) / kTile;
-  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
-  // Read before the dependency wait: the old mask word (its last writer
-  // finished before the partial pass began) and compaction's head info.
-  const uint32_t old_word =
-      (disc && mode == WISE_MODE_DISCOVER_UNION && (int)threadIdx.x < kp.W) ? support[(size_t)rg * kp.W + threadIdx.x] : 0u;
-  const int4 hi = ws.head_info[rg];
+  uint32_t* const mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // the pair's mask, or null
+  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
+  // Read before the dependency wait: the head info (written by compaction or
+  // by the finish that built list 1, both complete before the partial pass
+  // began).
+  const int4 hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
   if (threadIdx.x < 2) smask[threadIdx.x] = 0u;
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
+  // The mask words the call starts from: union-discover rows OR into them, and
+  // a list build takes them as they are for the rows this call does not select.
+  const bool need_old = (disc && mode == WISE_MODE_DISCOVER_UNION) || (kBuild && !disc);
+  const uint32_t old_word = (need_old && mw && (int)threadIdx.x < kp.W) ? mw[threadIdx.x] : 0u;
   float2 st[2];
   if (disc) short_load_stats<false>(ws, kp, r, h, nb, lane, st);
-  const int nslots = (L == 0 || hi.z == 0) ? 0 : (nb + kp.T - 1) / kp.T;
+  // Slot count from the head info, within the pair's S_max slots.
+  const int nslots = hi.z == 0 ? 0 : min(max(hi.y, 0), kp.S_max);
   const float lse2 = short_merge_head<T, false>(ws, kp, rg, warp, nslots,
                                                 out + ((size_t)r * kp.Hq + h) * kp.D,
                                                 lse + (size_t)r * kp.Hq + h, lane);
-  if (!disc || L == 0) return;  // a padding row's mask is left as it is
+  if (!kBuild && (!disc || L == 0)) return;  // a padding row's mask is left as it is
   __syncthreads();
-  if (lse2 > -INFINITY) {
+  if (disc && L > 0 && lse2 > -INFINITY) {
     const uint2 w = nb > 32 ? warp_select_words<2>(st, nb, lse2, kp.eta, lane)
                             : warp_select_words<1>(st, nb, lse2, kp.eta, lane);
     if (lane == 0) {
@@ -369,12 +394,19 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if ((int)threadIdx.x < kp.W) {
     const int tw = threadIdx.x;
-    const int lo = tw * 32;
-    const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
-    uint32_t w = smask[tw] & valid;
-    if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
-    support[(size_t)rg * kp.W + tw] = w;
+    uint32_t w = old_word;
+    if (disc && L > 0) {
+      const int lo = tw * 32;
+      const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
+      w = smask[tw] & valid;
+      if (mode == WISE_MODE_DISCOVER_UNION) w |= old_word & valid;
+      mw[tw] = w;
+    }
+    fwords[tw] = w;
   }
+  if (!kBuild) return;
+  __syncthreads();
+  list1_build_pair(ws, kp, rg, L, fwords, l1sm);
 }
 
 // Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
@@ -388,9 +420,9 @@ static int finish_npad(const KParams& kp) {
   return n;
 }
 
-template <typename T, int E, int W>
+template <typename T, int E, int W, bool kBuild>
 static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                               const WsView& ws, uint32_t* support, void* out, float* lse,
+                               const WsView& ws, const MaskView& mv, void* out, float* lse,
                                cudaStream_t stream) {
   const size_t smem = (size_t)32 * E * W * 8 + (size_t)W * (kp.D + 2) * 4;
   cudaLaunchConfig_t cfg = {};
@@ -407,40 +439,52 @@ static cudaError_t launch_long(const KParams& kp, const int8_t* modes, const int
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, finish_kernel<T, E, W>, modes, seq_lens, ws, kp, support,
+  return cudaLaunchKernelEx(&cfg, finish_kernel<T, E, W, kBuild>, modes, seq_lens, ws, kp, mv,
                             static_cast<T*>(out), lse);
 }
 
-template <typename T>
-static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
-                                   const int32_t* seq_lens, const WsView& ws, uint32_t* support,
+// The list build (WISE_FLAG_BUILD_SPARSE_LIST) is a separate instantiation,
+// so the other calls run kernels without its code (with it inlined, the
+// compiler gave the short finish 61 instead of 76 registers and issued its
+// split loads in two rounds: 1.5 us slower per launch, ncu launch list).
+template <typename T, bool kBuild>
+static cudaError_t launch_finish_b(const KParams& kp, const int8_t* modes,
+                                   const int32_t* seq_lens, const WsView& ws, const MaskView& mv,
                                    void* out, float* lse, cudaStream_t stream) {
   if (can_fold_finish(kp))
-    return launch_pdl(finish_short_kernel<T>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0, stream,
-                      modes, seq_lens, ws, kp, support, static_cast<T*>(out), lse);
+    return launch_pdl(finish_short_kernel<T, kBuild>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0,
+                      stream, modes, seq_lens, ws, kp, mv, static_cast<T*>(out), lse);
   const int w = finish_warps(kp);
   const int e = finish_npad(kp) / (32 * w);
   if (w == 4) {
     switch (e) {  // npad <= 512: e <= 4
-      case 1: return launch_long<T, 1, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
-      case 2: return launch_long<T, 2, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
-      default: return launch_long<T, 4, 4>(kp, modes, seq_lens, ws, support, out, lse, stream);
+      case 1: return launch_long<T, 1, 4, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+      case 2: return launch_long<T, 2, 4, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+      default: return launch_long<T, 4, 4, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
     }
   }
   switch (e) {  // npad = 1024 with 8 warps: e = 4
-    case 1: return launch_long<T, 1, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
-    case 2: return launch_long<T, 2, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
-    default: return launch_long<T, 4, 8>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    case 1: return launch_long<T, 1, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+    case 2: return launch_long<T, 2, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+    default: return launch_long<T, 4, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
   }
 }
 
+template <typename T>
+static cudaError_t launch_finish_t(const KParams& kp, const int8_t* modes,
+                                   const int32_t* seq_lens, const WsView& ws, const MaskView& mv,
+                                   void* out, float* lse, cudaStream_t stream) {
+  return kp.build ? launch_finish_b<T, true>(kp, modes, seq_lens, ws, mv, out, lse, stream)
+                  : launch_finish_b<T, false>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+}
+
 cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,
-                          const int32_t* seq_lens, const WsView& ws, uint32_t* support,
+                          const int32_t* seq_lens, const WsView& ws, const MaskView& mv,
                           void* out, float* lse, cudaStream_t stream) {
   if (kp.R == 0) return cudaSuccess;
   if (dtype == WISE_DTYPE_BF16)
-    return launch_finish_t<__nv_bfloat16>(kp, modes, seq_lens, ws, support, out, lse, stream);
-  return launch_finish_t<float>(kp, modes, seq_lens, ws, support, out, lse, stream);
+    return launch_finish_t<__nv_bfloat16>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+  return launch_finish_t<float>(kp, modes, seq_lens, ws, mv, out, lse, stream);
 }
 
 }  // namespace wise

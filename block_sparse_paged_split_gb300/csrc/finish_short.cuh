@@ -208,8 +208,10 @@ __device__ __forceinline__ void short_finish_pair_warp(const WsView& ws, const K
                                                        float* lse, int lane) {
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int nb = (L + kTile - 1) / kTile;
-  const int nslots = (nb + kp.T - 1) / kp.T;
-  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && support != nullptr;
+  uint32_t* const mw = support ? support + (size_t)rg * kp.W : nullptr;
+  // Written by compaction, before this launch; within the pair's slots.
+  const int nslots = min(max(ws.head_info[rg].y, 0), min(kp.S_max, kShortSlots));
+  const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
   uint32_t w0 = 0u, w1 = 0u;
   for (int hl = 0; hl < kp.G; ++hl) {
     const int h = g * kp.G + hl;
@@ -228,7 +230,7 @@ __device__ __forceinline__ void short_finish_pair_warp(const WsView& ws, const K
   if (disc && lane < kp.W) {
     const int lo = lane * 32;
     const uint32_t valid = lo + 32 <= nb ? 0xffffffffu : (lo < nb ? (1u << (nb - lo)) - 1u : 0u);
-    uint32_t* word = support + (size_t)rg * kp.W + lane;
+    uint32_t* word = mw + lane;
     uint32_t w = (lane == 0 ? w0 : w1) & valid;
     if (mode == WISE_MODE_DISCOVER_UNION) w |= ld_ws<true>(word) & valid;
     *word = w;

@@ -10,12 +10,12 @@ namespace wise {
 // Launchers (host).  Each enqueues one kernel on `stream` and returns the
 // launch status; none allocates or synchronises.
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
-                           const uint32_t* support, const WsView& ws, cudaStream_t stream);
+                           const MaskView& mv, const WsView& ws, cudaStream_t stream);
 
 // Where the finish pass writes when it is folded into the partial pass
 // (out == nullptr: not folded).
 struct FoldArgs {
-  uint32_t* support;
+  uint32_t* support;  // [R, Hkv, W] (the folded finish takes flat masks only)
   void* out;
   float* lse;
 };
@@ -33,7 +33,7 @@ cudaError_t launch_partial_f32(const KParams& kp, const CUtensorMap& tmK, const 
                                cudaStream_t stream);
 
 cudaError_t launch_finish(int dtype, const KParams& kp, const int8_t* modes,
-                          const int32_t* seq_lens, const WsView& ws, uint32_t* support,
+                          const int32_t* seq_lens, const WsView& ws, const MaskView& mv,
                           void* out, float* lse, cudaStream_t stream);
 
 cudaError_t launch_union(uint32_t* dst, const uint32_t* src, int64_t n_words,
@@ -47,8 +47,8 @@ cudaError_t launch_block_mass(int dtype, const KParams& kp, const void* q, const
                               cudaStream_t stream);
 
 cudaError_t launch_validate(const KParams& kp, const int32_t* page_table,
-                            const int32_t* seq_lens, const int8_t* modes,
-                            const uint32_t* support, int32_t* err_word, cudaStream_t stream);
+                            const int32_t* seq_lens, const int8_t* modes, const MaskView& mv,
+                            int32_t* err_word, cudaStream_t stream);
 
 // Launches `kern` as a programmatic dependent of the previous kernel in the
 // stream: its CTAs may start while that kernel finishes, and every kernel of

@@ -524,10 +524,61 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     // the number of consumers in the grid.
     const int n_consumers = gridDim.x * C;
     // The item count and the first item's record are loaded together (the
-    // record's slot is inside the item array whatever the count).
+    // record's slot is inside the item array whatever the count).  List 1
+    // keeps its items in one bucket per tile count (larger counts first in
+    // the schedule): the buckets' schedule positions come first, then the
+    // record.
     const int first_slot = blockIdx.x * C + c;
-    const int4 first_rec = first_slot < ws.max_items ? ws.items[first_slot] : make_int4(0, 0, 0, 0);
-    const int n_items = *ws.num_items;
+    int l1s[kMaxT];  // list 1: schedule position of the first item with j + 1 tiles
+    auto record_at = [&](int slot) -> int4 {
+      if (!kp.list1) return ws.items[slot];
+      // Bucket j holds schedule positions [l1s[j], l1s[j - 1]) (l1s is
+      // non-increasing in j and l1s[T - 1] = 0): the smallest j with
+      // l1s[j] <= slot.
+      int jsel = kp.T - 1, base = 0;
+#pragma unroll
+      for (int j = kMaxT - 1; j >= 0; --j)
+        if (j < kp.T && l1s[j] <= slot) {
+          jsel = j;
+          base = l1s[j];
+        }
+      const int idx = slot - base;
+      if (idx < 0 || idx >= ws.max_items) return make_int4(-1, 0, 0, 0);  // rejected below
+      return ws.items_1[(size_t)jsel * ws.max_items + idx];
+    };
+    // A record the library did not write for this shape (a call out of
+    // order on the workspace) is flagged and skipped, never followed.
+    auto record_ok = [&](const int4& rec) {
+      const unsigned bits = (unsigned)rec.z & 0xffffu;
+      const int cnt = (rec.z >> 16) & 0xff;
+      const int s_rng = rec.y & 0xffff, slot = (int)((unsigned)rec.y >> 16);
+      const int L = rec.w & kItemLenMask;
+      const bool ok = rec.x >= 0 && rec.x < kp.R * kp.Hkv && s_rng < kp.S_max && slot < kp.S_max &&
+                      cnt >= 1 && cnt <= kp.T && __popc(bits) == cnt && (bits >> kp.T) == 0u &&
+                      L <= kp.cap_tokens &&
+                      (s_rng * kp.T + 31 - __clz(bits | 1u)) * kTile < L;
+      if (!ok) flag_error(ws.status, WISE_DEVERR_BAD_WORK_LIST);
+      return ok;
+    };
+    int n_items;
+    int4 first_rec = make_int4(0, 0, 0, 0);
+    if (kp.list1) {
+      // Schedule position of each bucket: the items of larger buckets first.
+      int cnt[kMaxT];
+#pragma unroll
+      for (int j = 0; j < kMaxT; ++j) cnt[j] = j < kp.T ? ws.l1_counter[j] : 0;
+      int pos = 0;
+#pragma unroll
+      for (int j = kMaxT - 1; j >= 0; --j) {
+        l1s[j] = pos;
+        pos += min(max(cnt[j], 0), ws.max_items);
+      }
+      n_items = pos;
+      if (first_slot < n_items) first_rec = record_at(first_slot);
+    } else {
+      first_rec = first_slot < ws.max_items ? ws.items[first_slot] : make_int4(0, 0, 0, 0);
+      n_items = min(*ws.num_items, ws.max_items);
+    }
     bool timed_out = false;
     while (true) {
       if (!cur_ok && nxt_ok) {
@@ -543,8 +594,8 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       if (!nxt_ok && !exhausted && (!cur_ok || ((cur.z >> 16) & 0xff) - k <= 1)) {
         const int slot = first_claim ? first_slot : n_consumers + atomicAdd(ws.queue, 1);
         if (slot < n_items) {
-          nxt = first_claim ? first_rec : ws.items[slot];
-          nxt_ok = true;
+          nxt = first_claim ? first_rec : record_at(slot);
+          nxt_ok = record_ok(nxt);
         } else {
           exhausted = true;
         }
@@ -558,7 +609,8 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         const int ntiles = (cur.z >> 16) & 0xff;
         const int L = cur.w & kItemLenMask;
         const int row = rg / kp.Hkv;
-        const int b = cur.y * kp.T + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 1);
+        const int range0 = (cur.y & 0xffff) * kp.T;
+        const int b = range0 + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 1);
         // A tile's page ids are loaded one tile ahead (with the previous
         // tile's), so two tiles' copies go out back to back at an item's start.
         auto load_pages = [&](int blk, int (&pg)[2]) {
@@ -574,7 +626,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
           load_pages(b, p.pages);
         }
         ahead_ok = k + 1 < ntiles;
-        if (ahead_ok) load_pages(cur.y * kp.T + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 2), ahead);
+        if (ahead_ok) load_pages(range0 + (int)__fns((unsigned)cur.z & 0xffffu, 0, k + 2), ahead);
         const int tok0 = b * kTile;
         const int rem = L - tok0;
         const int pages_in_tile = kTile / kp.P;
@@ -582,7 +634,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         p.npg = npg < pages_in_tile ? npg : pages_in_tile;
         p.row = row;
         p.head = rg - row * kp.Hkv;
-        p.d.item = rg * kp.S_max + cur.y;
+        p.d.item = rg * kp.S_max + (cur.y >> 16);
         p.d.tile = b;
         p.d.info = (rem < kTile ? rem : kTile) | (k == 0 ? 256 : 0) | (k + 1 == ntiles ? 512 : 0) |
                    ((cur.w & kItemDiscover) ? 1024 : 0);
@@ -597,6 +649,11 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       if (!mbar_wait(empty_bar(c, stage), ((seq / S) & 1) ^ 1)) {
         flag_error(ws.status, WISE_DEVERR_WAIT_TIMEOUT);
         timed_out = true;
+        // Copies already issued into the ring may still be landing: wait
+        // (bounded) for the last phase of every stage issued before leaving,
+        // so the CTA never exits with a bulk copy writing its shared memory.
+        for (uint32_t i = seq > (uint32_t)S ? seq - S : 0u; i < seq; ++i)
+          mbar_wait(full_bar(c, i % S), (i / S) & 1);
         break;
       }
       StageDesc* d = descs(c) + stage;
@@ -649,6 +706,10 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         __threadfence();
         atomicExch(ws.queue, 0);
         atomicExch(ws.queue_done, 0);
+        // A finish of this call may build list 1: its counters start at 0.
+        // (A pass on list 1 leaves them: the next call may reuse the list.)
+        if (!kp.list1)
+          for (int j = 0; j < kMaxT; ++j) ws.l1_counter[j] = 0;
       }
     }
     return;

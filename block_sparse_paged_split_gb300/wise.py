@@ -27,11 +27,13 @@ DTYPE_F32 = 1
 
 DEVERR_SEQ_LEN_CLAMPED = 1
 DEVERR_WAIT_TIMEOUT = 2
+DEVERR_BAD_WORK_LIST = 4
 
 BAD_MODE = 1
 BAD_SEQ_LEN = 2
 BAD_PAGE = 4
 EMPTY_SPARSE_SUPPORT = 8
+BAD_SLOT = 16
 
 _STATUS = {0: "WISE_OK", 1: "WISE_ERR_INVALID_ARG", 2: "WISE_ERR_UNSUPPORTED",
            3: "WISE_ERR_WORKSPACE", 4: "WISE_ERR_CUDA"}
@@ -52,11 +54,39 @@ class wise_shape(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eta", ctypes.c_float)]
 
 
+class wise_mask(ctypes.Structure):
+    """Where the rows' masks live (see include/wise.h): the words of (row r,
+    KV head g) are at words + slot(r) * slot_stride + g * W."""
+    _fields_ = [("words", ctypes.c_void_p), ("row_slot", ctypes.c_void_p),
+                ("slot_stride", ctypes.c_int64), ("num_slots", ctypes.c_int32)]
+
+
+def make_mask(pool: Optional[torch.Tensor], row_slot: Optional[torch.Tensor] = None,
+              layer: int = 0) -> wise_mask:
+    """A mask descriptor over `pool`: an int32 CUDA tensor [num_rows,
+    num_kv_heads, W] (row_slot None: row r's mask is pool[r]) or
+    [slots, layers, num_kv_heads, W] with row_slot an int32 CUDA tensor
+    [num_rows] (row r's mask is pool[row_slot[r], layer]; -1: none).  The
+    descriptor holds raw pointers: keep the tensors alive while it is used."""
+    if pool is None:
+        return wise_mask(None, None, 0, 0)
+    words = _ptr(pool, torch.int32, "pool")
+    if row_slot is None:
+        return wise_mask(words, None, 0, 0)
+    if pool.dim() != 4:
+        raise ValueError("a slot pool is [slots, layers, num_kv_heads, W]")
+    S, Lyr, Hkv, Wd = pool.shape
+    if not 0 <= layer < Lyr:
+        raise ValueError(f"layer {layer} outside [0, {Lyr})")
+    return wise_mask(words + layer * Hkv * Wd * 4, _ptr(row_slot, torch.int32, "row_slot"),
+                     Lyr * Hkv * Wd, S)
+
+
 class wise_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status_word", "num_items", "queue", "head_info", "items",
         "partial_ml", "partial_acc", "tile_stats", "tickets", "partial_ml_1", "partial_acc_1",
-        "tile_stats_1", "max_items", "total_bytes")]
+        "tile_stats_1", "max_items", "total_bytes", "list1", "head_info_1", "items_1")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -88,6 +118,11 @@ def library() -> ctypes.CDLL:
             "wise_block_mass": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_validate": [S, P, P, P, P, P, P],
             "wise_selftest_wait_timeout": [P, P],
+            "wise_noalloc_status": [ctypes.POINTER(ctypes.c_int32), P],
+            "wise_compact_tiles_m": [S, P, P, ctypes.POINTER(wise_mask), P, SZ, P],
+            "wise_decode_finish_m": [S, P, P, P, SZ, U32, ctypes.POINTER(wise_mask), P, P, P],
+            "wise_decode_m": [S, P, P, P, P, P, P, ctypes.POINTER(wise_mask), P, P, P, SZ, P],
+            "wise_validate_m": [S, P, P, P, ctypes.POINTER(wise_mask), P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -188,10 +223,14 @@ def wise_decode_finish(shape, modes, seq_lens, workspace, support, out, lse, str
 
 FLAG_SLOT_SET_1 = 1
 FLAG_EARLY_START = 2
+FLAG_BUILD_SPARSE_LIST = 4
+FLAG_SPARSE_LIST = 8
 
 
 def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                            flags=0, stream=None) -> None:
+    """flags: FLAG_SLOT_SET_1, FLAG_EARLY_START, FLAG_SPARSE_LIST (modes may
+    then be None)."""
     e = _elem(shape)
     _check(library().wise_decode_partial_ex(
         ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
@@ -202,6 +241,8 @@ def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, mod
 
 def wise_decode_finish_ex(shape, modes, seq_lens, workspace, support, out, lse, flags=0,
                           stream=None) -> None:
+    """flags: FLAG_SLOT_SET_1, FLAG_BUILD_SPARSE_LIST, FLAG_SPARSE_LIST (modes
+    may then be None)."""
     e = _elem(shape)
     _check(library().wise_decode_finish_ex(
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
@@ -243,6 +284,50 @@ def wise_decode_noalloc(shape, q, k_cache, v_cache, page_table, seq_lens, modes,
         _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
         _ptr(modes, torch.int8, "modes"), _ptr(support, torch.int32, "support"),
         _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
+
+
+def wise_noalloc_status(stream=None) -> int:
+    """The WISE_DEVERR_* word of the last wise_decode_noalloc call in the
+    current context (copied to the host; synchronises the stream)."""
+    word = ctypes.c_int32(-1)
+    _check(library().wise_noalloc_status(ctypes.byref(word), _stream(stream)))
+    torch.cuda.synchronize()
+    return word.value
+
+
+def wise_compact_tiles_m(shape, modes, seq_lens, mask: wise_mask, workspace, stream=None) -> None:
+    _check(library().wise_compact_tiles_m(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.byref(mask), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
+
+
+def wise_decode_finish_m(shape, modes, seq_lens, workspace, mask: wise_mask, out, lse, flags=0,
+                         stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_finish_m(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), flags, ctypes.byref(mask),
+        _ptr(out, e, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
+
+
+def wise_decode_m(shape, q, k_cache, v_cache, page_table, seq_lens, modes, mask: wise_mask, out,
+                  lse, workspace, stream=None) -> None:
+    e = _elem(shape)
+    _check(library().wise_decode_m(
+        ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(modes, torch.int8, "modes"), ctypes.byref(mask), _ptr(out, e, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
+def wise_validate_m(shape, page_table, seq_lens, modes, mask: wise_mask, err_word,
+                    stream=None) -> None:
+    _check(library().wise_validate_m(
+        ctypes.byref(shape), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(modes, torch.int8, "modes"),
+        ctypes.byref(mask), _ptr(err_word, torch.int32, "err_word"), _stream(stream)))
 
 
 def wise_support_union(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
@@ -306,7 +391,19 @@ def workspace_views(shape: wise_shape, workspace: torch.Tensor) -> Dict[str, tor
         "partial_ml_1": region(lay["partial_ml_1"], mi * G * 2, torch.float32).view(mi, G, 2),
         "partial_acc_1": region(lay["partial_acc_1"], mi * G * D, torch.float32).view(mi, G, D),
         "tile_stats_1": region(lay["tile_stats_1"], R * Hq * shape.max_blocks * 2, torch.float32).view(R, Hq, shape.max_blocks, 2),
+        "list1_counter": region(lay["list1"], 16, torch.int32),
+        "head_info_1": region(lay["head_info_1"], R * Hkv * 4, torch.int32).view(R, Hkv, 4),
+        "items_1": region(lay["items_1"], _tiles_per_item(shape) * mi * 4,
+                          torch.int32).view(_tiles_per_item(shape), mi, 4),
     }
+
+
+def _tiles_per_item(shape: wise_shape) -> int:
+    """Blocks per split range T as the library resolves tiles_per_item = 0."""
+    if shape.tiles_per_item:
+        return shape.tiles_per_item
+    items16 = shape.num_rows * shape.num_kv_heads * (-(-shape.max_blocks // 16))
+    return 16 if shape.max_blocks > 64 and items16 >= 4096 else 8
 
 
 LOG2E = 1.0 / math.log(2.0)

@@ -153,6 +153,55 @@ class Workload:
         return out
 
 
+    def depth_inputs_device(self, depth: int, device="cuda") -> Dict[str, object]:
+        """The same recipe with K and V drawn on the device, for timing runs
+        whose oracle check is elsewhere: q is the host draw of
+        `queries_f32` (so the planted directions are the same), K and V ~
+        N(0,1) come from a torch generator on `device` seeded by (seed,
+        depth, tensor), planted keys get += 0.5 * the planting direction,
+        pool pages no row references and slots past a row's length hold NaN,
+        and the values are rounded to the storage dtype.  Same shapes,
+        distributions and structure as depth_inputs; other values."""
+        R, Hkv, D, P, B = self.num_rows, self.num_kv_heads, self.head_dim, self.page_size, self.tile_tokens
+        G = self.group
+        qf = self.queries_f32(depth)
+        plant_dir = qf.reshape(R, Hkv, G, D).mean(axis=2) if G > 1 else qf
+        used = np.zeros((self.num_pages, P), dtype=bool)
+        plant_pg, plant_sl, plant_h, plant_row = [], [], [], []
+        for r in range(R):
+            L = int(self.seq_lens[r])
+            if L == 0:
+                continue
+            tok = np.arange(L)
+            pages = self.page_table[r, tok // P]
+            used[pages, tok % P] = True
+            for h in range(Hkv):
+                for b in self.planted[r][h]:
+                    t = np.arange(int(b) * B, min((int(b) + 1) * B, L))
+                    plant_pg.append(self.page_table[r, t // P])
+                    plant_sl.append(t % P)
+                    plant_h.append(np.full(t.shape, h))
+                    plant_row.append(np.full(t.shape, r))
+        cat = lambda xs: torch.from_numpy(np.concatenate(xs).astype(np.int64)).to(device) \
+            if xs else torch.zeros(0, dtype=torch.int64, device=device)  # noqa: E731
+        pg, sl, hh, rr = cat(plant_pg), cat(plant_sl), cat(plant_h), cat(plant_row)
+        unused = torch.from_numpy(~used).to(device)
+        dirs = torch.from_numpy(np.ascontiguousarray(plant_dir)).to(device)
+        out = {"q": torch.from_numpy(qf).to(self.torch_dtype)}
+        for name in ("k", "v"):
+            gen = torch.Generator(device=device)
+            gen.manual_seed(int(np.random.SeedSequence([self.seed, depth, _TENSOR_IDS[name]])
+                                .generate_state(1)[0]))
+            pool = torch.randn((self.num_pages, P, Hkv, D), generator=gen, device=device,
+                               dtype=torch.float32)
+            if name == "k" and pg.numel():
+                pool[pg, sl, hh] += 0.5 * dirs[rr, hh]
+            pool[unused] = float("nan")
+            out[name + "_cache"] = pool.to(self.torch_dtype)
+            del pool
+        return out
+
+
 def custom_workload(name: str = "custom", **kw) -> Workload:
     """A workload of any shape built with the same recipe (see `_build`)."""
     return _build(name, **kw)

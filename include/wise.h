@@ -98,10 +98,15 @@ enum {
 enum { WISE_DTYPE_BF16 = 0, WISE_DTYPE_F32 = 1 };
 
 /* Bits of the workspace status word (set by the kernels, read by the caller
- * from the workspace after the stream has run; see wise_workspace_layout). */
+ * from the workspace after the stream has run; see wise_workspace_layout).
+ * After WISE_DEVERR_WAIT_TIMEOUT the out, lse and support a call wrote are
+ * undefined (some work items were not computed). */
 enum {
   WISE_DEVERR_SEQ_LEN_CLAMPED = 1, /* a seq_len exceeded the row's capacity */
-  WISE_DEVERR_WAIT_TIMEOUT = 2     /* a bounded wait gave up (no hang)      */
+  WISE_DEVERR_WAIT_TIMEOUT = 2,    /* a bounded wait gave up (no hang)      */
+  WISE_DEVERR_BAD_WORK_LIST = 4    /* the workspace's work list was not one
+                                      the library wrote for this shape (a
+                                      call out of order); bad items skipped */
 };
 
 /* Bits of the word written by wise_validate. */
@@ -109,7 +114,8 @@ enum {
   WISE_BAD_MODE = 1,           /* mode outside 0..3                          */
   WISE_BAD_SEQ_LEN = 2,        /* seq_len < 0 or above the row's capacity    */
   WISE_BAD_PAGE = 4,           /* a page id the row uses is outside the pool */
-  WISE_EMPTY_SPARSE_SUPPORT = 8 /* a sparse (row, KV head) selects nothing   */
+  WISE_EMPTY_SPARSE_SUPPORT = 8, /* a sparse (row, KV head) selects nothing  */
+  WISE_BAD_SLOT = 16            /* a row slot below -1 or past num_slots     */
 };
 
 typedef struct {
@@ -134,6 +140,27 @@ typedef struct {
   float scale;               /* softmax scale; 0 means 1/sqrt(head_dim)         */
   float eta;                 /* selection threshold, > 0; >= 1 selects all      */
 } wise_shape;
+
+/* Where the rows' support masks live, for the _m calls [WISE PR, "What
+ * changes", wise.py bullet: the engine keeps a [slot, layer, head, block]
+ * support bitmask of per-request slots, freed with the request's
+ * allocation].  The W = ceil(max_blocks / 32) words of (row r, KV head g)
+ * are at words + slot(r) * slot_stride + g * W, where slot(r) = row_slot[r]
+ * (or r when row_slot is NULL).  For a pool [slots, layers, num_kv_heads, W]
+ * and layer l: words = pool + l * num_kv_heads * W, slot_stride = layers *
+ * num_kv_heads * W, num_slots = slots.  A row whose slot is negative (or
+ * >= num_slots when num_slots > 0) has no mask: sparse rows attend nothing
+ * (out 0, lse -inf), discover rows select as usual but store nothing, and a
+ * list build gives them no item; wise_validate_m flags slots below -1 or
+ * past num_slots.  Rows whose slots coincide share one mask: two such rows
+ * that discover in the same call race on it. */
+typedef struct {
+  uint32_t *words;          /* device; 4-byte aligned                            */
+  const int32_t *row_slot;  /* device int32 [num_rows], or NULL: slot = row      */
+  int64_t slot_stride;      /* uint32 words between slots; 0 means num_kv_heads
+                               * W; with row_slot, at least num_kv_heads * W     */
+  int32_t num_slots;        /* slots in the pool, >= 0 (0: slots not checked)    */
+} wise_mask;
 
 /* Offsets (bytes from the workspace base) of the workspace regions, for
  * callers that inspect intermediate results.  All offsets are 256-aligned. */
@@ -165,6 +192,14 @@ typedef struct {
   size_t tile_stats_1;  /* splits while the previous call's finish reads set 0 */
   size_t max_items;     /* capacity of the item arrays                         */
   size_t total_bytes;   /* = wise_workspace_bytes                              */
+  size_t list1;         /* int32 [16]: list 1's items with n tiles at [n - 1]
+                           (WISE_FLAG_BUILD_SPARSE_LIST)                      */
+  size_t head_info_1;   /* int32x4 [R*Hkv]: head info of list 1 (first slot,
+                           slots = items, tiles, items)                       */
+  size_t items_1;       /* int32x4 [tiles_per_item * max_items]: list 1's
+                           items with n tiles at items_1 + (n - 1) * max_items;
+                           slots are compact (item k of a pair writes slot
+                           rg * S + k)                                          */
 } wise_layout;
 
 /* Bytes of device workspace one call sequence needs for this shape.  Host
@@ -228,11 +263,29 @@ enum {
    * it writes, and the compaction this call uses completed before that
    * kernel began: for instance the finish of the previous depth, on the other
    * slot set, when both calls share one compaction. */
-  WISE_FLAG_EARLY_START = 2u
+  WISE_FLAG_EARLY_START = 2u,
+  /* Finish only: also write the work list of a following call in which every
+   * row is sparse on the mask as this call leaves it ("list 1" of the
+   * workspace: head info, items bucketed by tile count, and their schedule
+   * positions), so that call needs no wise_compact_tiles launch [WISE PR,
+   * "What changes": sparse rows are compacted first; the finish of a
+   * discovery depth already holds each (row, KV head)'s final mask].  Rows of
+   * every mode get their list from the mask after the call; padding rows and
+   * masks selecting nothing get no item.  support must not be NULL, and the
+   * call's partial pass must not be on list 1 (that pass, or a compaction,
+   * empties list 1 for this finish to fill).  List 1 stays valid until the
+   * next partial pass that is not on it, or the next compaction. */
+  WISE_FLAG_BUILD_SPARSE_LIST = 4u,
+  /* Partial pass and finish: every row is sparse and the work list is list 1
+   * (written by an earlier finish with WISE_FLAG_BUILD_SPARSE_LIST over the
+   * same rows and lengths); modes is ignored and may be NULL.  Both passes of
+   * the call take the flag.  Not with wise_decode_partial_finish. */
+  WISE_FLAG_SPARSE_LIST = 8u
 };
 
-/* wise_decode_partial with flags (WISE_FLAG_SLOT_SET_1, WISE_FLAG_EARLY_START);
- * flags = 0 is wise_decode_partial.  Unknown flags: WISE_ERR_INVALID_ARG. */
+/* wise_decode_partial with flags (WISE_FLAG_SLOT_SET_1, WISE_FLAG_EARLY_START,
+ * WISE_FLAG_SPARSE_LIST); flags = 0 is wise_decode_partial.  Unknown flags:
+ * WISE_ERR_INVALID_ARG. */
 wise_status wise_decode_partial_ex(const wise_shape *shape, const void *q,
                                    const void *k_cache, const void *v_cache,
                                    const int32_t *page_table, const int32_t *seq_lens,
@@ -240,7 +293,8 @@ wise_status wise_decode_partial_ex(const wise_shape *shape, const void *q,
                                    size_t workspace_bytes, uint32_t flags,
                                    wise_stream_t stream);
 
-/* wise_decode_finish with flags (WISE_FLAG_SLOT_SET_1 only); flags = 0 is
+/* wise_decode_finish with flags (WISE_FLAG_SLOT_SET_1,
+ * WISE_FLAG_BUILD_SPARSE_LIST, WISE_FLAG_SPARSE_LIST); flags = 0 is
  * wise_decode_finish. */
 wise_status wise_decode_finish_ex(const wise_shape *shape, const int8_t *modes,
                                   const int32_t *seq_lens, void *workspace,
@@ -268,6 +322,31 @@ wise_status wise_decode_partial_finish(const wise_shape *shape, const void *q,
                                        void *workspace, size_t workspace_bytes,
                                        uint32_t *support, void *out, float *lse,
                                        wise_stream_t stream);
+
+/* The calls that read or write the mask, with the mask addressed through a
+ * wise_mask (per-request slots and a layer of a mask pool) instead of a
+ * [num_rows, num_kv_heads, W] array; otherwise as wise_compact_tiles,
+ * wise_decode_finish_ex, wise_decode and wise_validate.  `mask` is a HOST
+ * pointer to the descriptor (its words and row_slot are device pointers);
+ * mask->words may be NULL where the flat call's support may be NULL.  The
+ * compaction reads each row's slot with its mode and length. */
+wise_status wise_compact_tiles_m(const wise_shape *shape, const int8_t *modes,
+                                 const int32_t *seq_lens, const wise_mask *mask,
+                                 void *workspace, size_t workspace_bytes,
+                                 wise_stream_t stream);
+wise_status wise_decode_finish_m(const wise_shape *shape, const int8_t *modes,
+                                 const int32_t *seq_lens, void *workspace,
+                                 size_t workspace_bytes, uint32_t flags,
+                                 const wise_mask *mask, void *out, float *lse,
+                                 wise_stream_t stream);
+wise_status wise_decode_m(const wise_shape *shape, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *page_table,
+                          const int32_t *seq_lens, const int8_t *modes,
+                          const wise_mask *mask, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, wise_stream_t stream);
+wise_status wise_validate_m(const wise_shape *shape, const int32_t *page_table,
+                            const int32_t *seq_lens, const int8_t *modes,
+                            const wise_mask *mask, int32_t *err_word, wise_stream_t stream);
 
 /* compact + partial + finish, in that order, on one stream. */
 wise_status wise_decode(const wise_shape *shape, const void *q,
@@ -325,18 +404,31 @@ wise_status wise_validate(const wise_shape *shape, const int32_t *page_table,
  * lives in the library's static device memory, held by every GPU that loads
  * the library until the process exits.  A shape whose workspace
  * (wise_workspace_bytes) exceeds 16 MiB is rejected with WISE_ERR_WORKSPACE
- * and nothing is enqueued.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current),
- * which may load device code: make that first call before any stream
- * capture.  No call allocates or frees device memory.  All calls on a device
+ * and nothing is enqueued.  The first call in each CUDA context looks up the
+ * array's device address (cudaGetSymbolAddress, with that context current)
+ * and caches it under the context handle; the lookup may load device code,
+ * so make that first call before any stream capture.  The cached address
+ * does not survive cudaDeviceReset: after a reset, the first call in the new
+ * context looks it up again only if the driver gives that context a new
+ * handle.  No call allocates or frees device memory.  All calls on a device
  * share the one array and it keeps the last call's contents (nothing in it
  * needs to start at zero); calls whose GPU work overlaps (different streams
- * without ordering) race on it. */
+ * without ordering) race on it.  Device-side conditions (WISE_DEVERR_*) land
+ * in the array's status word: read them with wise_noalloc_status. */
 wise_status wise_decode_noalloc(const wise_shape *shape, const void *q,
                                 const void *k_cache, const void *v_cache,
                                 const int32_t *page_table, const int32_t *seq_lens,
                                 const int8_t *modes, uint32_t *support, void *out,
                                 float *lse, wise_stream_t stream);
+
+/* The WISE_DEVERR_* status word of the last wise_decode_noalloc call in the
+ * current context (0: no condition), copied into *host_status (a HOST
+ * pointer) by a 4-byte device-to-host copy enqueued on `stream`: order the
+ * stream after the decode call, then synchronise it before reading
+ * *host_status.  After WISE_DEVERR_WAIT_TIMEOUT the call's out, lse and
+ * support are undefined.  Allocates nothing.  NULL host_status:
+ * WISE_ERR_INVALID_ARG. */
+wise_status wise_noalloc_status(int32_t *host_status, wise_stream_t stream);
 
 /* Self-test of the failure path (the pages have no counterpart; it computes
  * nothing of the method).  Every mbarrier wait in this library's kernels is

@@ -23,6 +23,8 @@ from typing import Dict, Tuple
 
 import numpy as np
 
+from . import wise_oracle
+
 HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(HERE, "wise_oracle.cpp")
 LIBDIR = os.path.join(HERE, "lib")
@@ -194,6 +196,15 @@ class CppOracle:
                                     "k": int(kst[r, h]), "order": order[r, h, :nb].copy(),
                                     "margin": float(margin[r, h]), "gap": float(gap[r, h])}
         return {"out": out, "lse": lse, "support": new_support, "diag": diag, "scale": scale}
+
+    def decode_layer_slots(self, q, k_cache, v_cache, page_table, seq_lens, modes, pool,
+                           row_slot, layer: int, **kw) -> Dict[str, object]:
+        """decode_layer with masks addressed by slot and layer: the index
+        layer is the numpy oracle's (gather, call, store back; no arithmetic),
+        the call is this oracle's."""
+        return wise_oracle.decode_layer_slots(q, k_cache, v_cache, page_table, seq_lens, modes,
+                                              pool, row_slot, layer, decode=self.decode_layer,
+                                              **kw)
 
     # ------------------------------------------------------------------ selection
     def select_blocks(self, p, eta: float) -> Dict[str, object]:

@@ -245,6 +245,42 @@ def compact_tiles(support: np.ndarray, modes: np.ndarray, seq_lens: np.ndarray,
     return {"lists": lists, "counts": counts}
 
 
+# --------------------------------------------------------------------------- mask pool
+def gather_slot_masks(pool: np.ndarray, row_slot: np.ndarray, layer: int) -> np.ndarray:
+    """The masks a batch's rows use, read from a [slot, layer, KV head, word]
+    pool [WISE PR, "What changes", wise.py bullet: per-request slots hold a
+    [slot, layer, head, block] support bitmask]: row r takes
+    pool[row_slot[r], layer]; a row whose slot is -1 has no mask (all zero)."""
+    pool = np.asarray(pool, np.uint32)
+    R = len(row_slot)
+    out = np.zeros((R,) + pool.shape[2:], np.uint32)
+    for r in range(R):
+        if int(row_slot[r]) >= 0:
+            out[r] = pool[int(row_slot[r]), layer]
+    return out
+
+
+def decode_layer_slots(q, k_cache, v_cache, page_table, seq_lens, modes, pool, row_slot,
+                       layer: int, decode=None, **kw) -> Dict[str, object]:
+    """decode_layer with each row's mask addressed through its slot and the
+    layer: the masks are gathered by index, the call runs, and every row
+    whose mode writes its mask (discover, discover-union) and that has a
+    slot gets its new mask stored back at pool[slot, layer].  Rows without a
+    slot attend and discover as with an empty mask and store nothing.
+    Returns decode_layer's result with "pool" (the pool after the call) in
+    place of "support".  `decode` is the decode_layer to run (this module's
+    by default; the C++ oracle passes its own)."""
+    sup = gather_slot_masks(pool, row_slot, layer)
+    res = (decode or decode_layer)(q, k_cache, v_cache, page_table, seq_lens, modes, sup, **kw)
+    new_pool = np.array(pool, dtype=np.uint32, copy=True)
+    for r in range(len(row_slot)):
+        if int(row_slot[r]) >= 0 and int(modes[r]) in (MODE_DISCOVER, MODE_DISCOVER_UNION) \
+                and int(seq_lens[r]) > 0:
+            new_pool[int(row_slot[r]), layer] = res["support"][r]
+    res["pool"] = new_pool
+    return res
+
+
 # --------------------------------------------------------------------------- one call
 def decode_layer(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                  page_table: np.ndarray, seq_lens: np.ndarray, modes: np.ndarray,

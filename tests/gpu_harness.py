@@ -1,5 +1,7 @@
 """Shared helpers of the GPU parity tests: run one decode call through the C ABI
-and through the CPU oracle on the same seeded inputs, and compare.
+and through the CPU oracle on the same seeded inputs, and compare.  The oracle
+is the C++ one in fp32 unless a test asks for the float64 numpy one (both
+are pinned by the CPU tests; the main per-mode test runs against both).
 
 Tolerances (from the arithmetic; the acceptance bar of this library):
   * bf16 output: max |out_gpu - out_oracle| <= 1e-2, against the oracle's
@@ -26,6 +28,7 @@ import torch
 
 import block_sparse_paged_split_gb300 as W
 from oracle import wise_oracle as O
+from oracle.cpp_oracle import CppOracle
 from tests.oracle_pins import as_oracle_array
 
 OUT_TOL = {"bf16": 1e-2, "f32": 1e-4}
@@ -110,8 +113,22 @@ def gpu_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
             "support": np_support(sup), "ws": views}
 
 
+_CPP = {}
+
+
+def oracle_module(which: str):
+    """The oracle a comparison runs against: "f32" is the C++ oracle in fp32
+    (the acceptance oracle: plain loops, fp32 math, a sort-based eta prefix),
+    "f64" the numpy oracle in float64.  Both are pinned by the CPU tests."""
+    if which == "f64":
+        return O
+    if which not in _CPP:
+        _CPP[which] = CppOracle(which.replace("cpp-", ""))
+    return _CPP[which]
+
+
 def oracle_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
-                eta: Optional[float] = None, rows=None):
+                eta: Optional[float] = None, rows=None, oracle: str = "f32"):
     """The oracle on the same inputs (optionally on a subset of rows)."""
     w = b.w
     c = b.cpu(depth)
@@ -121,8 +138,9 @@ def oracle_call(b: Batch, depth: int, modes: np.ndarray, support: np.ndarray,
         rows = np.asarray(rows)
         q, pt, sl, md, sup = q[rows], pt[rows], sl[rows], md[rows], sup[rows]
     e = w.eta if eta is None else eta
-    res = O.decode_layer(q, as_oracle_array(c["k_cache"]), as_oracle_array(c["v_cache"]), pt, sl,
-                         md, sup, eta=e, tile_tokens=w.tile_tokens)
+    res = oracle_module(oracle).decode_layer(q, as_oracle_array(c["k_cache"]),
+                                             as_oracle_array(c["v_cache"]), pt, sl, md, sup, eta=e,
+                                             tile_tokens=w.tile_tokens)
     res["eta"] = e
     return res
 
@@ -192,7 +210,7 @@ def compare_masks(w, g_support, o, modes, rows=None, support_in=None) -> Dict[st
     G = w.group
     sup_g = g_support if rows is None else g_support[rows]
     rows_idx = range(sup_g.shape[0])
-    checked = excluded = 0
+    checked = excluded_margin = excluded_gap = 0
     fails = []
     for r in rows_idx:
         if int(np.asarray(modes)[r if rows is None else rows[r]]) not in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION):
@@ -204,6 +222,7 @@ def compare_masks(w, g_support, o, modes, rows=None, support_in=None) -> Dict[st
         for g in range(w.num_kv_heads):
             diags = [o["diag"][(r, h)] for h in range(g * G, (g + 1) * G)]
             clear = all(decision_is_clear(dg) for dg in diags)
+            near_margin = any(dg["margin"] <= MARGIN for dg in diags)
             gb = O.mask_bits(sup_g[r, g], nb)
             ob = O.mask_bits(o["support"][r, g], nb)
             if clear:
@@ -211,7 +230,10 @@ def compare_masks(w, g_support, o, modes, rows=None, support_in=None) -> Dict[st
                 if not np.array_equal(gb, ob):
                     fails.append(f"mask differs row {r} kv head {g}")
             else:
-                excluded += 1
+                if near_margin:
+                    excluded_margin += 1
+                else:
+                    excluded_gap += 1
                 must = np.zeros(nb, bool)
                 may = np.zeros(nb, bool)
                 mode_r = int(np.asarray(modes)[r if rows is None else rows[r]])
@@ -230,4 +252,79 @@ def compare_masks(w, g_support, o, modes, rows=None, support_in=None) -> Dict[st
             # never any bit at or past the block count
             if np.any(np.unpackbits(sup_g[r, g].view(np.uint8), bitorder="little")[nb:32 * sup_g.shape[2]]):
                 fails.append(f"bits past the row end row {r} kv head {g}")
-    return {"fails": fails, "checked": checked, "excluded": excluded}
+    return {"fails": fails, "checked": checked, "excluded": excluded_margin + excluded_gap,
+            "excluded_margin": excluded_margin, "excluded_gap": excluded_gap}
+
+
+def item_fields(rec: np.ndarray):
+    """Fields of work-item records int32 [n, 4]: pair rg, block range s,
+    partial slot k, tile bitmap over the range, tile count, row length,
+    sparse flag, discover flag."""
+    rec = np.asarray(rec, np.int64)
+    return {"rg": rec[:, 0], "s": rec[:, 1] & 0xFFFF, "k": rec[:, 1] >> 16,
+            "bits": rec[:, 2] & 0xFFFF, "count": (rec[:, 2] >> 16) & 0xFF,
+            "L": rec[:, 3] & 0xFFFFFF, "sparse": (rec[:, 3] >> 24) & 1,
+            "discover": (rec[:, 3] >> 25) & 1}
+
+
+def list1_schedule(views: dict, T: int) -> np.ndarray:
+    """List 1's items in the order the partial pass hands them out: bucket j
+    holds the items of j + 1 tiles (counter[j] of them), larger buckets
+    first."""
+    cnt = views["list1_counter"].cpu().numpy()[:T].astype(np.int64)
+    items = views["items_1"].cpu().numpy()
+    out = [items[j, :int(cnt[j])] for j in range(T - 1, -1, -1)]
+    return np.concatenate(out) if out else np.zeros((0, 4), np.int32)
+
+
+def item_invariant_fails(recs: np.ndarray, head_info: np.ndarray, lists, T: int, S_max: int,
+                         lens: np.ndarray, modes, Hkv: int, compact_slots: bool) -> list:
+    """A work list against the oracle's compacted tile lists, by properties
+    (the pages fix the lists; how they are cut into items is the kernel's
+    choice): every item holds 1..T tiles, all inside one range [s*T, s*T+T)
+    of its pair, as a bitmap whose popcount is its count; a pair's items,
+    taken by range, concatenate to exactly its list (so each item is a
+    contiguous, strictly ascending run and together they partition it); slots
+    are distinct and below the pair's slot count (equal to the range, or
+    compact 0..items-1 in range order); the schedule is non-increasing in
+    tile count; head info agrees; the record carries the row's length and
+    mode flags (modes None: every row sparse)."""
+    fails = []
+    f = item_fields(recs)
+    if recs.shape[0] and np.any(np.diff(f["count"]) > 0):
+        fails.append("schedule not in non-increasing tile count")
+    pc = np.array([bin(int(b)).count("1") for b in f["bits"]], np.int64)
+    if np.any(pc != f["count"]) or np.any(f["count"] < 1) or np.any(f["count"] > T):
+        fails.append("item counts do not match bitmaps or exceed T")
+    if recs.shape[0] and np.any(f["bits"] >> T):
+        fails.append("bitmap bits at or past T")
+    R = len(lens)
+    for r in range(R):
+        for g in range(Hkv):
+            rg = r * Hkv + g
+            sel = np.nonzero(f["rg"] == rg)[0]
+            order = sel[np.argsort(f["s"][sel], kind="stable")]
+            tiles = []
+            for i in order:
+                tiles += [int(f["s"][i]) * T + b for b in range(T) if (int(f["bits"][i]) >> b) & 1]
+            want = np.asarray(lists[r][g]).tolist()
+            if tiles != want:
+                fails.append(f"items of pair ({r},{g}) do not partition its list")
+            if len(set(f["s"][order].tolist())) != len(order):
+                fails.append(f"pair ({r},{g}) has two items in one range")
+            ks = f["k"][order].tolist()
+            want_k = list(range(len(order))) if compact_slots else f["s"][order].tolist()
+            if ks != want_k:
+                fails.append(f"pair ({r},{g}) slots {ks[:8]} != {want_k[:8]}")
+            hi = head_info[r, g]
+            if int(hi[0]) != rg * S_max or int(hi[2]) != len(want) or int(hi[3]) != len(order):
+                fails.append(f"head info of pair ({r},{g}): {hi.tolist()}")
+            if len(order) and int(hi[1]) <= max(ks):
+                fails.append(f"pair ({r},{g}) slot count {int(hi[1])} too small")
+            for i in order:
+                if int(f["L"][i]) != int(lens[r]):
+                    fails.append(f"item of pair ({r},{g}) has length {int(f['L'][i])}")
+                m = 3 if modes is None else int(np.asarray(modes)[r])
+                if int(f["sparse"][i]) != (m == 3) or int(f["discover"][i]) != (m in (1, 2)):
+                    fails.append(f"item of pair ({r},{g}) has wrong mode flags")
+    return fails

@@ -491,8 +491,75 @@ def pin_compaction(O) -> List[str]:
     return fails
 
 
+def pin_slot_masks(O) -> List[str]:
+    """Masks kept per request slot and layer [WISE PR, "What changes",
+    wise.py bullet: a [slot, layer, head, block] support bitmask], addressed
+    through each row's slot: (a) identity slots on a one-layer pool give
+    decode_layer's results exactly; (b) on a pool of 6 slots x 3 layers whose
+    (slot, layer, KV head) mask selects exactly block (slot + 2 layer + KV
+    head) mod 4, rows with slots [4, 1, -1, 3] at layer 1 attend in sparse mode
+    exactly that block of their own slot -- torch SDPA over its keys -- and the
+    row without a slot outputs 0 with LSE -inf; (c) a discover call stores
+    each row's new mask at (its slot, layer 1) and leaves every other pool
+    entry, and the slot-less row's, bitwise unchanged."""
+    fails = []
+    w, d = make_case(2, 2, 64, "f32", [128, 128, 128, 128], 61)
+    q, kc, vc = (as_oracle_array(d[k]) for k in ("q", "k_cache", "v_cache"))
+    R, B = 4, w.tile_tokens
+    # (a)
+    sup = random_support(w, 62)
+    plain = O.decode_layer(q, kc, vc, w.page_table, w.seq_lens, np.full(R, MODE_SPARSE, np.int8),
+                           sup, tile_tokens=B)
+    viaslots = O.decode_layer_slots(q, kc, vc, w.page_table, w.seq_lens,
+                                    np.full(R, MODE_SPARSE, np.int8), sup[:, None], np.arange(R),
+                                    0, tile_tokens=B)
+    if not (np.array_equal(plain["out"], viaslots["out"]) and
+            np.array_equal(plain["lse"], viaslots["lse"])):
+        fails.append("identity slots differ from decode_layer")
+    # (b)
+    S, Lyr, layer = 6, 3, 1
+    pool = np.zeros((S, Lyr, 2, 1), np.uint32)
+    for sl in range(S):
+        for ly in range(Lyr):
+            for g in range(2):
+                pool[sl, ly, g, 0] = np.uint32(1) << np.uint32((sl + 2 * ly + g) % 4)
+    row_slot = np.array([4, 1, -1, 3])
+    res = O.decode_layer_slots(q, kc, vc, w.page_table, w.seq_lens,
+                               np.full(R, MODE_SPARSE, np.int8), pool, row_slot, layer,
+                               tile_tokens=B)
+    scale = 1.0 / math.sqrt(64)
+    for r in range(R):
+        for h in range(2):
+            if row_slot[r] < 0:
+                if not (np.all(res["out"][r, h] == 0) and res["lse"][r, h] == -math.inf):
+                    fails.append(f"slot-less row {r} head {h} not zero/-inf")
+                continue
+            blk = (int(row_slot[r]) + 2 * layer + h) % 4
+            mask = np.zeros(128, bool)
+            mask[blk * B:(blk + 1) * B] = True
+            qq, K, V = _ref_row(d, r, h, h)
+            o = _sdpa(qq, K, V, scale, mask).numpy()
+            if not np.allclose(res["out"][r, h], o, rtol=tol(O, "out_rtol"), atol=tol(O, "out_atol")):
+                fails.append(f"row {r} head {h} does not attend its slot's block {blk}")
+    if not np.array_equal(res["pool"], pool):
+        fails.append("a sparse call changed the pool")
+    # (c)
+    res = O.decode_layer_slots(q, kc, vc, w.page_table, w.seq_lens,
+                               np.full(R, MODE_DISCOVER, np.int8), pool, row_slot, layer,
+                               tile_tokens=B)
+    own = O.decode_layer(q, kc, vc, w.page_table, w.seq_lens, np.full(R, MODE_DISCOVER, np.int8),
+                         np.zeros((R, 2, 1), np.uint32), tile_tokens=B)["support"]
+    want = pool.copy()
+    for r in range(R):
+        if row_slot[r] >= 0:
+            want[row_slot[r], layer] = own[r]
+    if not np.array_equal(res["pool"], want):
+        fails.append("discover stored masks at the wrong place or touched other entries")
+    return fails
+
+
 ALL_PINS = [pin_dense_sdpa, pin_sparse_masked_sdpa, pin_sparse_bruteforce_loops,
             pin_all_blocks_sparse_is_dense,
             pin_paging_invariance, pin_page_size_invariance, pin_block_masses, pin_selection_bruteforce,
             pin_selection_golden, pin_selection_limits, pin_union, pin_density_example,
-            pin_compaction, pin_head_union]
+            pin_compaction, pin_head_union, pin_slot_masks]

@@ -124,16 +124,43 @@ def test_flag_checks(lib):
     P = ctypes.c_void_p
     # unknown partial flags, and a partial-only flag given to the finish
     st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
-                                    P(4096), n, ctypes.c_uint32(8), None)
+                                    P(4096), n, ctypes.c_uint32(16), None)
     assert st == 1 and b"flags" in lib.wise_last_error()
+    st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
+                                    P(4096), n, ctypes.c_uint32(W.FLAG_BUILD_SPARSE_LIST), None)
+    assert st == 1  # a finish-only flag
     st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
                                    ctypes.c_uint32(W.FLAG_EARLY_START), P(16), P(16), P(16), None)
+    assert st == 1
+    # building the next sparse list needs the mask
+    st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                   ctypes.c_uint32(W.FLAG_BUILD_SPARSE_LIST), None, P(16), P(16), None)
+    assert st == 1 and b"support" in lib.wise_last_error()
+    # a call on list 1 cannot rebuild it
+    st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                   ctypes.c_uint32(W.FLAG_BUILD_SPARSE_LIST | W.FLAG_SPARSE_LIST),
+                                   P(16), P(16), P(16), None)
+    assert st == 1
+    # a call on list 1 needs no modes; without the flag it does
+    st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), None,
+                                    P(4096), n, ctypes.c_uint32(0), None)
     assert st == 1
     lay = W.wise_workspace_layout(s)
     # the second slot set: three more aligned regions after the first set
     second = [lay[k] for k in ("partial_ml_1", "partial_acc_1", "tile_stats_1")]
     assert all(o % 256 == 0 for o in second) and min(second) > lay["tile_stats"]
     assert lay["total_bytes"] > max(second)
+    # list 1: header inside the first 256 bytes, head info and T buckets of
+    # max_items records after the second slot set
+    assert 0 < lay["list1"] and lay["list1"] + 64 <= 256
+    assert lay["head_info_1"] % 256 == 0 and lay["items_1"] % 256 == 0
+    assert lay["head_info_1"] > max(second) and lay["items_1"] >= lay["head_info_1"] + 4 * 2 * 16
+    assert lay["total_bytes"] >= lay["items_1"] + 8 * lay["max_items"] * 16
+
+
+def test_noalloc_status_rejects_a_null_pointer(lib):
+    assert lib.wise_noalloc_status(None, None) == 1
+    assert b"host_status" in lib.wise_last_error()
 
 
 def test_default_split_size(lib):
@@ -157,3 +184,36 @@ def test_selftest_rejects_a_bad_status_pointer(lib):
     assert lib.wise_selftest_wait_timeout(None, None) == 1
     assert lib.wise_selftest_wait_timeout(P(4098), None) == 1
     assert b"status_word" in lib.wise_last_error()
+
+
+def test_mask_descriptor_checks(lib):
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    P = ctypes.c_void_p
+    mk = lambda words, slots, stride, num: W.wise.wise_mask(words, slots, stride, num)  # noqa: E731
+    W_ = -(-s.max_blocks // 32)
+    # no descriptor
+    assert lib.wise_compact_tiles_m(ctypes.byref(s), P(16), P(16), None, P(4096), n, None) == 1
+    # misaligned words or slots
+    m = mk(18, None, 0, 0)
+    assert lib.wise_compact_tiles_m(ctypes.byref(s), P(16), P(16), ctypes.byref(m), P(4096), n, None) == 1
+    m = mk(16, 18, 0, 0)
+    assert lib.wise_compact_tiles_m(ctypes.byref(s), P(16), P(16), ctypes.byref(m), P(4096), n, None) == 1
+    # a slot stride shorter than one slot's masks
+    m = mk(16, 16, s.num_kv_heads * W_ - 1, 4)
+    assert lib.wise_decode_finish_m(ctypes.byref(s), P(16), P(16), P(4096), n, 0, ctypes.byref(m),
+                                    P(16), P(16), None) == 1
+    assert b"slot_stride" in lib.wise_last_error()
+    m = mk(16, 16, 0, -1)
+    assert lib.wise_validate_m(ctypes.byref(s), P(16), P(16), P(16), ctypes.byref(m), P(16), None) == 1
+    # building list 1 needs mask words
+    m = mk(None, None, 0, 0)
+    assert lib.wise_decode_finish_m(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                    W.FLAG_BUILD_SPARSE_LIST, ctypes.byref(m), P(16), P(16), None) == 1
+
+
+def test_make_mask_addresses_a_layer_of_the_pool():
+    import torch
+    pool = torch.zeros((5, 3, 2, 4), dtype=torch.int32)
+    with pytest.raises(ValueError):
+        W.make_mask(pool, torch.zeros(2, dtype=torch.int32), 1)  # a CPU tensor is refused

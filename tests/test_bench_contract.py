@@ -52,6 +52,17 @@ def test_gpu_arm_line():
     assert set(out["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert out["config"]["workload"].startswith("ouro1.4b_1k")
     assert 0 < out["config"]["support_density_blocks"] <= 1
+    # the default run also covers the 4K, mixed 8K and 32K grouped-query workloads
+    sweep = out["modes_by_workload"]
+    assert set(sweep) == {"ouro1.4b_4k", "mixed_8k", "gqa_32k"}
+    for name, res in sweep.items():
+        assert res["step_ms"] > 0 and res["rows_per_s"] > 0 and res["dense_step_ms"] > 0, name
+        for mode, row in res["modes"].items():
+            assert row["call_us"] >= row["partial_us"] > 0, (name, mode)
+            assert 0 < row["call_frac_of_measured_hbm"] <= row["partial_frac_of_measured_hbm"]
+    # the sparse depths of the headline step run on the list the union depth built
+    assert "no compaction launch" in out["config"]["workload"]
+    assert "compact" not in out["modes"]["depth2_sparse"]["kernels_us"]
 
 
 @pytest.mark.gpu

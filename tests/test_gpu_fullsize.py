@@ -37,6 +37,8 @@ def _pipeline(name, rows=None):
     for depth in range(w.num_depths):
         modes = w.depth_modes[depth]
         g, o, cm = _check_depth(b, depth, modes, sup, rows=rows)
+        print(f"{name} depth {depth}: masks bit-exact {cm['checked']}, bounds-checked near the "
+              f"margin {cm['excluded_margin']}, near a mass tie {cm['excluded_gap']}")
         stats.append(cm)
         sup = g["support"]
     return w, sup, stats
@@ -85,6 +87,8 @@ def test_gqa_32k_discover_eta_sweep(eta):
     b = Batch(w)
     zero = np.zeros((w.num_rows, w.num_kv_heads, words(w)), np.uint32)
     g, o, cm = _check_depth(b, 0, w.depth_modes[0], zero, eta=eta)
+    print(f"gqa_32k eta {eta}: masks bit-exact {cm['checked']}, bounds-checked near the margin "
+          f"{cm['excluded_margin']}, near a mass tie {cm['excluded_gap']}")
     assert cm["checked"] > 0
 
 

@@ -55,6 +55,7 @@ def test_full_pipeline_every_row(name):
     for depth in range(w.num_depths):
         g, cm = _check(b, depth, w.depth_modes[depth], sup)
         checked += cm["checked"]
+        print(f"{name} depth {depth}: masks bit-exact {cm['checked']}, bounds-checked near the "
+              f"margin {cm['excluded_margin']}, near a mass tie {cm['excluded_gap']}")
         sup = g["support"]
-    if name != "gqa_32k":
-        assert checked > 0
+    assert checked > 0

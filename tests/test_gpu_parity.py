@@ -9,7 +9,9 @@ import block_sparse_paged_split_gb300 as W
 from block_sparse_paged_split_gb300.workload import custom_workload, make_workload
 from oracle import wise_oracle as O
 from tests.gpu_harness import (Batch, compare_masks, compare_outputs, dev_support, gpu_call,
-                               np_support, oracle_call, shape_for, words)
+                               item_invariant_fails, list1_schedule, np_support, oracle_call,
+                               shape_for, words)
+from tests.gpu_harness import oracle_call as _oracle_call
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +29,14 @@ CASES = [(4, 4, 128, "bf16"), (4, 4, 64, "bf16"), (8, 2, 128, "bf16"), (4, 1, 64
          (2, 2, 64, "f32"), (4, 2, 128, "f32")]
 
 
+@pytest.mark.parametrize("oracle", ["f32", "f64"])
 @pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
-def test_modes_match_oracle(Hq, Hkv, D, dtype):
+def test_modes_match_oracle(Hq, Hkv, D, dtype, oracle):
     w = _wl(Hq, Hkv, D, dtype)
     b = Batch(w)
     R = w.num_rows
     zero = np.zeros((R, Hkv, words(w)), np.uint32)
+    oracle_call = lambda *a, **k: _oracle_call(*a, oracle=oracle, **k)  # noqa: E731
     # dense
     m = np.full(R, W.MODE_DENSE, np.int8)
     g, o = gpu_call(b, 0, m, zero), oracle_call(b, 0, m, zero)
@@ -122,10 +126,24 @@ def test_tiny_schedule_f32():
         sup = o["support"]
 
 
-def test_compaction_matches_oracle():
-    """Work items (tiles as bitmaps over their block range) and per-head
-    counts, against the oracle's lists and items: bit-exact, over rows of up
-    to four mask words."""
+def _compact(w, T, modes, sup, lens=None):
+    """wise_compact_tiles alone; returns the workspace views on the host."""
+    lens = w.seq_lens if lens is None else lens
+    shape = shape_for(w, tiles_per_item=T)
+    ws = W.alloc_workspace(shape)
+    W.wise_compact_tiles(shape, torch.from_numpy(np.asarray(modes, np.int8)).cuda(),
+                         torch.from_numpy(np.asarray(lens, np.int32)).cuda(), dev_support(sup), ws)
+    torch.cuda.synchronize()
+    return shape, {k: t.cpu().numpy() for k, t in W.workspace_views(shape, ws).items()}
+
+
+def test_compaction_items_partition_the_oracle_lists():
+    """The compaction's work items against the oracle's compacted tile lists,
+    by properties (the pages fix the lists, the cut into items is the
+    kernel's): each item a run of 1..T tiles inside one range, a pair's items
+    partitioning its list, slots equal to ranges, schedule non-increasing in
+    tile count, head info and record fields right; empty ranges of sparse
+    rows marked in both slot sets so the finish skips them."""
     rng = np.random.default_rng(5)
     for T in (1, 2, 4, 8, 16):
         lens = rng.integers(0, 4000, size=9).astype(np.int32)
@@ -134,45 +152,190 @@ def test_compaction_matches_oracle():
         bits = rng.random((R, 2, words(w) * 32)) < 0.3
         sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 2, -1).copy()
         modes = rng.choice([0, 1, 2, 3], size=R).astype(np.int8)
-        shape = shape_for(w, tiles_per_item=T)
-        ws = W.alloc_workspace(shape)
-        W.wise_compact_tiles(shape, torch.from_numpy(modes).cuda(), torch.from_numpy(lens).cuda(),
-                             dev_support(sup), ws)
-        torch.cuda.synchronize()
-        v = {k: t.cpu().numpy() for k, t in W.workspace_views(shape, ws).items()}
-        ref = O.compact_tiles(sup, modes, lens, 32, T)
+        shape, v = _compact(w, T, modes, sup)
+        ref = O.compact_tiles(sup, modes, lens, 32)
         n = int(v["num_items"][0])
-        assert n == ref["items"].shape[0]
-        rec = v["items"][:n]
-        counts = (rec[:, 2] >> 16) & 0xFF
-        assert np.all(np.diff(counts) <= 0)  # schedule order: tile count descending
-        canon = rec[np.lexsort((rec[:, 1], rec[:, 0]))]
-        for (rg, s_, z, wfield), (r, g, s_ref, first, cnt) in zip(canon, ref["items"]):
-            assert (rg, s_) == (r * 2 + g, s_ref)
-            bitmap = int(z) & 0xFFFF
-            tiles = [s_ * T + i for i in range(16) if bitmap >> i & 1]
-            assert len(tiles) == cnt == (int(z) >> 16) & 0xFF
-            assert tiles == ref["lists"][r][g][first:first + cnt].tolist()
-            assert (int(wfield) & 0xFFFFFF) == lens[r]
-            assert bool(wfield & (1 << 24)) == (modes[r] == W.MODE_SPARSE)
-            assert bool(wfield & (1 << 25)) == (modes[r] in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION))
-        assert int(v["queue"][0]) == 0
         S_max = -(-shape.max_blocks // T)
+        fails = item_invariant_fails(v["items"][:n], v["head_info"], ref["lists"], T, S_max, lens,
+                                     modes, 2, compact_slots=False)
+        assert not fails, fails[:5]
+        assert int(v["queue"][0]) == 0 and int(v["status"][0]) == 0
         for r in range(R):
             nb = -(-int(lens[r]) // 32)
             for g in range(2):
-                lst = ref["lists"][r][g]
                 hi = v["head_info"][r, g]
-                assert hi[0] == (r * 2 + g) * S_max
-                assert hi[1] == -(-nb // T) and hi[2] == lst.shape[0]
-                assert hi[3] == len(set((lst // T).tolist()))
+                assert hi[1] == -(-nb // T)  # one slot per range
                 if modes[r] == W.MODE_SPARSE:
-                    # empty ranges are marked so the finish pass skips them
-                    ml = v["partial_ml"][hi[0]:hi[0] + hi[1]]
-                    for s_ in range(hi[1]):
-                        if not np.any(lst // T == s_):
-                            assert np.all(np.isneginf(ml[s_, :, 0])) and np.all(ml[s_, :, 1] == 0)
-        assert int(v["status"][0]) == 0
+                    lst = ref["lists"][r][g]
+                    for key in ("partial_ml", "partial_ml_1"):
+                        ml = v[key][hi[0]:hi[0] + hi[1]]
+                        for s_ in range(hi[1]):
+                            if not np.any(lst // T == s_):
+                                assert np.all(np.isneginf(ml[s_, :, 0])) and np.all(ml[s_, :, 1] == 0)
+
+
+def test_compaction_items_depend_only_on_their_row():
+    """A pair's items (as (range, slot, bitmap, count, length, flags)) are the
+    same in a mixed batch as when its row is compacted alone."""
+    rng = np.random.default_rng(15)
+    lens = rng.integers(0, 3000, size=7).astype(np.int32)
+    w = _wl(4, 2, 64, "bf16", lens=lens, seed=19)
+    R = w.num_rows
+    bits = rng.random((R, 2, words(w) * 32)) < 0.25
+    sup = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, 2, -1).copy()
+    modes = np.array([3, 0, 1, 3, 2, 3, 0], np.int8)
+    for T in (2, 8):
+        _, v = _compact(w, T, modes, sup)
+        allrec = v["items"][:int(v["num_items"][0])]
+        for r in range(R):
+            # the same batch with every other row padding (length 0)
+            solo = np.zeros_like(lens)
+            solo[r] = lens[r]
+            _, vs = _compact(w, T, modes, sup, lens=solo)
+            one = vs["items"][:int(vs["num_items"][0])]
+            for g in range(2):
+                a = allrec[allrec[:, 0] == r * 2 + g]
+                b = one[one[:, 0] == r * 2 + g]
+                key = lambda x: x[np.lexsort((x[:, 1],))]
+                assert np.array_equal(key(a), key(b)), (T, r, g)
+                assert np.array_equal(v["head_info"][r, g], vs["head_info"][r, g])
+
+
+def _list1_views(shape, ws):
+    return {k: t.cpu() for k, t in W.workspace_views(shape, ws).items()}
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens", [(4, 4, RAGGED), (8, 2, RAGGED),
+                                         (4, 2, np.array([10000, 5000, 1, 33, 0], np.int32))])
+def test_finish_built_list_partitions_the_oracle_lists(Hq, Hkv, lens):
+    """A finish with WISE_FLAG_BUILD_SPARSE_LIST writes list 1: for every row
+    (discover rows from the mask the call writes, the other rows from the
+    mask as it is) the items partition the oracle's compacted list of an
+    all-sparse call on that mask, with compact slots, bucketed by tile count,
+    taken in schedule order (larger buckets first)."""
+    w = _wl(Hq, Hkv, 128, "bf16", lens=lens, seed=41)
+    b = Batch(w)
+    R = w.num_rows
+    rng = np.random.default_rng(43)
+    bits = rng.random((R, Hkv, words(w) * 32)) < 0.3
+    sup_np = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(R, Hkv, -1).copy()
+    modes_np = np.array([1, 2, 0, 3, 1, 2, 3, 1] * 2, np.int8)[:R]
+    for T in (0, 2, 16):
+        shape = shape_for(w, tiles_per_item=T)
+        Tr = W.wise._tiles_per_item(shape)
+        ws = W.alloc_workspace(shape)
+        sup = dev_support(sup_np)
+        modes = torch.from_numpy(modes_np).cuda()
+        d = b.dev(0)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+        W.wise_compact_tiles(shape, modes, b.seq_lens, sup, ws)
+        W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
+                              modes, ws)
+        W.wise_decode_finish_ex(shape, modes, b.seq_lens, ws, sup, out, lse,
+                                flags=W.FLAG_BUILD_SPARSE_LIST)
+        torch.cuda.synchronize()
+        v = _list1_views(shape, ws)
+        after = np_support(sup)
+        ref = O.compact_tiles(after, np.full(R, W.MODE_SPARSE, np.int8), w.seq_lens, 32)
+        sched = list1_schedule(v, Tr)
+        S_max = -(-shape.max_blocks // Tr)
+        fails = item_invariant_fails(sched, v["head_info_1"].numpy(), ref["lists"], Tr, S_max,
+                                     w.seq_lens, None, Hkv, compact_slots=True)
+        assert not fails, fails[:5]
+        assert not v["list1_counter"][Tr:].any()
+        # the call itself is unchanged by the flag
+        g = gpu_call(b, 0, modes_np, sup_np, tiles_per_item=T)
+        assert torch.equal(out.cpu(), g["out_raw"]) and np.array_equal(after, g["support"])
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
+def test_sparse_on_finish_built_list(Hq, Hkv, D, dtype):
+    """The four-depth step the benchmark runs -- discover, union-discover
+    building list 1, then two sparse depths on list 1 with no compaction --
+    against the same calls each with its own compaction (bitwise: rows of at
+    most 64 blocks merge their splits in the same order) and against the
+    oracle."""
+    w = _wl(Hq, Hkv, D, dtype)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = W.alloc_workspace(shape)
+    sup = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    disc = torch.full((R,), W.MODE_DISCOVER, dtype=torch.int8, device="cuda")
+    union = torch.full((R,), W.MODE_DISCOVER_UNION, dtype=torch.int8, device="cuda")
+    sparse = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
+    outs = []
+    for rep in range(2):  # the second step reuses the workspace as the benchmark does
+        sup.zero_()
+        outs = []
+        for depth, m, flags, compact in ((0, disc, 0, True), (1, union, W.FLAG_BUILD_SPARSE_LIST, False),
+                                         (2, sparse, W.FLAG_SPARSE_LIST, False),
+                                         (0, sparse, W.FLAG_SPARSE_LIST, False)):
+            d = b.dev(depth)
+            out = torch.empty_like(d["q"])
+            lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+            if compact:
+                W.wise_compact_tiles(shape, m, b.seq_lens, sup, ws)
+            pflags = flags & W.FLAG_SPARSE_LIST
+            W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, None if pflags else m, ws, pflags)
+            W.wise_decode_finish_ex(shape, None if pflags else m, b.seq_lens, ws, sup, out, lse,
+                                    flags=flags)
+            torch.cuda.synchronize()
+            outs.append((out.cpu(), lse.cpu().numpy(), np_support(sup)))
+        assert int(W.workspace_views(shape, ws)["queue"].item()) == 0
+    s0 = np.zeros((R, Hkv, words(w)), np.uint32)
+    g0 = gpu_call(b, 0, np.full(R, 1, np.int8), s0)
+    g1 = gpu_call(b, 1, np.full(R, 2, np.int8), g0["support"])
+    g2 = gpu_call(b, 2, np.full(R, 3, np.int8), g1["support"])
+    g3 = gpu_call(b, 0, np.full(R, 3, np.int8), g1["support"])
+    for (out, lse, s_), g in zip(outs, (g0, g1, g2, g3)):
+        assert torch.equal(out, g["out_raw"]) and np.array_equal(lse, g["lse"])
+        assert np.array_equal(s_, g["support"])
+    o = oracle_call(b, 2, np.full(R, 3, np.int8), g1["support"])
+    assert not compare_outputs(w, g2, o)
+
+
+def test_finish_built_list_long_rows_match_oracle():
+    """Long rows (the clustered finish) through list 1: a union-discover
+    finish builds it, a sparse call runs on it, against the oracle on the
+    same mask, for a split of 16 tiles and of 1 (1024 ranges a pair)."""
+    lens = np.array([20000, 3000, 0, 700, 17000], np.int32)
+    w = _wl(8, 2, 128, "bf16", lens=lens, seed=47, n_planted=6)
+    b = Batch(w)
+    R = w.num_rows
+    for T in (16, 1):
+        shape = shape_for(w, tiles_per_item=T)
+        ws = W.alloc_workspace(shape)
+        g0 = gpu_call(b, 0, np.full(R, 1, np.int8), np.zeros((R, 2, words(w)), np.uint32))
+        sup = dev_support(g0["support"])
+        union = torch.full((R,), W.MODE_DISCOVER_UNION, dtype=torch.int8, device="cuda")
+        d1, d2 = b.dev(1), b.dev(2)
+        out = torch.empty_like(d1["q"])
+        lse = torch.empty((R, 8), dtype=torch.float32, device="cuda")
+        W.wise_compact_tiles(shape, union, b.seq_lens, sup, ws)
+        W.wise_decode_partial(shape, d1["q"], d1["k_cache"], d1["v_cache"], b.page_table,
+                              b.seq_lens, union, ws)
+        W.wise_decode_finish_ex(shape, union, b.seq_lens, ws, sup, out, lse,
+                                flags=W.FLAG_BUILD_SPARSE_LIST)
+        out2 = torch.empty_like(d2["q"])
+        lse2 = torch.empty_like(lse)
+        W.wise_decode_partial_ex(shape, d2["q"], d2["k_cache"], d2["v_cache"], b.page_table,
+                                 b.seq_lens, None, ws, W.FLAG_SPARSE_LIST)
+        W.wise_decode_finish_ex(shape, None, b.seq_lens, ws, None, out2, lse2,
+                                flags=W.FLAG_SPARSE_LIST)
+        torch.cuda.synchronize()
+        mask = np_support(sup)
+        g = {"out": out2.double().cpu().numpy(), "lse": lse2.cpu().numpy()}
+        o = oracle_call(b, 2, np.full(R, W.MODE_SPARSE, np.int8), mask)
+        assert not compare_outputs(w, g, o)
+        v = _list1_views(shape, ws)
+        ref = O.compact_tiles(mask, np.full(R, 3, np.int8), w.seq_lens, 32)
+        fails = item_invariant_fails(list1_schedule(v, T), v["head_info_1"].numpy(), ref["lists"],
+                                     T, -(-shape.max_blocks // T), w.seq_lens, None, 2,
+                                     compact_slots=True)
+        assert not fails, fails[:5]
 
 
 def test_all_selected_sparse_is_dense_bitwise():
@@ -613,5 +776,9 @@ def test_compaction_beyond_cached_rounds():
     g, o = gpu_call(b, 0, m, sup, tiles_per_item=1), oracle_call(b, 0, m, sup)
     assert not compare_outputs(w, g, o)
     assert not compare_masks(w, g["support"], o, m, support_in=sup)["fails"]
-    ref = O.compact_tiles(sup, m, lens, 32, 1)
-    assert int(g["ws"]["num_items"][0]) == ref["items"].shape[0]
+    ref = O.compact_tiles(sup, m, lens, 32)
+    v = {k: t.numpy() for k, t in g["ws"].items()}
+    n = int(v["num_items"][0])
+    fails = item_invariant_fails(v["items"][:n], v["head_info"], ref["lists"], 1, 1024, lens, m, 1,
+                                 compact_slots=False)
+    assert not fails, fails[:5]

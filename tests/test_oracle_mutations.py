@@ -148,6 +148,32 @@ def m_compaction_ignores_mode(O):
     O.compact_tiles = compact_tiles
 
 
+def m_slot_ignored(O):
+    """Rows index the pool by their row number instead of their slot."""
+    orig = O.decode_layer_slots
+
+    def decode_layer_slots(q, k, v, pt, sl, modes, pool, row_slot, layer, **kw):
+        return orig(q, k, v, pt, sl, modes, pool, np.where(np.asarray(row_slot) >= 0,
+                                                           np.arange(len(row_slot)), -1), layer, **kw)
+    O.decode_layer_slots = decode_layer_slots
+
+
+def m_slot_wrong_layer(O):
+    orig = O.decode_layer_slots
+
+    def decode_layer_slots(q, k, v, pt, sl, modes, pool, row_slot, layer, **kw):
+        return orig(q, k, v, pt, sl, modes, pool, row_slot, (layer + 1) % pool.shape[1], **kw)
+    O.decode_layer_slots = decode_layer_slots
+
+
+def m_no_slot_reads_slot_zero(O):
+    orig = O.decode_layer_slots
+
+    def decode_layer_slots(q, k, v, pt, sl, modes, pool, row_slot, layer, **kw):
+        return orig(q, k, v, pt, sl, modes, pool, np.maximum(np.asarray(row_slot), 0), layer, **kw)
+    O.decode_layer_slots = decode_layer_slots
+
+
 def m_head_union_skips_last_head(O):
     def support_head_union(support):
         sup = np.asarray(support, dtype=np.uint32)
@@ -162,7 +188,8 @@ MUTANTS = [m_scale_squared, m_slot_off_by_one, m_page_order_reversed, m_wrong_kv
            m_tile_sum_without_max, m_masses_drop_partial_block, m_ties_to_higher_index,
            m_strict_cutoff, m_one_extra_block, m_union_overwrites, m_mask_ignored,
            m_mask_bit_order_reversed, m_compaction_drops_last_block,
-           m_compaction_ignores_mode, m_head_union_skips_last_head]
+           m_compaction_ignores_mode, m_head_union_skips_last_head, m_slot_ignored,
+           m_slot_wrong_layer, m_no_slot_reads_slot_zero]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)

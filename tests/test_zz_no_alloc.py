@@ -4,9 +4,11 @@ capture, or a host framework that forbids allocations outside its own pool).
 It uses the library's static 16 MiB device scratch instead of a workspace.
 
 The GPU test calls it through the C ABI twice in a row (the second call finds
-the first call's leftovers in the shared scratch) and checks each result
-against the ordinary wise_decode with a caller-owned workspace, within the
-tolerances the parity tests use.  This file is collected last on purpose.
+the first call's leftovers in the shared scratch), then once more with a
+shape whose workspace layout differs, and checks each result against the
+ordinary wise_decode with a caller-owned workspace bit for bit (both run the
+same kernels on the same inputs), and that the scratch's status word, read
+with wise_noalloc_status, is 0.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -18,7 +20,7 @@ import block_sparse_paged_split_gb300 as W
 from block_sparse_paged_split_gb300 import wise
 from block_sparse_paged_split_gb300.build import build_library
 from block_sparse_paged_split_gb300.workload import custom_workload
-from tests.gpu_harness import LSE_TOL, OUT_TOL, dev_support, np_support, shape_for, words
+from tests.gpu_harness import dev_support, np_support, shape_for, words
 
 
 @pytest.fixture(scope="module")
@@ -56,6 +58,11 @@ def _call(shape, d, pt, sl, modes, sup, ws=None):
 
 @pytest.mark.gpu
 def test_noalloc_matches_wise_decode_twice(lib):
+    """Two calls in a row (a discover depth, then sparse / union rows on its
+    mask), then a third with another shape and split size, whose workspace
+    layout puts every region at other offsets in the shared scratch: each
+    equals wise_decode with a caller-owned workspace bit for bit (the same
+    kernels on the same inputs), and the scratch's status word reads 0."""
     lens = np.array([1, 33, 200, 517, 0, 1024], np.int32)
     R = len(lens)
     w = custom_workload("noalloc", R=R, Hq=8, Hkv=4, D=128, dtype="bf16", depths=2, n_planted=3,
@@ -75,11 +82,29 @@ def test_noalloc_matches_wise_decode_twice(lib):
         modes = torch.from_numpy(modes_np).cuda()
         ref_out, ref_lse, ref_sup = _call(shape, d, pt, sl, modes, sup, ws)
         out, lse, new_sup = _call(shape, d, pt, sl, modes, sup)
-        err = (out.double() - ref_out.double()).abs().max().item()
-        assert err <= OUT_TOL["bf16"], err
-        a, b = lse.cpu().numpy(), ref_lse.cpu().numpy()
-        fin = np.isfinite(b)
-        assert np.array_equal(np.isfinite(a), fin)
-        assert np.max(np.abs(a[fin] - b[fin])) <= LSE_TOL
+        assert torch.equal(out, ref_out)
+        assert np.array_equal(lse.cpu().numpy(), ref_lse.cpu().numpy())
         assert np.array_equal(np_support(new_sup), np_support(ref_sup))
+        assert wise.wise_noalloc_status() == 0
         sup = ref_sup
+    # A different layout: GQA 32/8 heads, longer rows, 2-block ranges.
+    lens2 = np.array([3000, 40, 0, 1500], np.int32)
+    w2 = custom_workload("noalloc2", R=4, Hq=32, Hkv=8, D=128, dtype="bf16", depths=1,
+                         n_planted=4, seq_lens=lens2, pool_factor=1, seed=23,
+                         depth_modes=[np.zeros(4, np.int8)])
+    shape2 = shape_for(w2, tiles_per_item=2)
+    assert W.wise_workspace_layout(shape2)["partial_ml"] != W.wise_workspace_layout(shape)["partial_ml"]
+    assert W.wise_workspace_bytes(shape2) <= (16 << 20)
+    d2 = {k: v.cuda() for k, v in w2.depth_inputs(0).items()}
+    pt2 = torch.from_numpy(w2.page_table).cuda()
+    sl2 = torch.from_numpy(w2.seq_lens).cuda()
+    modes2 = torch.from_numpy(np.array([1, 3, 1, 2], np.int8)).cuda()
+    rng = np.random.default_rng(3)
+    bits = rng.random((4, 8, words(w2) * 32)) < 0.3
+    s2 = dev_support(np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(4, 8, -1))
+    ref_out, ref_lse, ref_sup = _call(shape2, d2, pt2, sl2, modes2, s2, W.alloc_workspace(shape2))
+    out, lse, new_sup = _call(shape2, d2, pt2, sl2, modes2, s2)
+    assert torch.equal(out, ref_out)
+    assert np.array_equal(lse.cpu().numpy(), ref_lse.cpu().numpy())
+    assert np.array_equal(np_support(new_sup), np_support(ref_sup))
+    assert wise.wise_noalloc_status() == 0
