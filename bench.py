@@ -88,6 +88,9 @@ def parse():
                         "selected tiles; prints one JSON line with the table")
     p.add_argument("--point", default=None, metavar="CONTEXT:TILES",
                    help="with --sparse-scaling: time only this point (e.g. 8192:1)")
+    p.add_argument("--gqa", action="store_true",
+                   help="with --sparse-scaling: 32 query / 8 KV heads (the tensor-core path), "
+                        "16 rows, contexts 4K-32K")
     p.add_argument("--shared-blocks", action="store_true",
                    help="with --sparse-scaling: every head of a row selects the same blocks")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -1145,25 +1148,31 @@ def sparse_scaling_main(args):
     build_library()
     lib = wise.library()
     torch.cuda.set_device(0)
-    R, H, D, reps = args.rows or 64, 16, 128, 30
+    if args.gqa:
+        # Grouped-query heads (the tensor-core consumer): 32 query / 8 KV heads.
+        R, H, Hq, D, reps = args.rows or 16, 8, 32, 128, 30
+        points = ([(L, 16, True) for L in (4096, 8192, 16384, 32768)] +
+                  [(32768, k, False) for k in (1, 4, 64, 256, 1024)])
+    else:
+        R, H, Hq, D, reps = args.rows or 64, 16, 16, 128, 30
+        points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768)] +
+                  [(8192, k, False) for k in (1, 2, 4, 16, 32, 64, 128, 256)])
     peak, peak_kind = peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768)] +
-              [(8192, k, False) for k in (1, 2, 4, 16, 32, 64, 128, 256)])
     if args.point:
         L, k = (int(x) for x in args.point.split(":"))
         points = [(L, k, False)]
     rows = []
     for L, k, with_dense in points:
         d = sparse_scaling_inputs(R, H, D, L, k, seed=4242 + L + k,
-                                  shared_blocks=args.shared_blocks)
-        shape = W.make_shape(num_rows=R, num_q_heads=H, num_kv_heads=H, head_dim=D, page_size=16,
+                                  shared_blocks=args.shared_blocks, num_q_heads=Hq)
+        shape = W.make_shape(num_rows=R, num_q_heads=Hq, num_kv_heads=H, head_dim=D, page_size=16,
                              max_pages_per_row=d["page_table"].shape[1], num_pages=d["num_pages"],
                              max_blocks=d["max_blocks"], dtype=W.DTYPE_BF16, eta=0.95)
         ws = W.alloc_workspace(shape)
         out = torch.empty_like(d["q"])
-        lse = torch.empty((R, H), dtype=torch.float32, device="cuda")
+        lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
         S = ctypes.byref(shape)
         st = stream.cuda_stream
         args_common = (d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
@@ -1225,7 +1234,7 @@ def sparse_scaling_main(args):
         rows.append(row)
         del d, ws, out, lse
         torch.cuda.empty_cache()
-    print(json.dumps({"sparse_scaling": rows, "rows": R, "heads": H, "head_dim": D,
+    print(json.dumps({"sparse_scaling": rows, "rows": R, "heads": H, "q_heads": Hq, "head_dim": D,
                       "blocks": "shared by a row's heads" if args.shared_blocks else "per head",
                       "peak_gbs": peak, "peak_kind": peak_kind, "reps": reps,
                       "l2": "flushed by a 512 MiB write before every call"}))

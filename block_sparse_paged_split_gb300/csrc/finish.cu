@@ -157,13 +157,136 @@ __device__ __forceinline__ void group_select(const float2 (&st)[E], int nb, floa
   }
 }
 
+// Sums over the group's threads of N unsigned integers at once: one warp
+// reduction instruction each, the warps' sums through shared memory, one named
+// barrier.  `buf` holds two sets of wph * N sums used alternately (by
+// `parity`), so a warp that races ahead to the next call never overwrites a set
+// another warp is still reading.
+template <int N>
+__device__ __forceinline__ void group_sums_u32(const uint32_t (&v)[N], uint32_t (&out)[N],
+                                               int lane, int wsub, int wph, uint32_t* buf,
+                                               int& parity, int bar_id) {
+  uint32_t* b = buf + (parity & 1) * 8 * N;
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    const uint32_t w = __reduce_add_sync(kFull, v[n]);
+    if (lane == 0) b[wsub * N + n] = w;
+  }
+  group_sync(bar_id, wph * 32);
+#pragma unroll
+  for (int n = 0; n < N; ++n) out[n] = 0u;
+  for (int w = 0; w < wph; ++w) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) out[n] += b[w * N + n];
+  }
+  ++parity;
+}
+
+// Selection for one query head without sorting (rows of 512 or more padded
+// blocks).  The rule -- order blocks by mass descending, equal masses by the
+// lower block index, keep the shortest prefix reaching eta -- keeps every
+// block whose mass exceeds some threshold value v, plus the blocks of mass
+// exactly v in index order until the sum reaches eta.  The masses become
+// fixed-point integers (p * 2^31, truncated: every sum is exact, so the result
+// does not depend on the order of addition; the masses sum to about 1, so
+// every sum fits in 32 bits), and v is the largest float bit pattern whose
+// blocks of mass >= v sum to eta or more, found two bits at a time from the
+// top (three group sums a step).  The truncation moves a sum by less than
+// 1024 * 2^-31 = 4.8e-7, so the cutoff can differ from an exact prefix sum
+// only where the cumulative mass lies that close to eta.  Block i = wsub * 32E
+// + lane * E + e stays in index order, so the kept blocks become mask words by
+// shuffles (each word written once, no atomics).
+template <int E>
+__device__ __forceinline__ void group_select_threshold(const float2 (&st)[E], int nb, float lse2,
+                                                       float eta, int lane, int wsub, int wph,
+                                                       uint32_t* buf, int* cnt, int bar_id,
+                                                       uint32_t* smask) {
+  constexpr float kFix = 2147483648.0f;  // 2^31
+  const int base = wsub * 32 * E + lane * E;
+  uint32_t key[E], m[E];
+  uint32_t mine[1] = {0u};
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (base + e < nb) {
+      const float p = st[e].y * exp2f(st[e].x - lse2);
+      key[e] = __float_as_uint(p);
+      m[e] = __float2uint_rz(p * kFix);
+    } else {
+      key[e] = 0u;
+      m[e] = 0u;
+    }
+    mine[0] += m[e];
+  }
+  int parity = 0;
+  uint32_t total[1];
+  group_sums_u32<1>(mine, total, lane, wsub, wph, buf, parity, bar_id);
+  // At least one fixed-point unit: the rule always keeps a block.
+  const uint32_t eta_fix = max(__double2uint_rn(fmin((double)eta, 1.0) * 2147483648.0), 1u);
+  bool keep[E];
+  if (eta >= 1.f || total[0] < eta_fix) {
+    // eta >= 1 keeps every block; so does a sum that never reaches eta.
+#pragma unroll
+    for (int e = 0; e < E; ++e) keep[e] = base + e < nb;
+  } else {
+    uint32_t v = 0u;
+    // Masses are below 2 (bit 30 clear): bits 29..0, two a step.
+    for (int b = 28; b >= 0; b -= 2) {
+      uint32_t sm[3] = {0u, 0u, 0u}, tot[3];
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) sm[c] += key[e] >= (v | ((uint32_t)(c + 1) << b)) ? m[e] : 0u;
+      group_sums_u32<3>(sm, tot, lane, wsub, wph, buf, parity, bar_id);
+      v |= (tot[2] >= eta_fix ? 3u : tot[1] >= eta_fix ? 2u : tot[0] >= eta_fix ? 1u : 0u) << b;
+    }
+    uint32_t a[1] = {0u}, above[1];
+    int ties = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      a[0] += key[e] > v ? m[e] : 0u;
+      ties += (key[e] == v && base + e < nb) ? 1 : 0;
+    }
+    group_sums_u32<1>(a, above, lane, wsub, wph, buf, parity, bar_id);
+    // Every tied block has mass v, hence the same fixed-point mass.
+    const uint32_t mt = __float2uint_rz(__uint_as_float(v) * kFix);
+    const uint32_t need = eta_fix - above[0];  // > 0 by the choice of v
+    const uint32_t take = mt ? (need + mt - 1u) / mt : 0xffffffffu;
+    // Ties before this thread's first block, in block order.
+    int incl = ties;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) cnt[wsub] = incl;
+    group_sync(bar_id, wph * 32);
+    uint32_t rank = (uint32_t)(incl - ties);
+    for (int w = 0; w < wsub; ++w) rank += (uint32_t)cnt[w];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const bool tied = key[e] == v && base + e < nb;
+      keep[e] = (key[e] > v && base + e < nb) || (tied && rank < take);
+      rank += tied ? 1u : 0u;
+    }
+  }
+  // 32 / E consecutive lanes hold one mask word.
+  constexpr int kLanesPerWord = 32 / E;
+  uint32_t nib = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) nib |= keep[e] ? (1u << e) : 0u;
+  uint32_t word = nib << ((lane % kLanesPerWord) * E);
+#pragma unroll
+  for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(kFull, word, o);
+  if (lane % kLanesPerWord == 0) smask[base >> 5] = word;
+}
+
 // Long rows: one CTA of W warps per (row, query head); the G CTAs of
 // a KV head's group form one thread-block cluster, so their selections are
 // ORed through distributed shared memory (every SM of the group sorts one
 // head's keys, instead of one SM sorting all of them).
-//   merge   the warps take the split slots round-robin, four loads in flight
-//           per lane, with an online rescale; the warps' (m, l, acc) are then
-//           combined through shared memory.
+//   merge   the warps take the split slots round-robin, four (eight for
+//           1024-key rows) loads in flight per lane, with an online rescale;
+//           the warps' (m, l, acc) are then combined through shared memory.
 //   select  npad = 32 * E * W keys (npad >= max_blocks, a power of
 //           two; blocks past the row's n_b are padding) are sorted mostly in
 //           registers (see group_bitonic_sort).
@@ -239,11 +362,14 @@ __global__ void __launch_bounds__(W * 32)
   const float* acc = ws.partial_acc + (slot0 * G + hgrp) * D + lane * dpl;
   const int n = min(max(hi.y, 0), kp.S_max);
   float m_w = -INFINITY, lam = 0.f;
-  for (int s0 = wsub; s0 < n; s0 += 4 * wph) {
-    float2 t[4];
-    float4 a[4];
+  // Slots in flight per lane: 8 for 1024-key rows (64 slots of 16 tiles: one
+  // round of loads for 8 warps), 4 otherwise.
+  constexpr int U = 32 * E * W >= 1024 ? 8 : 4;
+  for (int s0 = wsub; s0 < n; s0 += U * wph) {
+    float2 t[U];
+    float4 a[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int s = s0 + u * wph;
       const bool in = s < n;
       t[u] = in ? ml[(size_t)s * G] : make_float2(-INFINITY, 0.f);
@@ -252,7 +378,7 @@ __global__ void __launch_bounds__(W * 32)
     }
     float mb = m_w;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < U; ++u)
       if (t[u].y > 0.f) mb = fmaxf(mb, t[u].x);
     if (mb > m_w) {  // rescale what this warp has summed so far
       const float sc = exp2f(m_w - mb);
@@ -262,7 +388,7 @@ __global__ void __launch_bounds__(W * 32)
       m_w = mb;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const bool used = t[u].y > 0.f;  // an empty range's accumulator is never used
       const float w = used ? exp2f(t[u].x - m_w) : 0.f;
       lam = fmaf(t[u].y, w, lam);
@@ -323,7 +449,15 @@ __global__ void __launch_bounds__(W * 32)
   // ---- eta selection for this query head, then the group's OR
   if (th < 32) smask[th] = 0u;
   __syncthreads();
-  group_select<E>(st, nb, lse2, kp.eta, lane, wsub, wph, xbuf, scratch, bar_id, smask);
+  if constexpr (32 * E * W >= 512) {
+    // 512 or 1024 keys: the threshold search (the bitonic sort of 1024 keys
+    // took 10 us of a 19 us finish at 32K, %globaltimer stamps per CTA).
+    group_select_threshold<E>(st, nb, lse2, kp.eta, lane, wsub, wph,
+                              reinterpret_cast<uint32_t*>(xbuf), reinterpret_cast<int*>(scratch),
+                              bar_id, smask);
+  } else {
+    group_select<E>(st, nb, lse2, kp.eta, lane, wsub, wph, xbuf, scratch, bar_id, smask);
+  }
   __syncthreads();
   cluster_arrive();  // every head's choice is in its CTA's smask
   cluster_wait();

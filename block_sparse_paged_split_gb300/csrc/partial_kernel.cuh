@@ -548,15 +548,18 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     };
     // A record the library did not write for this shape (a call out of
     // order on the workspace) is flagged and skipped, never followed.
+    // Only what keeps every access in bounds is checked: the pair, the range
+    // and the slot, a non-empty bitmap inside the range, and its last tile
+    // below the row's length.  (The producer counts an item's tiles from the
+    // bitmap, so the record's count field is never trusted.)
     auto record_ok = [&](const int4& rec) {
       const unsigned bits = (unsigned)rec.z & 0xffffu;
-      const int cnt = (rec.z >> 16) & 0xff;
-      const int s_rng = rec.y & 0xffff, slot = (int)((unsigned)rec.y >> 16);
+      const unsigned s_rng = (unsigned)rec.y & 0xffffu, slot = (unsigned)rec.y >> 16;
       const int L = rec.w & kItemLenMask;
-      const bool ok = rec.x >= 0 && rec.x < kp.R * kp.Hkv && s_rng < kp.S_max && slot < kp.S_max &&
-                      cnt >= 1 && cnt <= kp.T && __popc(bits) == cnt && (bits >> kp.T) == 0u &&
-                      L <= kp.cap_tokens &&
-                      (s_rng * kp.T + 31 - __clz(bits | 1u)) * kTile < L;
+      const int last = (int)s_rng * kp.T + 31 - __clz(bits | 1u);
+      const bool ok = (unsigned)rec.x < (unsigned)(kp.R * kp.Hkv) &&
+                      max(s_rng, slot) < (unsigned)kp.S_max && bits - 1u < (1u << kp.T) - 1u &&
+                      L <= kp.cap_tokens && last * kTile < L;
       if (!ok) flag_error(ws.status, WISE_DEVERR_BAD_WORK_LIST);
       return ok;
     };
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // (one tile left to prepare): claiming earlier would hoard items other
       // consumers could start sooner (measured: claiming at four tiles left
       // is 0.9% slower, at one 0.5% faster than at two).
-      if (!nxt_ok && !exhausted && (!cur_ok || ((cur.z >> 16) & 0xff) - k <= 1)) {
+      if (!nxt_ok && !exhausted && (!cur_ok || __popc((unsigned)cur.z & 0xffffu) - k <= 1)) {
         const int slot = first_claim ? first_slot : n_consumers + atomicAdd(ws.queue, 1);
         if (slot < n_items) {
           nxt = first_claim ? first_rec : record_at(slot);
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         // Prepare tile k of the current item: the k-th set bit of its range
         // bitmap, and the page ids of its one or two pages.
         const int rg = cur.x;
-        const int ntiles = (cur.z >> 16) & 0xff;
+        const int ntiles = __popc((unsigned)cur.z & 0xffffu);
         const int L = cur.w & kItemLenMask;
         const int row = rg / kp.Hkv;
         const int range0 = (cur.y & 0xffff) * kp.T;

@@ -298,20 +298,21 @@ WORKLOADS = tuple(BASE_SEEDS)
 
 def sparse_scaling_inputs(R: int, H: int, D: int, L: int, k: int, seed: int,
                           device="cuda", page_size: int = 16, tile_tokens: int = 32,
-                          shared_blocks: bool = False):
+                          shared_blocks: bool = False, num_q_heads: Optional[int] = None):
     """Inputs of the sparse-scaling measurement, drawn on the device (timing
-    only; no parity check reads them): R rows of L tokens, H heads MHA, bf16
-    q/K/V ~ N(0,1) from a seeded device generator, each row's pages at a
-    seeded permutation of a pool exactly the batch's size, and per (row, head)
-    k distinct blocks drawn uniformly without replacement from the row's
-    L / tile_tokens blocks (a seeded host draw; with shared_blocks, one draw per
-    row that all its heads share).  Returns q, k_cache, v_cache,
-    page_table, seq_lens and the mask [R, H, W] (int32 words)."""
+    only; no parity check reads them): R rows of L tokens, H KV heads (and
+    num_q_heads query heads, H by default: MHA), bf16 q/K/V ~ N(0,1) from a
+    seeded device generator, each row's pages at a seeded permutation of a
+    pool exactly the batch's size, and per (row, KV head) k distinct blocks
+    drawn uniformly without replacement from the row's L / tile_tokens
+    blocks (a seeded host draw; with shared_blocks, one draw per row that all
+    its heads share).  Returns q, k_cache, v_cache, page_table, seq_lens and
+    the mask [R, H, W] (int32 words)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     npg = -(-L // page_size)
     num_pages = R * npg
-    q = torch.randn((R, H, D), generator=gen, device=device).to(torch.bfloat16)
+    q = torch.randn((R, num_q_heads or H, D), generator=gen, device=device).to(torch.bfloat16)
     k_cache = torch.randn((num_pages, page_size, H, D), generator=gen, device=device,
                           dtype=torch.bfloat16)
     v_cache = torch.randn((num_pages, page_size, H, D), generator=gen, device=device,

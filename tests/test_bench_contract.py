@@ -83,6 +83,22 @@ def test_sparse_scaling_point():
     assert 0 < pt["partial_frac"] < 1.5
 
 
+@pytest.mark.gpu
+def test_sparse_scaling_point_grouped_query():
+    """The same measurement on the tensor-core path: 32 query / 8 KV heads,
+    4 rows at 8K context, 16 selected tiles per (row, KV head): the selected
+    bytes count each KV tile once for its four query heads."""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--sparse-scaling",
+                          "--gqa", "--point", "8192:16", "--rows", "4"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    out = json.loads([l for l in res.stdout.splitlines() if l.startswith("{")][-1])
+    (pt,) = out["sparse_scaling"]
+    assert out["heads"] == 8 and out["q_heads"] == 32 and out["rows"] == 4
+    assert pt["selected_kv_bytes"] == 4 * 8 * 16 * 32 * 512
+    assert 0 < pt["sparse_partial_us"] <= pt["sparse_call_us"] * 1.01
+
+
 def test_reference_arm_other_ranks_exit_quietly():
     """Under torchrun only rank 0 runs the reference arm; the others print
     nothing and exit 0."""

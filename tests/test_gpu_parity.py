@@ -536,6 +536,38 @@ def test_long_rows_match_oracle(Hq, Hkv, lens):
     assert not compare_outputs(w, g, o)
 
 
+@pytest.mark.parametrize("eta", [1e-13, 0.3, 0.95, 0.999, 1.0])
+def test_long_row_selection_across_eta(eta):
+    """Rows of 512 and more padded blocks select by the threshold search (no
+    sort): against the oracle at every threshold, including the ends -- a
+    vanishing eta keeps each query head's heaviest block only (the group's
+    union of argmaxes), eta = 1 keeps every causal block."""
+    lens = np.array([20000, 17000, 9000, 700], np.int32)
+    w = _wl(8, 2, 128, "bf16", lens=lens, seed=53, n_planted=6)
+    b = Batch(w)
+    R = w.num_rows
+    zero = np.zeros((R, 2, words(w)), np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, zero, eta=eta), oracle_call(b, 0, m, zero, eta=eta)
+    assert not compare_outputs(w, g, o)
+    cm = compare_masks(w, g["support"], o, m)
+    assert not cm["fails"], cm
+    for r in range(R):
+        nb = -(-int(lens[r]) // 32)
+        for g_ in range(2):
+            bits = O.mask_bits(g["support"][r, g_], nb)
+            if eta >= 1.0:
+                assert bits.all()
+            elif eta < 1e-9:
+                # at most one block per query head, each within rounding of its head's maximum
+                assert 1 <= bits.sum() <= 4
+                heavy = np.zeros(nb, bool)
+                for h in range(4 * g_, 4 * g_ + 4):
+                    p = o["diag"][(r, h)]["p"]
+                    heavy |= p >= p.max() * (1 - 1e-5)
+                assert not np.any(bits & ~heavy)
+
+
 @pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
 def test_folded_finish_matches_two_passes_bitwise(Hq, Hkv, D, dtype):
     """The partial pass with the finish folded in gives the partial + finish
