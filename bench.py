@@ -77,6 +77,9 @@ def parse():
     p.add_argument("--no-sweep", action="store_true",
                    help="measure only the headline workload (the default run also measures "
                         "the 4K, mixed 8K and 32K grouped-query workloads)")
+    p.add_argument("--no-dense-list", action="store_true",
+                   help="dense and discover depths get a compaction instead of deriving their "
+                        "work list from the row lengths")
     p.add_argument("--no-sparse-list", action="store_true",
                    help="sparse depths get their own compaction instead of the work list the "
                         "previous depth's finish builds")
@@ -333,7 +336,7 @@ class Pipeline:
 
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
                  lse_discover: bool = False, overlap: bool = False, share=None,
-                 sparse_list: bool = True, device_inputs: bool = False):
+                 sparse_list: bool = True, device_inputs: bool = False, dense_list: bool = True):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -419,11 +422,29 @@ class Pipeline:
         # those depths run on it (WISE_FLAG_SPARSE_LIST) with no compaction
         # launch.  The variants above keep a compaction per sparse depth.
         self.sparse_list = sparse_list and not (fold or overlap or head_union or lse_discover)
+        # dense_list=True: depths with no sparse row derive their work list
+        # from the row lengths in the partial pass (WISE_FLAG_DENSE_LIST), so
+        # with the sparse list the step launches no compaction at all.
+        self.dense_list = (dense_list and w.num_rows <= W.DENSE_LIST_MAX_ROWS and
+                           not (fold or overlap or head_union or lse_discover))
+        # A list-derived pass needs the workspace's queue counters at 0.
+        W.wise_workspace_reset(self.shape, self.ws)
 
-        def calls(modes_t, t, compact=True, early=False, build=False, on_list=False):
+        def calls(modes_t, t, compact=True, early=False, build=False, on_list=False, dense=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
+            if dense:
+                # Every kernel ahead of it in the step is a pass of the library.
+                pf = W.FLAG_DENSE_LIST | W.FLAG_INPUTS_READY
+                ff = W.FLAG_DENSE_LIST | (W.FLAG_BUILD_SPARSE_LIST if build else 0)
+                c.append(("partial", lib.wise_decode_partial_ex,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, pf, st)))
+                c.append(("finish", lib.wise_decode_finish_ex,
+                          (S, m, sl, ws, nws, ff, sup, self.out[t].data_ptr(),
+                           self.lse[t].data_ptr(), st)))
+                return c
             if on_list:
                 f = W.FLAG_SPARSE_LIST
                 c.append(("partial", lib.wise_decode_partial_ex,
@@ -505,21 +526,26 @@ class Pipeline:
 
         self.wise_step = []
         listed = False  # list 1 holds the work list of an all-sparse depth on the current mask
+        list0 = False   # the compacted list holds the previous depth's work list
         for t in range(w.num_depths):
             dm = w.depth_modes
-            reuse = t > 0 and same_work_list(dm[t], dm[t - 1])
+            reuse = list0 and same_work_list(dm[t], dm[t - 1])
+            list0 = False
             if lse_discover and all_discover(dm[t]):
                 self.wise_step.append((t, depth_name(dm[t]), lse_discover_calls(self.modes[t], t)))
                 continue
             on_list = self.sparse_list and listed and all_sparse(dm[t])
             build = (self.sparse_list and not all_sparse(dm[t]) and t + 1 < w.num_depths and
                      all_sparse(dm[t + 1]))
+            dense = self.dense_list and not any(int(x) == W.MODE_SPARSE for x in dm[t])
             listed = build or on_list
-            if on_list or build:
+            if on_list or build or dense:
                 self.wise_step.append((t, depth_name(dm[t]),
-                                       calls(self.modes[t], t, compact=not reuse, build=build,
-                                             on_list=on_list)))
+                                       calls(self.modes[t], t, compact=not reuse and not dense,
+                                             build=build, on_list=on_list, dense=dense)))
+                list0 = build and not dense
                 continue
+            list0 = True
             c = calls(self.modes[t], t, compact=not reuse, early=reuse)
             if head_union and all_sparse(w.depth_modes[t]) and not reuse:
                 # The page-granular variant: sparse depths attend the head
@@ -528,8 +554,13 @@ class Pipeline:
             self.wise_step.append((t, depth_name(w.depth_modes[t]), c))
         # The dense baseline gets the same call sequence: one compaction for
         # its four depths (they share the work list) and the same overlap.
-        self.dense_step = [(t, "dense", calls(self.dense_modes, t, compact=(t == 0), early=(t > 0)))
-                           for t in range(w.num_depths)]
+        if self.dense_list:
+            self.dense_step = [(t, "dense", calls(self.dense_modes, t, dense=True))
+                               for t in range(w.num_depths)]
+        else:
+            self.dense_step = [(t, "dense", calls(self.dense_modes, t, compact=(t == 0),
+                                                  early=(t > 0)))
+                               for t in range(w.num_depths)]
         # Sparse rows of a depth that no earlier depth discovers (a mixed
         # batch) use the support of a prior discovery of the same inputs.
         if any(int(x) == W.MODE_SPARSE for x in w.depth_modes[0]):
@@ -620,22 +651,33 @@ class Pipeline:
         return w.num_rows * w.num_q_heads * w.head_dim * es  # q read
 
 
+# Eager launches go out one ctypes call at a time, slower than the GPU runs
+# them, so without a lead every event bracket would also hold the host's
+# submission of the launch.  Each eager step therefore starts behind a spin
+# kernel long enough for the host to queue the whole step first; the events
+# then see only the GPU, and the step's time is taken from the end of the spin.
+LEAD_CYCLES = 4_000_000  # about 2 ms at the GB300's 2.07 GHz maximum SM clock
+
+
 def timed_region(pipe, step, K, dist, with_events=True):
     import torch
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     events = [] if with_events else None
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(pipe.stream)
+    marks = []
     for _ in range(K):
+        torch.cuda._sleep(LEAD_CYCLES)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(pipe.stream)
         pipe.run(step, events)
-    end.record(pipe.stream)
+        end.record(pipe.stream)
+        marks.append((start, end))
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    return start.elapsed_time(end), events
+    return sum(s.elapsed_time(e) for s, e in marks), events
 
 
 def graph_region(pipe, graph, K, dist):
@@ -887,7 +929,7 @@ def sweep_workload(name, args, steps, peak):
     t0 = time.time()
     w = make_workload(name, **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
-                    device_inputs=True)
+                    device_inputs=True, dense_list=not args.no_dense_list)
     for _ in range(3):
         pipe.run(pipe.wise_step)
         pipe.run(pipe.dense_step)
@@ -950,7 +992,7 @@ def main_ours(args):
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank), **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
                     lse_discover=args.lse_discover, overlap=args.overlap,
-                    sparse_list=not args.no_sparse_list)
+                    sparse_list=not args.no_sparse_list, dense_list=not args.no_dense_list)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -1031,7 +1073,8 @@ def main_ours(args):
     # the compute), then the same steps with each step's copies in line.
     pipe_b = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold,
                       head_union=args.head_union, lse_discover=args.lse_discover,
-                      overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list)
+                      overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list,
+                      dense_list=not args.no_dense_list)
     graph_b = pipe_b.graph(pipe_b.wise_step)
     e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
     e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)
@@ -1072,14 +1115,18 @@ def main_ours(args):
                                + (", finish folded into the partial pass" if pipe.folded else "")
                                + (", consecutive depths overlap (two slot sets, early start)" if pipe.overlap else "")
                                + (", sparse depths on the work list the union depth's finish "
-                                  "builds (no compaction launch)" if pipe.sparse_list else ""),
+                                  "builds (no compaction launch)" if pipe.sparse_list else "")
+                               + (", dense and discover depths on work lists derived from the "
+                                  "row lengths (no compaction launch)" if pipe.dense_list else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "
                          f"of K/V per step (129 MB L2)",
                    "timing": "value: CUDA-graph replay of the step, CUDA events around the K "
                              "replays; modes and roofline: eager launches with CUDA events "
-                             "around every launch on the launching stream",
+                             "around every launch on the launching stream, each step queued "
+                             "behind a spin kernel so that no event bracket holds host "
+                             "submission time",
                    "union_density": round(density, 4) if density else None,
                    "support_density_blocks": round(block_density, 4) if block_density else None},
         "modes": modes,

@@ -102,6 +102,8 @@ KParams make_params(const wise_shape* s) {
   kp.early = 0;
   kp.list1 = 0;
   kp.build = 0;
+  kp.dense_list = 0;
+  kp.inputs_ready = 0;
   return kp;
 }
 
@@ -299,6 +301,16 @@ wise_status wise_workspace_bytes(const wise_shape* shape, size_t* bytes) {
   return WISE_OK;
 }
 
+wise_status wise_workspace_reset(const wise_shape* shape, void* workspace, size_t workspace_bytes,
+                                 wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  WsView ws;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "workspace header reset");
+}
+
 wise_status wise_workspace_layout(const wise_shape* shape, wise_layout* layout) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
@@ -344,10 +356,19 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
                          const FoldArgs& fa, uint32_t flags, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
-  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START | WISE_FLAG_SPARSE_LIST))
+  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START | WISE_FLAG_SPARSE_LIST |
+                          WISE_FLAG_DENSE_LIST | WISE_FLAG_INPUTS_READY))
     return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-  if ((flags & WISE_FLAG_SPARSE_LIST) && fa.out)
-    return fail(WISE_ERR_INVALID_ARG, "the folded finish takes no WISE_FLAG_SPARSE_LIST");
+  if ((flags & (WISE_FLAG_SPARSE_LIST | WISE_FLAG_DENSE_LIST)) && fa.out)
+    return fail(WISE_ERR_INVALID_ARG, "the folded finish takes neither list flag");
+  if ((flags & WISE_FLAG_SPARSE_LIST) && (flags & WISE_FLAG_DENSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_SPARSE_LIST and WISE_FLAG_DENSE_LIST exclude each other");
+  if ((flags & WISE_FLAG_DENSE_LIST) && shape->num_rows > WISE_DENSE_LIST_MAX_ROWS)
+    return fail(WISE_ERR_UNSUPPORTED, "WISE_FLAG_DENSE_LIST takes at most %d rows (got %d)",
+                WISE_DENSE_LIST_MAX_ROWS, shape->num_rows);
+  if ((flags & WISE_FLAG_DENSE_LIST) && (flags & WISE_FLAG_EARLY_START))
+    return fail(WISE_ERR_INVALID_ARG,
+                "WISE_FLAG_DENSE_LIST clears the status word, so the pass cannot start early");
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
     return st;
@@ -363,6 +384,8 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
   KParams kp = make_params(shape);
   kp.early = (flags & WISE_FLAG_EARLY_START) ? 1 : 0;
   kp.list1 = (flags & WISE_FLAG_SPARSE_LIST) ? 1 : 0;
+  kp.dense_list = (flags & WISE_FLAG_DENSE_LIST) ? 1 : 0;
+  kp.inputs_ready = (flags & WISE_FLAG_INPUTS_READY) ? 1 : 0;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = shape->dtype == WISE_DTYPE_BF16
                       ? launch_partial_bf16(kp, tmK, tmV, q, page_table, seq_lens, modes, ws, fa, st_)
@@ -421,8 +444,14 @@ wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
                                  void* out, float* lse, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
-  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_BUILD_SPARSE_LIST | WISE_FLAG_SPARSE_LIST))
+  if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_BUILD_SPARSE_LIST | WISE_FLAG_SPARSE_LIST |
+                          WISE_FLAG_DENSE_LIST))
     return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((flags & WISE_FLAG_SPARSE_LIST) && (flags & WISE_FLAG_DENSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_SPARSE_LIST and WISE_FLAG_DENSE_LIST exclude each other");
+  if ((flags & WISE_FLAG_DENSE_LIST) && shape->num_rows > WISE_DENSE_LIST_MAX_ROWS)
+    return fail(WISE_ERR_UNSUPPORTED, "WISE_FLAG_DENSE_LIST takes at most %d rows (got %d)",
+                WISE_DENSE_LIST_MAX_ROWS, shape->num_rows);
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
     return st;
@@ -441,6 +470,7 @@ wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
   KParams kp = make_params(shape);
   kp.build = (flags & WISE_FLAG_BUILD_SPARSE_LIST) ? 1 : 0;
   kp.list1 = (flags & WISE_FLAG_SPARSE_LIST) ? 1 : 0;
+  kp.dense_list = (flags & WISE_FLAG_DENSE_LIST) ? 1 : 0;
   cudaError_t e = launch_finish(shape->dtype, kp, modes, seq_lens, ws, mv, out, lse,
                                 reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "finish launch");

@@ -14,6 +14,7 @@ namespace wise {
 
 constexpr int kTile = 32;             // block / tile size B in tokens
 constexpr int kMaxT = 16;             // largest tiles_per_item
+constexpr int kMaxDenseRows = WISE_DENSE_LIST_MAX_ROWS;  // rows of a call on the dense list
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -33,6 +34,10 @@ struct KParams {
   int list1;         // partial and finish: the work list is list 1 (built by an
                      // earlier finish), every row sparse
   int build;         // finish: also build list 1 from the mask this call leaves
+  int dense_list;    // partial and finish: every block of every row, items derived from
+                     // the row lengths (no compaction)
+  int inputs_ready;  // partial: the caller's inputs were complete before the previous
+                     // kernel began (a dense-list pass may read them before its wait)
 };
 
 // Device view of the caller's workspace (offsets from wise_workspace_layout).

@@ -132,13 +132,16 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
   constexpr int kCached = 4;
   const int rounds = (nunits + nthreads - 1) / nthreads;
   UnitLoad ld[kCached];
+  // Everything is read after the dependency wait: the mask comes from the
+  // previous call, and the caller's inputs may come from the kernel before
+  // this one (its writes are only certain to be visible past the wait).
+  grid_dependency_wait();
+  grid_dependents_launch();  // the partial pass may start its prologue now
 #pragma unroll
   for (int c = 0; c < kCached; ++c) {
     ld[c] = UnitLoad{-1, 0, -1, 0u};
     if (c < rounds) unit_load_inputs(ld[c], c * nthreads + gt, nunits, modes, seq_lens, mv, kp);
   }
-  grid_dependency_wait();    // the previous call's mask
-  grid_dependents_launch();  // the partial pass may start its prologue now
 #pragma unroll
   for (int c = 0; c < kCached; ++c)
     if (c < rounds) unit_load_mask(ld[c], c * nthreads + gt, nunits, mv, kp);

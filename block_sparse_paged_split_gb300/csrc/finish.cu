@@ -326,9 +326,16 @@ __global__ void __launch_bounds__(W * 32)
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 
   // Read before the dependency wait: the caller's inputs and the head info
-  // (written by compaction or by the finish that built list 1, both complete
-  // before the partial pass began).
-  const int4 hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
+  // (written by compaction or by the finish that built list 1).  The kernel
+  // before this one is the call's partial pass, which triggers this launch
+  // only after its own dependency wait, so all of them are complete.
+  int4 hi;
+  if (kp.dense_list) {  // every range of the row is one item
+    const int nr = (nb + kp.T - 1) / kp.T;
+    hi = make_int4(rg * kp.S_max, nr, nb, nr);
+  } else {
+    hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
+  }
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching
   // The mask words the call starts from (the group's first CTA): union-discover
@@ -498,9 +505,16 @@ __global__ void __launch_bounds__(256)
   uint32_t* const mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // the pair's mask, or null
   const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
   // Read before the dependency wait: the head info (written by compaction or
-  // by the finish that built list 1, both complete before the partial pass
-  // began).
-  const int4 hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
+  // by the finish that built list 1).  The kernel before this one is the
+  // call's partial pass, which triggers this launch only after its own
+  // dependency wait, so it is complete.
+  int4 hi;
+  if (kp.dense_list) {  // every range of the row is one item
+    const int nr = (nb + kp.T - 1) / kp.T;
+    hi = make_int4(rg * kp.S_max, nr, nb, nr);
+  } else {
+    hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
+  }
   if (threadIdx.x < 2) smask[threadIdx.x] = 0u;
   grid_dependency_wait();    // the partial pass's results
   grid_dependents_launch();  // the next call's compaction may start launching

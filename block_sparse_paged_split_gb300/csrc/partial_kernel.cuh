@@ -85,7 +85,11 @@ struct PartialCfg {
   static constexpr int EXTRA_BYTES =
       ((DESC_BYTES + BAR_BYTES + PBUF_BYTES + STAGE_ALIGN - 1) / STAGE_ALIGN) * STAGE_ALIGN;
   static constexpr int CONSUMER_BYTES = RING_BYTES + EXTRA_BYTES;
-  static constexpr int SMEM_BYTES = C * CONSUMER_BYTES;
+  // The dense list's per-row table (WISE_FLAG_DENSE_LIST): first item and
+  // length | mode flags of every row, after the consumers' regions.
+  static constexpr int TAB_OFF = C * CONSUMER_BYTES;
+  static constexpr int TAB_BYTES = ((2 * kMaxDenseRows + 1) * 4 + 127) / 128 * 128;
+  static constexpr int SMEM_BYTES = TAB_OFF + TAB_BYTES;
   static constexpr int THREADS = 2 * C * 32;  // C consumer warps, C producer warps
 };
 
@@ -494,13 +498,76 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   // prefetch returns no data, so it may run before the dependency wait).
   prefetch_l2(page_table, (size_t)kp.R * kp.max_pages * sizeof(int32_t));
   prefetch_l2(q, (size_t)kp.R * kp.Hq * D * sizeof(T));
+  // The dense list: every range of T blocks of every row is an item, ordered
+  // by row, then KV head, then range; warp 0 tabulates each row's first item
+  // (a prefix over the rows' Hkv * ceil(ceil(L / 32) / T) items) and its
+  // length and mode flags, so a claim maps to its item with no record load.
+  // Every row's two loads go out at once.
+  int* tab_start = reinterpret_cast<int*>(smem + Cfg::TAB_OFF);  // [R + 1]
+  int* tab_w = tab_start + kMaxDenseRows + 1;                      // [R]
+  bool clamped = false;
+  auto build_table = [&]() {
+    constexpr int kChunks = kMaxDenseRows / 32;
+    int raw[kChunks], md[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+      const int r = j * 32 + lane;
+      raw[j] = r < kp.R ? seq_lens[r] : 0;
+      md[j] = r < kp.R ? (int)modes[r] : 0;
+    }
+    int carry = 0;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+      if (j * 32 < kp.R) {
+        const int r = j * 32 + lane;
+        const int L = clamp_len(raw[j], kp.cap_tokens);
+        const int nb = (L + kTile - 1) / kTile;
+        const int items = r < kp.R ? kp.Hkv * ((nb + kp.T - 1) / kp.T) : 0;
+        clamped |= raw[j] > kp.cap_tokens;
+        int incl = items;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (r < kp.R) {
+          tab_start[r] = carry + incl - items;
+          tab_w[r] = L | ((md[j] == WISE_MODE_DISCOVER || md[j] == WISE_MODE_DISCOVER_UNION)
+                              ? kItemDiscover : 0);
+        }
+        carry += __shfl_sync(kFull, incl, 31);
+      }
+    }
+    if (lane == 0) tab_start[kp.R] = carry;
+  };
+  // With the caller's inputs complete before the previous kernel began
+  // (WISE_FLAG_INPUTS_READY), the table is built before the dependency wait,
+  // and the producers issue their first item's copies (page table, K and V:
+  // caller inputs the library never writes) while that kernel still runs,
+  // waiting only before their first access to the workspace (the queue); the
+  // consumers wait here, before they write.
+  const bool early_table = kp.dense_list && kp.inputs_ready;
+  if (early_table && warp == 0) build_table();
   __syncthreads();
   // Compaction's items, schedule and counters.  An early-start launch (the
   // previous kernel writes nothing it reads and reads nothing it writes; the
   // compaction it uses completed before that kernel began) skips the wait
   // here and waits before it exits instead, so its completion still implies
   // the previous kernel's.
-  if (!kp.early) grid_dependency_wait();
+  const bool producer_defers = early_table && warp >= C;
+  if (!kp.early && !producer_defers) grid_dependency_wait();
+  if (kp.dense_list && !kp.inputs_ready) {
+    if (warp == 0) build_table();
+    __syncthreads();
+  }
+  // A dense-list pass has no compaction to clear the status word: block 0
+  // clears it once the previous kernel (which may flag into it) is done, then
+  // flags a clamped length.
+  if (kp.dense_list && blockIdx.x == 0 && warp == 0) {
+    if (lane == 0) *ws.status = 0;
+    __syncwarp();
+    if (__any_sync(kFull, clamped) && lane == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
+  }
 
   if (warp >= C) {
     // ------------------------------------------------------------ producers
@@ -531,6 +598,24 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     const int first_slot = blockIdx.x * C + c;
     int l1s[kMaxT];  // list 1: schedule position of the first item with j + 1 tiles
     auto record_at = [&](int slot) -> int4 {
+      if (kp.dense_list) {
+        // The row: the last one whose first item is at or before the slot
+        // (an empty row shares its start with the next row, which wins).
+        int lo = 0, hi = kp.R - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (tab_start[mid] <= slot) lo = mid;
+          else hi = mid - 1;
+        }
+        const int w = tab_w[lo];
+        const int nb = ((w & kItemLenMask) + kTile - 1) / kTile;
+        const int nr = (nb + kp.T - 1) / kp.T;
+        const int local = slot - tab_start[lo];
+        const int g = local / nr, s_rng = local - g * nr;
+        const int n = min(kp.T, nb - s_rng * kp.T);
+        return make_int4(lo * kp.Hkv + g, s_rng | (s_rng << 16),
+                         (int)(((1u << n) - 1u) | ((unsigned)n << 16)), w);
+      }
       if (!kp.list1) return ws.items[slot];
       // Bucket j holds schedule positions [l1s[j], l1s[j - 1]) (l1s is
       // non-increasing in j and l1s[T - 1] = 0): the smallest j with
@@ -565,7 +650,10 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     };
     int n_items;
     int4 first_rec = make_int4(0, 0, 0, 0);
-    if (kp.list1) {
+    if (kp.dense_list) {
+      n_items = tab_start[kp.R];
+      if (first_slot < n_items) first_rec = record_at(first_slot);
+    } else if (kp.list1) {
       // Schedule position of each bucket: the items of larger buckets first.
       int cnt[kMaxT];
 #pragma unroll
@@ -583,6 +671,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       n_items = min(*ws.num_items, ws.max_items);
     }
     bool timed_out = false;
+    bool waited = !producer_defers;  // the dependency wait is behind this lane
     while (true) {
       if (!cur_ok && nxt_ok) {
         cur = nxt;
@@ -595,6 +684,10 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // consumers could start sooner (measured: claiming at four tiles left
       // is 0.9% slower, at one 0.5% faster than at two).
       if (!nxt_ok && !exhausted && (!cur_ok || __popc((unsigned)cur.z & 0xffffu) - k <= 1)) {
+        if (!first_claim && !waited) {
+          grid_dependency_wait();
+          waited = true;
+        }
         const int slot = first_claim ? first_slot : n_consumers + atomicAdd(ws.queue, 1);
         if (slot < n_items) {
           nxt = first_claim ? first_rec : record_at(slot);
@@ -647,8 +740,15 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       }
       if (!p.ok && (cur_ok || nxt_ok || !exhausted)) continue;
       // Wait for the stage (bounded), then issue the prepared tile or, with
-      // nothing left, the end marker.
+      // nothing left, the end marker.  A stage is reused only once the
+      // consumer frees it, which it does past its dependency wait: a deferring
+      // producer takes that wait first, so the bounded wait below never
+      // counts the previous kernel's run time.
       const int stage = seq % S;
+      if (seq >= (uint32_t)S && !waited) {
+        grid_dependency_wait();
+        waited = true;
+      }
       if (!mbar_wait(empty_bar(c, stage), ((seq / S) & 1) ^ 1)) {
         flag_error(ws.status, WISE_DEVERR_WAIT_TIMEOUT);
         timed_out = true;
@@ -699,6 +799,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       ++seq;
       p.ok = false;
     }
+    if (!waited) grid_dependency_wait();  // before the counters below
     // This CTA's last producer past the queue tells the grid; the last CTA
     // puts the counter back to 0, so a later partial launch over the same
     // compaction (the next depth reusing a mask) starts afresh.

@@ -105,6 +105,7 @@ def library() -> ctypes.CDLL:
         sigs = {
             "wise_workspace_bytes": [S, ctypes.POINTER(ctypes.c_size_t)],
             "wise_workspace_layout": [S, ctypes.POINTER(wise_layout)],
+            "wise_workspace_reset": [S, P, SZ, P],
             "wise_compact_tiles": [S, P, P, P, P, SZ, P],
             "wise_decode_partial": [S, P, P, P, P, P, P, P, SZ, P],
             "wise_decode_finish": [S, P, P, P, SZ, P, P, P, P],
@@ -189,6 +190,11 @@ def wise_workspace_layout(shape: wise_shape) -> Dict[str, int]:
     return {name: getattr(lay, name) for name, _ in wise_layout._fields_}
 
 
+def wise_workspace_reset(shape: wise_shape, workspace: torch.Tensor, stream=None) -> None:
+    _check(library().wise_workspace_reset(ctypes.byref(shape), _ptr(workspace, torch.uint8, "workspace"),
+                                          workspace.numel(), _stream(stream)))
+
+
 def alloc_workspace(shape: wise_shape, device=None) -> torch.Tensor:
     """A workspace of the right size (torch allocations are 256-byte aligned)."""
     return torch.empty(wise_workspace_bytes(shape), dtype=torch.uint8,
@@ -225,12 +231,15 @@ FLAG_SLOT_SET_1 = 1
 FLAG_EARLY_START = 2
 FLAG_BUILD_SPARSE_LIST = 4
 FLAG_SPARSE_LIST = 8
+FLAG_DENSE_LIST = 16
+FLAG_INPUTS_READY = 32
+DENSE_LIST_MAX_ROWS = 256
 
 
 def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                            flags=0, stream=None) -> None:
     """flags: FLAG_SLOT_SET_1, FLAG_EARLY_START, FLAG_SPARSE_LIST (modes may
-    then be None)."""
+    then be None), FLAG_DENSE_LIST, FLAG_INPUTS_READY."""
     e = _elem(shape)
     _check(library().wise_decode_partial_ex(
         ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
@@ -242,7 +251,7 @@ def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, mod
 def wise_decode_finish_ex(shape, modes, seq_lens, workspace, support, out, lse, flags=0,
                           stream=None) -> None:
     """flags: FLAG_SLOT_SET_1, FLAG_BUILD_SPARSE_LIST, FLAG_SPARSE_LIST (modes
-    may then be None)."""
+    may then be None), FLAG_DENSE_LIST."""
     e = _elem(shape)
     _check(library().wise_decode_finish_ex(
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),

@@ -206,6 +206,13 @@ typedef struct {
  * only; enqueues nothing.  `bytes` is a host pointer. */
 wise_status wise_workspace_bytes(const wise_shape *shape, size_t *bytes);
 
+/* Zeroes the workspace header (status word, item count, queue counters,
+ * list-1 counters): asynchronously on `stream`, allocating nothing.  A new
+ * workspace needs it (or a wise_compact_tiles) before its first call with
+ * WISE_FLAG_DENSE_LIST. */
+wise_status wise_workspace_reset(const wise_shape *shape, void *workspace,
+                                 size_t workspace_bytes, wise_stream_t stream);
+
 /* Region offsets for this shape (host only). `layout` is a host pointer. */
 wise_status wise_workspace_layout(const wise_shape *shape,
                                   wise_layout *layout);
@@ -280,12 +287,38 @@ enum {
    * (written by an earlier finish with WISE_FLAG_BUILD_SPARSE_LIST over the
    * same rows and lengths); modes is ignored and may be NULL.  Both passes of
    * the call take the flag.  Not with wise_decode_partial_finish. */
-  WISE_FLAG_SPARSE_LIST = 8u
+  WISE_FLAG_SPARSE_LIST = 8u,
+  /* Partial pass and finish: every row attends every block below its length
+   * (sparse rows too), discover and discover-union rows (by modes) also
+   * record and select; the work list is derived from seq_lens by the passes
+   * themselves, so no wise_compact_tiles runs [WISE PR, "What changes": the
+   * compaction only matters to sparse rows; a dense row's tiles are all of
+   * them].  At most WISE_DENSE_LIST_MAX_ROWS rows (else
+   * WISE_ERR_UNSUPPORTED).  Both passes of the call take the flag; the
+   * partial pass clears the workspace status word.  The workspace's queue
+   * counters must be 0, as every compaction and every completed partial pass
+   * leave them (wise_workspace_reset zeroes a new workspace).  Not with
+   * WISE_FLAG_SPARSE_LIST, WISE_FLAG_EARLY_START or
+   * wise_decode_partial_finish. */
+  WISE_FLAG_DENSE_LIST = 16u,
+  /* Partial pass: the caller's inputs (q, the K/V pools, the page table,
+   * lengths and modes) were complete before the kernel ahead of this launch
+   * in the stream began -- as when that kernel is a pass of this library.
+   * A pass on the dense list then builds its item table and issues its
+   * first copies while that kernel still runs.  Without the flag every read
+   * waits for the previous kernel (a programmatic dependent launch sees that
+   * kernel's writes only past its dependency wait).  Only the dense list
+   * uses it; other passes accept and ignore it. */
+  WISE_FLAG_INPUTS_READY = 32u
 };
 
+/* Rows a call with WISE_FLAG_DENSE_LIST takes (its table lives in the
+ * partial pass's shared memory). */
+#define WISE_DENSE_LIST_MAX_ROWS 256
+
 /* wise_decode_partial with flags (WISE_FLAG_SLOT_SET_1, WISE_FLAG_EARLY_START,
- * WISE_FLAG_SPARSE_LIST); flags = 0 is wise_decode_partial.  Unknown flags:
- * WISE_ERR_INVALID_ARG. */
+ * WISE_FLAG_SPARSE_LIST, WISE_FLAG_DENSE_LIST, WISE_FLAG_INPUTS_READY); flags = 0
+ * is wise_decode_partial.  Unknown flags: WISE_ERR_INVALID_ARG. */
 wise_status wise_decode_partial_ex(const wise_shape *shape, const void *q,
                                    const void *k_cache, const void *v_cache,
                                    const int32_t *page_table, const int32_t *seq_lens,
@@ -294,8 +327,8 @@ wise_status wise_decode_partial_ex(const wise_shape *shape, const void *q,
                                    wise_stream_t stream);
 
 /* wise_decode_finish with flags (WISE_FLAG_SLOT_SET_1,
- * WISE_FLAG_BUILD_SPARSE_LIST, WISE_FLAG_SPARSE_LIST); flags = 0 is
- * wise_decode_finish. */
+ * WISE_FLAG_BUILD_SPARSE_LIST, WISE_FLAG_SPARSE_LIST, WISE_FLAG_DENSE_LIST);
+ * flags = 0 is wise_decode_finish. */
 wise_status wise_decode_finish_ex(const wise_shape *shape, const int8_t *modes,
                                   const int32_t *seq_lens, void *workspace,
                                   size_t workspace_bytes, uint32_t flags,

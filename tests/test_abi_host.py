@@ -124,7 +124,10 @@ def test_flag_checks(lib):
     P = ctypes.c_void_p
     # unknown partial flags, and a partial-only flag given to the finish
     st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
-                                    P(4096), n, ctypes.c_uint32(16), None)
+                                    P(4096), n, ctypes.c_uint32(1 << 10), None)
+    assert st == 1 and b"flags" in lib.wise_last_error()
+    st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                   ctypes.c_uint32(1 << 10), P(16), P(16), P(16), None)
     assert st == 1 and b"flags" in lib.wise_last_error()
     st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
                                     P(4096), n, ctypes.c_uint32(W.FLAG_BUILD_SPARSE_LIST), None)
@@ -156,6 +159,46 @@ def test_flag_checks(lib):
     assert lay["head_info_1"] % 256 == 0 and lay["items_1"] % 256 == 0
     assert lay["head_info_1"] > max(second) and lay["items_1"] >= lay["head_info_1"] + 4 * 2 * 16
     assert lay["total_bytes"] >= lay["items_1"] + 8 * lay["max_items"] * 16
+
+
+def test_dense_list_checks(lib):
+    """WISE_FLAG_DENSE_LIST: at most DENSE_LIST_MAX_ROWS rows, and neither
+    with list 1, an early start nor the folded finish; checked on the host
+    before anything is enqueued."""
+    P = ctypes.c_void_p
+    D = ctypes.c_uint32(W.FLAG_DENSE_LIST)
+    big = _shape(num_rows=W.DENSE_LIST_MAX_ROWS + 1)
+    nb = W.wise_workspace_bytes(big)
+    assert lib.wise_decode_partial_ex(ctypes.byref(big), P(16), P(16), P(16), P(16), P(16), P(16),
+                                      P(4096), nb, D, None) == 2  # WISE_ERR_UNSUPPORTED
+    assert b"rows" in lib.wise_last_error()
+    assert lib.wise_decode_finish_ex(ctypes.byref(big), P(16), P(16), P(4096), nb, D, None,
+                                     P(16), P(16), None) == 2
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    for flags in (W.FLAG_DENSE_LIST | W.FLAG_SPARSE_LIST, W.FLAG_DENSE_LIST | W.FLAG_EARLY_START):
+        st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
+                                        P(4096), n, ctypes.c_uint32(flags), None)
+        assert st == 1, flags
+    st = lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n,
+                                   ctypes.c_uint32(W.FLAG_DENSE_LIST | W.FLAG_SPARSE_LIST),
+                                   None, P(16), P(16), None)
+    assert st == 1
+    assert W.DENSE_LIST_MAX_ROWS == 256
+
+
+def test_workspace_reset_checks(lib):
+    """wise_workspace_reset checks the shape and the workspace (NULL, too
+    small, misaligned) before it enqueues anything."""
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    P = ctypes.c_void_p
+    assert lib.wise_workspace_reset(ctypes.byref(s), None, n, None) == 3  # WISE_ERR_WORKSPACE
+    assert lib.wise_workspace_reset(ctypes.byref(s), P(4096), n - 1, None) == 3
+    assert b"too small" in lib.wise_last_error()
+    assert lib.wise_workspace_reset(ctypes.byref(s), P(4096 + 16), n, None) == 3
+    bad = _shape(head_dim=96)
+    assert lib.wise_workspace_reset(ctypes.byref(bad), P(4096), n, None) == 2
 
 
 def test_noalloc_status_rejects_a_null_pointer(lib):
