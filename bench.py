@@ -430,7 +430,8 @@ class Pipeline:
         # A list-derived pass needs the workspace's queue counters at 0.
         W.wise_workspace_reset(self.shape, self.ws)
 
-        def calls(modes_t, t, compact=True, early=False, build=False, on_list=False, dense=False):
+        def calls(modes_t, t, compact=True, early=False, build=False, on_list=False, dense=False,
+                  list_ready=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
@@ -447,9 +448,12 @@ class Pipeline:
                 return c
             if on_list:
                 f = W.FLAG_SPARSE_LIST
+                # A call after the first on the list reads a list built two or
+                # more kernels back, and inputs no kernel of the step writes.
+                pf = f | (W.FLAG_INPUTS_READY if list_ready else 0)
                 c.append(("partial", lib.wise_decode_partial_ex,
                           (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
-                           pt, sl, m, ws, nws, f, st)))
+                           pt, sl, m, ws, nws, pf, st)))
                 c.append(("finish", lib.wise_decode_finish_ex,
                           (S, m, sl, ws, nws, f, sup, self.out[t].data_ptr(),
                            self.lse[t].data_ptr(), st)))
@@ -527,6 +531,7 @@ class Pipeline:
         self.wise_step = []
         listed = False  # list 1 holds the work list of an all-sparse depth on the current mask
         list0 = False   # the compacted list holds the previous depth's work list
+        prev_on_list = False  # the previous depth ran on list 1
         for t in range(w.num_depths):
             dm = w.depth_modes
             reuse = list0 and same_work_list(dm[t], dm[t - 1])
@@ -538,11 +543,14 @@ class Pipeline:
             build = (self.sparse_list and not all_sparse(dm[t]) and t + 1 < w.num_depths and
                      all_sparse(dm[t + 1]))
             dense = self.dense_list and not any(int(x) == W.MODE_SPARSE for x in dm[t])
+            list_ready = on_list and prev_on_list
+            prev_on_list = on_list
             listed = build or on_list
             if on_list or build or dense:
                 self.wise_step.append((t, depth_name(dm[t]),
                                        calls(self.modes[t], t, compact=not reuse and not dense,
-                                             build=build, on_list=on_list, dense=dense)))
+                                             build=build, on_list=on_list, dense=dense,
+                                             list_ready=list_ready)))
                 list0 = build and not dense
                 continue
             list0 = True

@@ -512,8 +512,8 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) {
       const int r = j * 32 + lane;
-      raw[j] = r < kp.R ? seq_lens[r] : 0;
-      md[j] = r < kp.R ? (int)modes[r] : 0;
+      raw[j] = r < kp.R ? __ldcg(seq_lens + r) : 0;
+      md[j] = r < kp.R ? (int)__ldcg(modes + r) : 0;
     }
     int carry = 0;
 #pragma unroll
@@ -540,21 +540,22 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
     }
     if (lane == 0) tab_start[kp.R] = carry;
   };
-  // With the caller's inputs complete before the previous kernel began
-  // (WISE_FLAG_INPUTS_READY), the table is built before the dependency wait,
-  // and the producers issue their first item's copies (page table, K and V:
-  // caller inputs the library never writes) while that kernel still runs,
-  // waiting only before their first access to the workspace (the queue); the
-  // consumers wait here, before they write.
-  const bool early_table = kp.dense_list && kp.inputs_ready;
-  if (early_table && warp == 0) build_table();
+  // With everything the pass reads complete before the previous kernel began
+  // (WISE_FLAG_INPUTS_READY: the caller's inputs, and on list 1 the list),
+  // the table is built before the dependency wait, and the producers take
+  // their first item (from the table, or list 1's counters and records) and
+  // issue its copies (page table, K and V) while that kernel still runs,
+  // waiting only before the queue claims and the first reuse of a stage; the
+  // consumers wait here, before they write.  Those early reads bypass L1.
+  const bool early_reads = (kp.dense_list || kp.list1) && kp.inputs_ready;
+  if (early_reads && kp.dense_list && warp == 0) build_table();
   __syncthreads();
   // Compaction's items, schedule and counters.  An early-start launch (the
   // previous kernel writes nothing it reads and reads nothing it writes; the
   // compaction it uses completed before that kernel began) skips the wait
   // here and waits before it exits instead, so its completion still implies
   // the previous kernel's.
-  const bool producer_defers = early_table && warp >= C;
+  const bool producer_defers = early_reads && warp >= C;
   if (!kp.early && !producer_defers) grid_dependency_wait();
   if (kp.dense_list && !kp.inputs_ready) {
     if (warp == 0) build_table();
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         }
       const int idx = slot - base;
       if (idx < 0 || idx >= ws.max_items) return make_int4(-1, 0, 0, 0);  // rejected below
-      return ws.items_1[(size_t)jsel * ws.max_items + idx];
+      return __ldcg(ws.items_1 + (size_t)jsel * ws.max_items + idx);
     };
     // A record the library did not write for this shape (a call out of
     // order on the workspace) is flagged and skipped, never followed.
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // Schedule position of each bucket: the items of larger buckets first.
       int cnt[kMaxT];
 #pragma unroll
-      for (int j = 0; j < kMaxT; ++j) cnt[j] = j < kp.T ? ws.l1_counter[j] : 0;
+      for (int j = 0; j < kMaxT; ++j) cnt[j] = j < kp.T ? __ldcg(ws.l1_counter + j) : 0;
       int pos = 0;
 #pragma unroll
       for (int j = kMaxT - 1; j >= 0; --j) {
@@ -682,8 +683,12 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // Claim the next item only when the current one is about to run out
       // (one tile left to prepare): claiming earlier would hoard items other
       // consumers could start sooner (measured: claiming at four tiles left
-      // is 0.9% slower, at one 0.5% faster than at two).
-      if (!nxt_ok && !exhausted && (!cur_ok || __popc((unsigned)cur.z & 0xffffu) - k <= 1)) {
+      // is 0.9% slower, at one 0.5% faster than at two).  List 1 holds small
+      // items (a few selected tiles each), whose claim, record and page-table
+      // round trips one tile does not cover: there the claim goes out two
+      // tiles ahead (measured: sparse partial 22.9 vs 23.6 µs, step -0.35%).
+      if (!nxt_ok && !exhausted &&
+          (!cur_ok || __popc((unsigned)cur.z & 0xffffu) - k <= (kp.list1 ? 2 : 1))) {
         if (!first_claim && !waited) {
           grid_dependency_wait();
           waited = true;
@@ -712,8 +717,8 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
         auto load_pages = [&](int blk, int (&pg)[2]) {
           const int32_t* pt = page_table + (size_t)row * kp.max_pages + blk * (kTile / kp.P);
           const bool two = kp.P * 2 == kTile && blk * kTile + kp.P < L;
-          pg[0] = pt[0];
-          pg[1] = two ? pt[1] : 0;
+          pg[0] = __ldcg(pt);
+          pg[1] = two ? __ldcg(pt + 1) : 0;
         };
         if (ahead_ok) {
           p.pages[0] = ahead[0];

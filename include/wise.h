@@ -301,14 +301,16 @@ enum {
    * WISE_FLAG_SPARSE_LIST, WISE_FLAG_EARLY_START or
    * wise_decode_partial_finish. */
   WISE_FLAG_DENSE_LIST = 16u,
-  /* Partial pass: the caller's inputs (q, the K/V pools, the page table,
-   * lengths and modes) were complete before the kernel ahead of this launch
-   * in the stream began -- as when that kernel is a pass of this library.
-   * A pass on the dense list then builds its item table and issues its
-   * first copies while that kernel still runs.  Without the flag every read
-   * waits for the previous kernel (a programmatic dependent launch sees that
-   * kernel's writes only past its dependency wait).  Only the dense list
-   * uses it; other passes accept and ignore it. */
+  /* Partial pass: everything the pass reads was complete before the kernel
+   * ahead of this launch in the stream began: the caller's inputs (q, the
+   * K/V pools, the page table, lengths and modes) -- as when that kernel is
+   * a pass of this library -- and, with WISE_FLAG_SPARSE_LIST, list 1 (the
+   * call is not the first on the list since the finish that built it).  A
+   * pass on the dense list or on list 1 then takes its first items and
+   * issues their copies while that kernel still runs.  Without the flag
+   * every read waits for the previous kernel (a programmatic dependent
+   * launch sees that kernel's writes only past its dependency wait).  Other
+   * passes accept and ignore it. */
   WISE_FLAG_INPUTS_READY = 32u
 };
 

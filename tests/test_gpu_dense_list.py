@@ -90,8 +90,9 @@ def test_dense_list_equals_compaction_bitwise(Hq, Hkv, D, dtype, T, ready):
 def test_step_without_compaction(Hq, Hkv, D, dtype):
     """The benchmark's WISE step with no compaction launch: discover on the
     dense list, union-discover on the dense list building list 1, two sparse
-    depths on list 1; twice on one workspace.  Bitwise against the same calls
-    each after its own compaction, and depth 2 against the oracle."""
+    depths on list 1 (the second reading early); twice on one workspace.
+    Bitwise against the same calls each after its own compaction, and depth 2
+    against the oracle."""
     w = _wl(Hq, Hkv, D, dtype)
     b = Batch(w)
     R = w.num_rows
@@ -102,15 +103,18 @@ def test_step_without_compaction(Hq, Hkv, D, dtype):
     for rep in range(2):
         sup.zero_()
         outs = []
+        # The second call on list 1 reads the list and its inputs before the
+        # dependency wait (both complete before the kernel ahead of it began).
         for depth, mode, kind in ((0, W.MODE_DISCOVER, "dense"), (1, W.MODE_DISCOVER_UNION, "build"),
-                                  (2, W.MODE_SPARSE, "list1"), (0, W.MODE_SPARSE, "list1")):
+                                  (2, W.MODE_SPARSE, "list1"), (0, W.MODE_SPARSE, "list1-ready")):
             m = np.full(R, mode, np.int8)
-            if kind == "list1":
+            if kind.startswith("list1"):
                 d = b.dev(depth)
                 out = torch.empty_like(d["q"])
                 lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+                pf = W.FLAG_SPARSE_LIST | (W.FLAG_INPUTS_READY if kind == "list1-ready" else 0)
                 W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
-                                         b.seq_lens, None, ws, W.FLAG_SPARSE_LIST)
+                                         b.seq_lens, None, ws, pf)
                 W.wise_decode_finish_ex(shape, None, b.seq_lens, ws, sup, out, lse,
                                         flags=W.FLAG_SPARSE_LIST)
             else:
