@@ -976,6 +976,39 @@ def sweep_workload(name, args, steps, peak):
     return out
 
 
+ETA_SWEEP = (0.8, 0.9, 0.95, 0.99)
+
+
+def eta_point(name, eta, args, steps):
+    """One point of the eta sweep: the WISE step's and the dense step's
+    graph-replay times and the reused-union density the sparse depths
+    attend, for one selection threshold."""
+    import torch
+    from block_sparse_paged_split_gb300.workload import make_workload
+    w = make_workload(name, eta=eta)
+    pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
+                    device_inputs=True, dense_list=not args.no_dense_list)
+    for _ in range(3):
+        pipe.run(pipe.wise_step)
+    torch.cuda.synchronize()
+    sparse_t = [t for t in range(w.num_depths) if any(int(x) == 3 for x in w.depth_modes[t])]
+    density = pipe.support_density(w.depth_modes[sparse_t[0]]) if sparse_t else None
+    g, gd = pipe.graph(pipe.wise_step), pipe.graph(pipe.dense_step)
+    for _ in range(3):
+        g.replay()
+        gd.replay()
+    ms = graph_region(pipe, g, steps, None)
+    ms_dense = graph_region(pipe, gd, steps, None)
+    out = {"eta": eta, "support_density_blocks": round(density, 4) if density is not None else None,
+           "step_ms": round(ms / steps, 4), "dense_step_ms": round(ms_dense / steps, 4),
+           "speedup_vs_dense": round(ms_dense / ms, 3),
+           "launches": steps * (pipe.launches_per_step(pipe.wise_step) +
+                                pipe.launches_per_step(pipe.dense_step))}
+    del g, gd, pipe
+    torch.cuda.empty_cache()
+    return out
+
+
 def pipe_depth_names(pipe):
     return [f"{mode}" + ("" if not any(c[0] == "compact" for c in calls) else "+compact")
             for _, mode, calls in pipe.wise_step]
@@ -1105,6 +1138,13 @@ def main_ours(args):
         sweep_steps = max(5, min(args.steps, 50))
         sclock = ClockSampler(local)
         sweep = {name: sweep_workload(name, args, sweep_steps, peak) for name in SWEEP}
+        # The GQA workload over the selection threshold: the step against
+        # the reused-union density it leaves the sparse depths.
+        if "gqa_32k" in sweep and args.eta is None:
+            pts = [eta_point("gqa_32k", e, args, sweep_steps) for e in ETA_SWEEP]
+            for pt in pts:
+                launches += pt.pop("launches")
+            sweep["gqa_32k"]["eta_sweep"] = pts
         sweep_clocks = sclock.stop()
         for name, res in sweep.items():
             launches += 2 * sweep_steps * res.pop("launches_per_step")
@@ -1174,7 +1214,9 @@ def main_ours(args):
         result["config"]["sweep"] = (f"after the headline: {', '.join(SWEEP)}, each with its WISE "
                                      f"and dense steps replayed from CUDA graphs "
                                      f"({sweep_steps} steps) and launched eagerly for the "
-                                     f"per-mode table; K/V drawn on the device")
+                                     f"per-mode table; K/V drawn on the device; gqa_32k also "
+                                     f"at eta {', '.join(str(e) for e in ETA_SWEEP)} "
+                                     f"(graph replays only)")
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_oracle_sample(args.workload, rows=16, eta=args.eta)
     if rank == 0:

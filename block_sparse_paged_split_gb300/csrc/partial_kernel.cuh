@@ -683,12 +683,14 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // Claim the next item only when the current one is about to run out
       // (one tile left to prepare): claiming earlier would hoard items other
       // consumers could start sooner (measured: claiming at four tiles left
-      // is 0.9% slower, at one 0.5% faster than at two).  List 1 holds small
-      // items (a few selected tiles each), whose claim, record and page-table
-      // round trips one tile does not cover: there the claim goes out two
-      // tiles ahead (measured: sparse partial 22.9 vs 23.6 µs, step -0.35%).
+      // is 0.9% slower, at one 0.5% faster than at two).  Small items of
+      // list 1 (a few selected tiles each) need their claim, record and
+      // page-table round trips started earlier than one tile covers: there
+      // the claim goes out two tiles ahead (measured at 1K: sparse partial
+      // 22.9 vs 23.6 µs, step -0.35%).
+      const int cur_tiles = __popc((unsigned)cur.z & 0xffffu);
       if (!nxt_ok && !exhausted &&
-          (!cur_ok || __popc((unsigned)cur.z & 0xffffu) - k <= (kp.list1 ? 2 : 1))) {
+          (!cur_ok || cur_tiles - k <= (kp.list1 && cur_tiles <= 4 ? 2 : 1))) {
         if (!first_claim && !waited) {
           grid_dependency_wait();
           waited = true;

@@ -60,9 +60,19 @@ def test_gpu_arm_line():
         for mode, row in res["modes"].items():
             assert row["call_us"] >= row["partial_us"] > 0, (name, mode)
             assert 0 < row["call_frac_of_measured_hbm"] <= row["partial_frac_of_measured_hbm"]
-    # the sparse depths of the headline step run on the list the union depth built
+    # the grouped-query workload over the selection threshold: a lower eta
+    # leaves the sparse depths fewer blocks
+    pts = sweep["gqa_32k"]["eta_sweep"]
+    assert [p["eta"] for p in pts] == [0.8, 0.9, 0.95, 0.99]
+    dens = [p["support_density_blocks"] for p in pts]
+    assert all(0 < d <= 1 for d in dens) and dens == sorted(dens)
+    assert all(p["step_ms"] > 0 and p["dense_step_ms"] > 0 for p in pts)
+    # no depth of the headline step launches a compaction: the sparse depths
+    # run on the list the union depth built, the others on the dense list
     assert "no compaction launch" in out["config"]["workload"]
-    assert "compact" not in out["modes"]["depth2_sparse"]["kernels_us"]
+    for mode, row in out["modes"].items():
+        if mode.startswith("depth"):
+            assert "compact" not in row["kernels_us"], mode
 
 
 @pytest.mark.gpu
