@@ -88,10 +88,13 @@ def test_slot_pool_equals_gathered_masks(Hq, Hkv):
                 assert np.array_equal(after[sl, ly], pool_np[sl, ly]), (sl, ly)
 
 
-def test_slot_pool_through_list1():
+@pytest.mark.parametrize("dense", [False, True])
+def test_slot_pool_through_list1(dense):
     """Discover, union-discover building list 1, then a sparse call on list 1,
-    all on the slot pool: equal to the gathered-mask calls, bit for bit; list
-    1's items partition the oracle's lists of the slot masks."""
+    all on the slot pool: equal to the gathered-mask calls (after their own
+    compaction), bit for bit; list 1's items partition the oracle's lists of
+    the slot masks.  dense: the two discovery depths on the dense list (no
+    compaction at all on the pool side)."""
     w, pool_np, row_slot = _setup(4, 4, seed=73)
     b = Batch(w)
     R = w.num_rows
@@ -100,20 +103,24 @@ def test_slot_pool_through_list1():
     disc = torch.full((R,), W.MODE_DISCOVER, dtype=torch.int8, device="cuda")
     union = torch.full((R,), W.MODE_DISCOVER_UNION, dtype=torch.int8, device="cuda")
 
-    def run(mask_of_call, flat: bool):
+    def run(mask_of_call, flat: bool, dense_list: bool = False):
         ws = W.alloc_workspace(shape)
+        W.wise_workspace_reset(shape, ws)
         outs = []
         for depth, m, flags in ((0, disc, 0), (1, union, W.FLAG_BUILD_SPARSE_LIST),
                                 (2, None, W.FLAG_SPARSE_LIST)):
             d = b.dev(depth)
             out = torch.empty_like(d["q"])
             lse = torch.empty((R, 4), dtype=torch.float32, device="cuda")
-            if depth == 0:
+            on_dense = dense_list and depth < 2
+            if depth == 0 and not on_dense:
                 if flat:
                     W.wise_compact_tiles(shape, m, b.seq_lens, mask_of_call, ws)
                 else:
                     W.wise_compact_tiles_m(shape, m, b.seq_lens, mask_of_call, ws)
-            pflags = flags & W.FLAG_SPARSE_LIST
+            if on_dense:
+                flags |= W.FLAG_DENSE_LIST
+            pflags = flags & (W.FLAG_SPARSE_LIST | W.FLAG_DENSE_LIST)
             W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
                                      b.seq_lens, m, ws, pflags)
             if flat:
@@ -125,7 +132,7 @@ def test_slot_pool_through_list1():
         return outs, {k: v.cpu() for k, v in W.workspace_views(shape, ws).items()}
 
     pool = dev_support(pool_np)
-    a, va = run(W.make_mask(pool, slots_t, LAYER), flat=False)
+    a, va = run(W.make_mask(pool, slots_t, LAYER), flat=False, dense_list=dense)
     sup = dev_support(_gathered(pool_np, row_slot))
     bb, vb = run(sup, flat=True)
     # Depths 0 and 1 discover (their outputs do not depend on the mask); at
