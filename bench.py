@@ -674,8 +674,10 @@ def timed_region(pipe, step, K, dist, with_events=True):
     torch.cuda.synchronize()
     events = [] if with_events else None
     marks = []
+    spin = getattr(torch.cuda, "_sleep", None)  # torch's spin kernel (present in 2.9 and 2.11)
     for _ in range(K):
-        torch.cuda._sleep(LEAD_CYCLES)
+        if spin is not None:
+            spin(LEAD_CYCLES)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(pipe.stream)
