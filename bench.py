@@ -210,12 +210,21 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "partial_kernel_traffic.json")
 KERNEL_SOURCES = ("partial_kernel.cuh", "partial_bf16.cu", "finish_short.cuh", "common.cuh", "internal.h")
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without comments and with whitespace collapsed, so the
+    hash follows the code, not its commentary."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     for n in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "block_sparse_paged_split_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "block_sparse_paged_split_gb300", "csrc", n)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -11,10 +11,13 @@
 //     one stage holds one 32-token tile of K and of V (and, for the first tile
 //     of a work item, the item's query rows).
 //   * One producer warp per consumer (one active lane).  It takes the next
-//     work item from the largest-first schedule through an atomic counter
-//     (one self-contained record per item, its tiles as a bitmap over its
-//     block range, claimed shortly before it is needed), reads the page
-//     table a tile ahead, writes a small
+//     work item through an atomic counter from one of three lists: the
+//     largest-first schedule compaction wrote, list 1 (a sparse call's items,
+//     written by the previous depth's finish), or the dense list (every range
+//     of every row, mapped from the row lengths through a shared-memory table,
+//     no record load).  One self-contained record per item, its tiles as a
+//     bitmap over its block range, claimed shortly before it is needed; the
+//     producer reads the page table a tile ahead, writes a small
 //     descriptor into the stage, and issues one TMA bulk-tensor copy per page
 //     and cache (box = one page of one KV head) plus a bulk copy of q, all
 //     completing on the stage's "full" mbarrier.  Consumers release a stage
@@ -32,6 +35,10 @@
 //   * Online softmax per item: running max m, per-lane exp-sum, accumulator
 //     rescaled once per tile.  The item's unnormalised output, max and
 //     exp-sum go to the workspace; the finish kernel merges the items.
+//   * Programmatic dependent launch: the CTAs start while the previous kernel
+//     drains and wait before touching the workspace; with
+//     WISE_FLAG_INPUTS_READY a dense-list pass, or a pass on a list built
+//     before the previous kernel, issues its first copies before that wait.
 #pragma once
 
 #include <mutex>
