@@ -336,8 +336,12 @@ __global__ void __launch_bounds__(W * 32)
   } else {
     hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
   }
+  // The next kernel may start launching now: its CTAs take the SMs the
+  // partial pass frees in its tail and wait there (a pass whose inputs are
+  // ready issues its first copies meanwhile); every kernel of the library
+  // waits for this one before it touches the workspace or the mask.
+  grid_dependents_launch();
   grid_dependency_wait();    // the partial pass's results
-  grid_dependents_launch();  // the next call's compaction may start launching
   // The mask words the call starts from (the group's first CTA): union-discover
   // rows OR into them, and a list build takes them as they are for rows this
   // call does not select.
@@ -516,8 +520,12 @@ __global__ void __launch_bounds__(256)
     hi = (kp.list1 ? ws.head_info_1 : ws.head_info)[rg];
   }
   if (threadIdx.x < 2) smask[threadIdx.x] = 0u;
+  // The next kernel may start launching now: its CTAs take the SMs the
+  // partial pass frees in its tail and wait there (a pass whose inputs are
+  // ready issues its first copies meanwhile); every kernel of the library
+  // waits for this one before it touches the workspace or the mask.
+  grid_dependents_launch();
   grid_dependency_wait();    // the partial pass's results
-  grid_dependents_launch();  // the next call's compaction may start launching
   // The mask words the call starts from: union-discover rows OR into them, and
   // a list build takes them as they are for the rows this call does not select.
   const bool need_old = (disc && mode == WISE_MODE_DISCOVER_UNION) || (kBuild && !disc);
