@@ -1349,7 +1349,7 @@ def sparse_scaling_main(args):
 
 
 def main_reference(args):
-    rank = rank_env()[1]
+    world, rank = rank_env()[0], rank_env()[1]
     if rank != 0:
         return
     K, Wm = args.steps, args.warmup
@@ -1362,7 +1362,7 @@ def main_reference(args):
                             eta=args.eta)
     value = res["value"]
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
-           "n_gpus": 1, "steps": K, "warmup": Wm,
+           "n_gpus": world, "steps": K, "warmup": Wm,
            "ms_per_step": round(1e3 * rows * 4 / value, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"{args.workload} (oracle sample of {rows} rows per step)"},
