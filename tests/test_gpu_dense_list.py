@@ -22,11 +22,11 @@ RAGGED = np.array([1, 31, 32, 33, 300, 517, 0, 1024], np.int32)
 CASES = [(4, 4, 128, "bf16"), (8, 2, 128, "bf16"), (4, 1, 64, "bf16"), (4, 2, 128, "f32")]
 
 
-def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=5, n_planted=3):
+def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=5, n_planted=3, page_size=16):
     R = len(lens)
     return custom_workload("dense-list", R=R, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, depths=3,
                            n_planted=n_planted, seq_lens=lens, pool_factor=2, seed=seed,
-                           depth_modes=[np.zeros(R, np.int8)] * 3)
+                           depth_modes=[np.zeros(R, np.int8)] * 3, page_size=page_size)
 
 
 def _dense_call(b, depth, modes_np, sup, shape, ws, flags=0, finish_flags=0):
@@ -257,3 +257,97 @@ def test_slot_set_1():
     g = gpu_call(b, 0, m, sup_np)
     assert torch.equal(out.cpu(), g["out_raw"]) and np.array_equal(lse.cpu().numpy(), g["lse"])
     assert np.array_equal(np_support(sup), g["support"])
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 128, "bf16"), (8, 2, 128, "bf16"),
+                                           (2, 2, 64, "f32")])
+def test_page_size_32(Hq, Hkv, D, dtype):
+    """32-token pages (one page per tile): the compaction-free step (dense list
+    with early reads, list 1 built by the union finish, a sparse depth on it)
+    against the same calls after their own compaction, bit for bit, and the
+    sparse depth against the oracle."""
+    w = _wl(Hq, Hkv, D, dtype, page_size=32, seed=33)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = _fresh(shape)
+    sup = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    got = []
+    for depth, mode in ((0, W.MODE_DISCOVER), (1, W.MODE_DISCOVER_UNION), (2, W.MODE_SPARSE)):
+        m = np.full(R, mode, np.int8)
+        if mode == W.MODE_SPARSE:
+            d = b.dev(depth)
+            out = torch.empty_like(d["q"])
+            lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+            W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, None, ws, W.FLAG_SPARSE_LIST)
+            W.wise_decode_finish_ex(shape, None, b.seq_lens, ws, sup, out, lse,
+                                    flags=W.FLAG_SPARSE_LIST)
+        else:
+            out, lse = _dense_call(b, depth, m, sup, shape, ws, flags=W.FLAG_INPUTS_READY,
+                                   finish_flags=W.FLAG_BUILD_SPARSE_LIST if depth == 1 else 0)
+        torch.cuda.synchronize()
+        got.append((out.cpu(), lse.cpu().numpy(), np_support(sup)))
+    s0 = np.zeros((R, Hkv, words(w)), np.uint32)
+    g0 = gpu_call(b, 0, np.full(R, 1, np.int8), s0)
+    g1 = gpu_call(b, 1, np.full(R, 2, np.int8), g0["support"])
+    g2 = gpu_call(b, 2, np.full(R, 3, np.int8), g1["support"])
+    for i, ((out, lse, s_), g) in enumerate(zip(got, (g0, g1, g2))):
+        assert torch.equal(out, g["out_raw"]) and np.array_equal(lse, g["lse"]), i
+        assert np.array_equal(s_, g["support"]), i
+    o = oracle_call(b, 2, np.full(R, 3, np.int8), g1["support"])
+    assert not compare_outputs(w, g2, o)
+    assert _status(shape, ws) == 0
+
+
+def test_workspace_state_across_call_kinds():
+    """One workspace through a sequence of every kind of call -- dense list,
+    compaction, list 1 built and used (also read early), the dense list again,
+    a compaction-based sparse call between -- each output and mask bit for bit
+    the same as that call made alone on a fresh workspace after its own
+    compaction: no queue, counter or list state leaks from one call into the
+    next."""
+    w = _wl(4, 2, 128, "bf16", seed=35)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    ws = _fresh(shape)
+    sup = dev_support(np.zeros((R, 2, words(w)), np.uint32))
+    D_, DU, DS, SP = W.MODE_DISCOVER, W.MODE_DISCOVER_UNION, W.MODE_DENSE, W.MODE_SPARSE
+
+    def step(depth, mode, kind):
+        m = np.full(R, mode, np.int8)
+        mt = torch.from_numpy(m).cuda()
+        d = b.dev(depth)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((R, 4), dtype=torch.float32, device="cuda")
+        sup_in = np_support(sup)
+        if kind.startswith("dense"):
+            fflags = W.FLAG_BUILD_SPARSE_LIST if kind == "dense+build" else 0
+            out, lse = _dense_call(b, depth, m, sup, shape, ws, flags=W.FLAG_INPUTS_READY,
+                                   finish_flags=fflags)
+        elif kind.startswith("list1"):
+            pf = W.FLAG_SPARSE_LIST | (W.FLAG_INPUTS_READY if kind == "list1-ready" else 0)
+            W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                     b.seq_lens, None, ws, pf)
+            W.wise_decode_finish_ex(shape, None, b.seq_lens, ws, sup, out, lse,
+                                    flags=W.FLAG_SPARSE_LIST)
+        else:  # compaction, then the two passes (the finish may build list 1)
+            W.wise_compact_tiles(shape, mt, b.seq_lens, sup, ws)
+            W.wise_decode_partial(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                  b.seq_lens, mt, ws)
+            W.wise_decode_finish_ex(shape, mt, b.seq_lens, ws, sup, out, lse,
+                                    flags=W.FLAG_BUILD_SPARSE_LIST if kind == "compact+build" else 0)
+        torch.cuda.synchronize()
+        g = gpu_call(b, depth, m, sup_in)  # alone, on a fresh workspace
+        assert torch.equal(out.cpu(), g["out_raw"]), (depth, mode, kind)
+        assert np.array_equal(lse.cpu().numpy(), g["lse"]), (depth, mode, kind)
+        assert np.array_equal(np_support(sup), g["support"]), (depth, mode, kind)
+
+    for depth, mode, kind in ((0, D_, "dense"), (1, DU, "compact+build"), (2, SP, "list1"),
+                              (0, DS, "dense"), (1, SP, "compact"), (2, DU, "dense+build"),
+                              (0, SP, "list1"), (1, SP, "list1-ready"), (2, D_, "compact"),
+                              (0, DU, "dense")):
+        step(depth, mode, kind)
+        v = W.workspace_views(shape, ws)
+        assert int(v["queue"].item()) == 0 and _status(shape, ws) == 0, (depth, mode, kind)
