@@ -55,10 +55,10 @@ struct UnitInfo {
   int raw;        // the row's length before clamping
 };
 
-// The loads of one unit (issued together; nothing here waits on them).  The
-// row's mode and length are the caller's inputs and are read before the
-// dependency wait; the mask word may come from the previous call's finish
-// pass and is read after it.
+// The loads of one unit (issued together; nothing here waits on them), all
+// after the dependency wait: the row's mode, length and mask slot (the
+// caller's inputs, possibly written by the kernel before this one), then the
+// mask word (possibly written by the previous call's finish pass).
 struct UnitLoad {
   int mode, raw, slot;
   uint32_t word;

@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(W * 32)
   // Read before the dependency wait: the caller's inputs and the head info
   // (written by compaction or by the finish that built list 1).  The kernel
   // before this one is the call's partial pass, which triggers this launch
-  // only after its own dependency wait, so all of them are complete.
+  // only after its own dependency wait, so all of them are complete (and the
+  // partial pass does not write them).
   int4 hi;
   if (kp.dense_list) {  // every range of the row is one item
     const int nr = (nb + kp.T - 1) / kp.T;
