@@ -77,6 +77,9 @@ def parse():
     p.add_argument("--no-sweep", action="store_true",
                    help="measure only the headline workload (the default run also measures "
                         "the 4K, mixed 8K and 32K grouped-query workloads)")
+    p.add_argument("--early", action="store_true",
+                   help="depths on the dense list or a ready list 1 start beside the previous "
+                        "finish on the other slot set (measured: no gain; off by default)")
     p.add_argument("--no-dense-list", action="store_true",
                    help="dense and discover depths get a compaction instead of deriving their "
                         "work list from the row lengths")
@@ -345,7 +348,8 @@ class Pipeline:
 
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
                  lse_discover: bool = False, overlap: bool = False, share=None,
-                 sparse_list: bool = True, device_inputs: bool = False, dense_list: bool = True):
+                 sparse_list: bool = True, device_inputs: bool = False, dense_list: bool = True,
+                 early_lists: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -440,14 +444,23 @@ class Pipeline:
         W.wise_workspace_reset(self.shape, self.ws)
 
         def calls(modes_t, t, compact=True, early=False, build=False, on_list=False, dense=False,
-                  list_ready=False):
+                  list_ready=False, alt=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
+            # alt: consecutive depths take the workspace's two slot sets in
+            # turn, so a depth on the dense list, or on a list built before
+            # the previous finish, starts while that finish still runs
+            # (WISE_FLAG_EARLY_START); the first depth of a step only when the
+            # step's depth count is even (the previous step's last depth then
+            # used the other set).
+            sset = W.FLAG_SLOT_SET_1 if (alt and t % 2) else 0
+            may_early = alt and (t > 0 or w.num_depths % 2 == 0)
             if dense:
                 # Every kernel ahead of it in the step is a pass of the library.
-                pf = W.FLAG_DENSE_LIST | W.FLAG_INPUTS_READY
-                ff = W.FLAG_DENSE_LIST | (W.FLAG_BUILD_SPARSE_LIST if build else 0)
+                pf = (W.FLAG_DENSE_LIST | W.FLAG_INPUTS_READY | sset |
+                      (W.FLAG_EARLY_START if may_early else 0))
+                ff = W.FLAG_DENSE_LIST | (W.FLAG_BUILD_SPARSE_LIST if build else 0) | sset
                 c.append(("partial", lib.wise_decode_partial_ex,
                           (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                            pt, sl, m, ws, nws, pf, st)))
@@ -456,10 +469,11 @@ class Pipeline:
                            self.lse[t].data_ptr(), st)))
                 return c
             if on_list:
-                f = W.FLAG_SPARSE_LIST
+                f = W.FLAG_SPARSE_LIST | sset
                 # A call after the first on the list reads a list built two or
                 # more kernels back, and inputs no kernel of the step writes.
-                pf = f | (W.FLAG_INPUTS_READY if list_ready else 0)
+                pf = f | ((W.FLAG_INPUTS_READY | (W.FLAG_EARLY_START if may_early else 0))
+                          if list_ready else 0)
                 c.append(("partial", lib.wise_decode_partial_ex,
                           (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                            pt, sl, m, ws, nws, pf, st)))
@@ -537,6 +551,24 @@ class Pipeline:
         def all_discover(m):
             return all(int(x) in (W.MODE_DISCOVER, W.MODE_DISCOVER_UNION) for x in m)
 
+        def compaction_free():
+            # Every depth of the step on the dense list or on list 1.
+            listed = False
+            for t in range(w.num_depths):
+                dm = w.depth_modes
+                if lse_discover and all_discover(dm[t]):
+                    return False
+                on_list = self.sparse_list and listed and all_sparse(dm[t])
+                build = (self.sparse_list and not all_sparse(dm[t]) and t + 1 < w.num_depths and
+                         all_sparse(dm[t + 1]))
+                dense = self.dense_list and not any(int(x) == W.MODE_SPARSE for x in dm[t])
+                listed = build or on_list
+                if not (on_list or dense):
+                    return False
+            return True
+
+        self.early_lists = early_lists and self.dense_list and compaction_free()
+        self.early_dense = early_lists and self.dense_list
         self.wise_step = []
         listed = False  # list 1 holds the work list of an all-sparse depth on the current mask
         list0 = False   # the compacted list holds the previous depth's work list
@@ -559,7 +591,7 @@ class Pipeline:
                 self.wise_step.append((t, depth_name(dm[t]),
                                        calls(self.modes[t], t, compact=not reuse and not dense,
                                              build=build, on_list=on_list, dense=dense,
-                                             list_ready=list_ready)))
+                                             list_ready=list_ready, alt=self.early_lists)))
                 list0 = build and not dense
                 continue
             list0 = True
@@ -572,7 +604,8 @@ class Pipeline:
         # The dense baseline gets the same call sequence: one compaction for
         # its four depths (they share the work list) and the same overlap.
         if self.dense_list:
-            self.dense_step = [(t, "dense", calls(self.dense_modes, t, dense=True))
+            self.dense_step = [(t, "dense", calls(self.dense_modes, t, dense=True,
+                                                  alt=self.early_dense))
                                for t in range(w.num_depths)]
         else:
             self.dense_step = [(t, "dense", calls(self.dense_modes, t, compact=(t == 0),
@@ -948,7 +981,8 @@ def sweep_workload(name, args, steps, peak):
     t0 = time.time()
     w = make_workload(name, **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
-                    device_inputs=True, dense_list=not args.no_dense_list)
+                    device_inputs=True, dense_list=not args.no_dense_list,
+                    early_lists=args.early)
     for _ in range(3):
         pipe.run(pipe.wise_step)
         pipe.run(pipe.dense_step)
@@ -998,7 +1032,8 @@ def eta_point(name, eta, args, steps):
     from block_sparse_paged_split_gb300.workload import make_workload
     w = make_workload(name, eta=eta)
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
-                    device_inputs=True, dense_list=not args.no_dense_list)
+                    device_inputs=True, dense_list=not args.no_dense_list,
+                    early_lists=args.early)
     for _ in range(3):
         pipe.run(pipe.wise_step)
     torch.cuda.synchronize()
@@ -1044,7 +1079,8 @@ def main_ours(args):
     w = make_workload(args.workload, num_rows=args.rows, seed=rank_seed(rank), **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
                     lse_discover=args.lse_discover, overlap=args.overlap,
-                    sparse_list=not args.no_sparse_list, dense_list=not args.no_dense_list)
+                    sparse_list=not args.no_sparse_list, dense_list=not args.no_dense_list,
+                    early_lists=args.early)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -1126,7 +1162,8 @@ def main_ours(args):
     pipe_b = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold,
                       head_union=args.head_union, lse_discover=args.lse_discover,
                       overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list,
-                      dense_list=not args.no_dense_list)
+                      dense_list=not args.no_dense_list,
+                    early_lists=args.early)
     graph_b = pipe_b.graph(pipe_b.wise_step)
     e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
     e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)
@@ -1176,7 +1213,10 @@ def main_ours(args):
                                + (", sparse depths on the work list the union depth's finish "
                                   "builds (no compaction launch)" if pipe.sparse_list else "")
                                + (", dense and discover depths on work lists derived from the "
-                                  "row lengths (no compaction launch)" if pipe.dense_list else ""),
+                                  "row lengths (no compaction launch)" if pipe.dense_list else "")
+                               + (", consecutive depths on alternate slot sets, a depth on the "
+                                  "dense list or a ready list starting beside the previous finish"
+                                  if pipe.early_lists else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "

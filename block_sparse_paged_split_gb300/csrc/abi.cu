@@ -366,9 +366,10 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
   if ((flags & WISE_FLAG_DENSE_LIST) && shape->num_rows > WISE_DENSE_LIST_MAX_ROWS)
     return fail(WISE_ERR_UNSUPPORTED, "WISE_FLAG_DENSE_LIST takes at most %d rows (got %d)",
                 WISE_DENSE_LIST_MAX_ROWS, shape->num_rows);
-  if ((flags & WISE_FLAG_DENSE_LIST) && (flags & WISE_FLAG_EARLY_START))
+  if ((flags & (WISE_FLAG_DENSE_LIST | WISE_FLAG_SPARSE_LIST)) && (flags & WISE_FLAG_EARLY_START) &&
+      !(flags & WISE_FLAG_INPUTS_READY))
     return fail(WISE_ERR_INVALID_ARG,
-                "WISE_FLAG_DENSE_LIST clears the status word, so the pass cannot start early");
+                "an early start on the dense list or list 1 needs WISE_FLAG_INPUTS_READY");
   WsView ws;
   if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
     return st;

@@ -561,8 +561,11 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   // previous kernel writes nothing it reads and reads nothing it writes; the
   // compaction it uses completed before that kernel began) skips the wait
   // here and waits before it exits instead, so its completion still implies
-  // the previous kernel's.
-  const bool producer_defers = early_reads && warp >= C;
+  // the previous kernel's.  Its producers, like those of an early-reading
+  // pass, still wait before their first queue claim: the kernel ahead may
+  // have started before the partial pass that last used the queue had put
+  // it back to 0.
+  const bool producer_defers = (kp.early || early_reads) && warp >= C;
   if (!kp.early && !producer_defers) grid_dependency_wait();
   if (kp.dense_list && !kp.inputs_ready) {
     if (warp == 0) build_table();
@@ -570,9 +573,10 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
   }
   // A dense-list pass has no compaction to clear the status word: block 0
   // clears it once the previous kernel (which may flag into it) is done, then
-  // flags a clamped length.
+  // flags a clamped length.  An early-start pass runs beside that kernel, so
+  // it leaves the word as it is and only adds its own flag.
   if (kp.dense_list && blockIdx.x == 0 && warp == 0) {
-    if (lane == 0) *ws.status = 0;
+    if (lane == 0 && !kp.early) *ws.status = 0;
     __syncwarp();
     if (__any_sync(kFull, clamped) && lane == 0) flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
   }
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(2 * C * 32, 1)
       // producer takes that wait first, so the bounded wait below never
       // counts the previous kernel's run time.
       const int stage = seq % S;
-      if (seq >= (uint32_t)S && !waited) {
+      if (seq >= (uint32_t)S && !waited && !kp.early) {
         grid_dependency_wait();
         waited = true;
       }

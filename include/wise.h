@@ -269,7 +269,11 @@ enum {
    * Legal when that kernel writes nothing this call reads and reads nothing
    * it writes, and the compaction this call uses completed before that
    * kernel began: for instance the finish of the previous depth, on the other
-   * slot set, when both calls share one compaction. */
+   * slot set, when both calls share one compaction, or -- with
+   * WISE_FLAG_INPUTS_READY, which a pass on the dense list or on list 1
+   * then needs -- a call on the dense list or on a list built before that
+   * finish.  The queue claims still wait for the previous kernel.  An
+   * early dense-list pass leaves the status word as it is. */
   WISE_FLAG_EARLY_START = 2u,
   /* Finish only: also write the work list of a following call in which every
    * row is sparse on the mask as this call leaves it ("list 1" of the
@@ -298,8 +302,8 @@ enum {
    * partial pass clears the workspace status word.  The workspace's queue
    * counters must be 0, as every compaction and every completed partial pass
    * leave them (wise_workspace_reset zeroes a new workspace).  Not with
-   * WISE_FLAG_SPARSE_LIST, WISE_FLAG_EARLY_START or
-   * wise_decode_partial_finish. */
+   * WISE_FLAG_SPARSE_LIST or wise_decode_partial_finish; with
+   * WISE_FLAG_EARLY_START only together with WISE_FLAG_INPUTS_READY. */
   WISE_FLAG_DENSE_LIST = 16u,
   /* Partial pass: everything the pass reads was complete before the kernel
    * ahead of this launch in the stream began: the caller's inputs (q, the

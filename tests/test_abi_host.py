@@ -162,9 +162,9 @@ def test_flag_checks(lib):
 
 
 def test_dense_list_checks(lib):
-    """WISE_FLAG_DENSE_LIST: at most DENSE_LIST_MAX_ROWS rows, and neither
-    with list 1, an early start nor the folded finish; checked on the host
-    before anything is enqueued."""
+    """WISE_FLAG_DENSE_LIST: at most DENSE_LIST_MAX_ROWS rows, not with list 1
+    nor the folded finish, an early start only with WISE_FLAG_INPUTS_READY;
+    checked on the host before anything is enqueued."""
     P = ctypes.c_void_p
     D = ctypes.c_uint32(W.FLAG_DENSE_LIST)
     big = _shape(num_rows=W.DENSE_LIST_MAX_ROWS + 1)
@@ -176,7 +176,9 @@ def test_dense_list_checks(lib):
                                      P(16), P(16), None) == 2
     s = _shape()
     n = W.wise_workspace_bytes(s)
-    for flags in (W.FLAG_DENSE_LIST | W.FLAG_SPARSE_LIST, W.FLAG_DENSE_LIST | W.FLAG_EARLY_START):
+    # an early start on the dense list or list 1 needs WISE_FLAG_INPUTS_READY
+    for flags in (W.FLAG_DENSE_LIST | W.FLAG_SPARSE_LIST, W.FLAG_DENSE_LIST | W.FLAG_EARLY_START,
+                  W.FLAG_SPARSE_LIST | W.FLAG_EARLY_START):
         st = lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
                                         P(4096), n, ctypes.c_uint32(flags), None)
         assert st == 1, flags

@@ -71,9 +71,9 @@ def _status(pipe):
     return int(W.workspace_views(pipe.shape, pipe.ws)["status"].item())
 
 
-def _check_step(name, rows=None, device_inputs=False):
+def _check_step(name, rows=None, device_inputs=False, early=False):
     w = make_workload(name)
-    pipe = bench.Pipeline(w, device_inputs=device_inputs)
+    pipe = bench.Pipeline(w, device_inputs=device_inputs, early_lists=early)
     for _ in range(2):  # the step as the benchmark replays it, on a used workspace
         pipe.run(pipe.wise_step)
     torch.cuda.synchronize()
@@ -122,6 +122,14 @@ def test_bench_step_1k_every_row():
     """64 rows x 1024 tokens, 16 heads: every row of every depth."""
     report = _check_step("ouro1.4b_1k")
     assert all(c > 0 for t, c, _, _ in report if t < 2)
+
+
+def test_bench_step_1k_early_start():
+    """The same with `bench.py --early`: consecutive depths on alternate slot
+    sets, the dense-list depths and the second list-1 depth starting beside
+    the previous finish; the graph replay then overlaps them, and still gives
+    the depth-by-depth bits."""
+    _check_step("ouro1.4b_1k", rows=np.arange(0, 64, 7), early=True)
 
 
 def test_bench_step_4k_sampled():

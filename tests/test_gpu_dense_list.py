@@ -351,3 +351,62 @@ def test_workspace_state_across_call_kinds():
         step(depth, mode, kind)
         v = W.workspace_views(shape, ws)
         assert int(v["queue"].item()) == 0 and _status(shape, ws) == 0, (depth, mode, kind)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 128, "bf16"), (8, 2, 128, "bf16"),
+                                           (4, 2, 128, "f32")])
+def test_early_start_on_alternate_slot_sets(Hq, Hkv, D, dtype):
+    """The step as the benchmark overlaps it: depths on alternate slot sets,
+    the dense-list depths and the second list-1 depth starting beside the
+    previous finish (WISE_FLAG_EARLY_START with WISE_FLAG_INPUTS_READY), three
+    steps queued back to back with no synchronisation: every depth's output,
+    LSE and mask bit for bit those of the serial step."""
+    w = _wl(Hq, Hkv, D, dtype, seed=37)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    plan = ((0, W.MODE_DISCOVER, "dense"), (1, W.MODE_DISCOVER_UNION, "build"),
+            (2, W.MODE_SPARSE, "list1"), (0, W.MODE_SPARSE, "list1-ready"))
+    modes = {mode: torch.full((R,), mode, dtype=torch.int8, device="cuda") for _, mode, _ in plan}
+
+    def run_step(ws, sup, early):
+        outs = []
+        for t, (depth, mode, kind) in enumerate(plan):
+            sset = W.FLAG_SLOT_SET_1 if (early and t % 2) else 0
+            e = W.FLAG_EARLY_START if early else 0
+            d = b.dev(depth)
+            out = torch.empty_like(d["q"])
+            lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+            m = modes[mode]
+            if kind.startswith("list1"):
+                pf = W.FLAG_SPARSE_LIST | sset
+                if kind == "list1-ready":
+                    pf |= W.FLAG_INPUTS_READY | e
+                W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                         b.seq_lens, None, ws, pf)
+                W.wise_decode_finish_ex(shape, None, b.seq_lens, ws, sup, out, lse,
+                                        flags=W.FLAG_SPARSE_LIST | sset)
+            else:
+                W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table,
+                                         b.seq_lens, m, ws,
+                                         W.FLAG_DENSE_LIST | W.FLAG_INPUTS_READY | sset | e)
+                ff = W.FLAG_DENSE_LIST | sset | (W.FLAG_BUILD_SPARSE_LIST if kind == "build" else 0)
+                W.wise_decode_finish_ex(shape, m, b.seq_lens, ws, sup, out, lse, flags=ff)
+            if not early:
+                torch.cuda.synchronize()
+            outs.append((out, lse))
+        return outs
+
+    ref_ws = _fresh(shape)
+    ref_sup = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    ref = run_step(ref_ws, ref_sup, early=False)
+    torch.cuda.synchronize()
+    ws = _fresh(shape)
+    sup = dev_support(np.zeros((R, Hkv, words(w)), np.uint32))
+    for _ in range(3):
+        got = run_step(ws, sup, early=True)
+    torch.cuda.synchronize()
+    for i, ((o, l), (ro, rl)) in enumerate(zip(got, ref)):
+        assert torch.equal(o.cpu(), ro.cpu()) and torch.equal(l.cpu(), rl.cpu()), i
+    assert np.array_equal(np_support(sup), np_support(ref_sup))
+    assert int(W.workspace_views(shape, ws)["queue"].item()) == 0 and _status(shape, ws) == 0
