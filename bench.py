@@ -1397,6 +1397,8 @@ def main_reference(args):
     # the 4 depths on every host thread (tens of milliseconds); the warm-up
     # passes run untimed inside the child before the K timed ones.
     rows = 16
+    from block_sparse_paged_split_gb300.workload import make_workload
+    w_ref = make_workload(args.workload, **eta_kw(args.eta))  # its shape only (no inputs drawn)
     t0 = time.perf_counter()
     res = run_oracle_sample(args.workload, rows=rows, seconds_1t=0.0, reps=K, warmup=Wm,
                             eta=args.eta)
@@ -1405,7 +1407,11 @@ def main_reference(args):
            "n_gpus": world, "steps": K, "warmup": Wm,
            "ms_per_step": round(1e3 * rows * 4 / value, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-           "config": {"workload": f"{args.workload} (oracle sample of {rows} rows per step)"},
+           "config": {"workload": f"{args.workload}: {w_ref.num_rows} rows x "
+                                  f"{int(w_ref.seq_lens.max())} tokens, {w_ref.num_q_heads} q / "
+                                  f"{w_ref.num_kv_heads} kv heads, D={w_ref.head_dim}, page "
+                                  f"{w_ref.page_size}, B=32, eta={w_ref.eta}, 4 depths",
+                      "sample": f"{rows} of its rows per step through the oracle"},
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": res["cores"],
                             "kind": "oracle", "sample": res["sample"],
                             "per_mode_rows_per_s": res["per_mode_rows_per_s"]},
