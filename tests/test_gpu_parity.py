@@ -89,6 +89,51 @@ def test_eta_range(Hq, Hkv, eta):
     assert not compare_outputs(w, g, o)
 
 
+@pytest.mark.parametrize("lens", [RAGGED, np.array([16384, 3000, 0, 9000], np.int32)],
+                         ids=["short", "long"])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4)])
+def test_tiny_eta_keeps_each_heads_top_block(Hq, Hkv, lens):
+    """The small end of the threshold: with eta below every block's mass the
+    shortest prefix reaching it is one block, so each query head keeps exactly
+    its heaviest block (equal masses: the lower index) and a KV head's mask is
+    the OR of its group's choices.  Checked against the oracle's block masses
+    wherever the two heaviest blocks differ by more than a relative 1e-5 (the
+    rest must still keep one to G blocks); rows of 512 blocks and more take the
+    finish's threshold search instead of the sort.  Then a sparse call on that
+    mask (one tile per query head) against the oracle."""
+    eta = 1e-6
+    w = _wl(Hq, Hkv, 128, "bf16", lens=lens)
+    b = Batch(w)
+    R, G = w.num_rows, w.group
+    zero = np.zeros((R, Hkv, words(w)), np.uint32)
+    m = np.full(R, W.MODE_DISCOVER, np.int8)
+    g, o = gpu_call(b, 0, m, zero, eta=eta), oracle_call(b, 0, m, zero, eta=eta)
+    assert not compare_outputs(w, g, o)
+    checked = 0
+    for r in range(R):
+        nb = -(-int(w.seq_lens[r]) // 32)
+        if nb == 0:
+            assert not g["support"][r].any()
+            continue
+        for kv in range(Hkv):
+            want = np.zeros(nb, bool)
+            clear = True
+            for h in range(kv * G, (kv + 1) * G):
+                dg = o["diag"][(r, h)]
+                ps = np.asarray(dg["p"], np.float64)[dg["order"]]
+                want[dg["order"][0]] = True
+                clear &= nb == 1 or ps[0] - ps[1] > 1e-5 * ps[0]
+            got = O.mask_bits(g["support"][r, kv], nb)
+            assert 1 <= got.sum() <= G, (r, kv)
+            if clear:
+                checked += 1
+                assert np.array_equal(got, want), (r, kv)
+    assert checked > 0
+    m = np.full(R, W.MODE_SPARSE, np.int8)
+    g2, o2 = gpu_call(b, 1, m, g["support"], eta=eta), oracle_call(b, 1, m, g["support"], eta=eta)
+    assert not compare_outputs(w, g2, o2)
+
+
 def test_tile_stats_match_oracle():
     """Discover rows' per-tile max and exp-sum (the workspace intermediates)."""
     w = _wl(4, 4, 128, "bf16")
