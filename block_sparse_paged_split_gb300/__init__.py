@@ -10,7 +10,7 @@ from .wise import (MODE_DENSE, MODE_DISCOVER, MODE_DISCOVER_UNION, MODE_SPARSE, 
                    wise_block_mass, wise_compact_tiles, wise_decode, wise_decode_finish, wise_decode_partial,
                    wise_decode_partial_finish, wise_decode_partial_ex, wise_decode_finish_ex,
                    FLAG_SLOT_SET_1, FLAG_EARLY_START, FLAG_BUILD_SPARSE_LIST, FLAG_SPARSE_LIST,
-                   FLAG_DENSE_LIST, FLAG_INPUTS_READY, DENSE_LIST_MAX_ROWS, wise_workspace_reset,
+                   FLAG_DENSE_LIST, FLAG_INPUTS_READY, DENSE_LIST_MAX_ROWS, MAX_BLOCKS, wise_workspace_reset,
                    wise_support_head_union, wise_support_union, wise_validate, wise_workspace_bytes,
                    wise_workspace_layout, workspace_views, wise_mask, make_mask,
                    wise_compact_tiles_m, wise_decode_finish_m, wise_decode_m, wise_validate_m)
@@ -20,7 +20,7 @@ __all__ = ["MODE_DENSE", "MODE_DISCOVER", "MODE_DISCOVER_UNION", "MODE_SPARSE", 
            "wise_block_mass", "wise_compact_tiles", "wise_decode", "wise_decode_finish", "wise_decode_partial",
            "wise_decode_partial_finish", "wise_decode_partial_ex", "wise_decode_finish_ex",
            "FLAG_SLOT_SET_1", "FLAG_EARLY_START", "FLAG_BUILD_SPARSE_LIST", "FLAG_SPARSE_LIST",
-           "FLAG_DENSE_LIST", "FLAG_INPUTS_READY", "DENSE_LIST_MAX_ROWS", "wise_workspace_reset",
+           "FLAG_DENSE_LIST", "FLAG_INPUTS_READY", "DENSE_LIST_MAX_ROWS", "MAX_BLOCKS", "wise_workspace_reset",
            "wise_support_head_union", "wise_support_union", "wise_validate", "wise_workspace_bytes",
            "wise_workspace_layout", "workspace_views", "wise_mask", "make_mask",
            "wise_compact_tiles_m", "wise_decode_finish_m", "wise_decode_m", "wise_validate_m"]

@@ -53,8 +53,9 @@ wise_status check_shape(const wise_shape* s) {
     return fail(WISE_ERR_INVALID_ARG, "max_pages_per_row and num_pages must be >= 1");
   if ((int64_t)s->num_pages * s->page_size > INT32_MAX / 2)
     return fail(WISE_ERR_UNSUPPORTED, "num_pages * page_size too large");
-  if (s->max_blocks < 1 || s->max_blocks > 1024)
-    return fail(WISE_ERR_UNSUPPORTED, "max_blocks must be in [1, 1024] (got %d)", s->max_blocks);
+  if (s->max_blocks < 1 || s->max_blocks > WISE_MAX_BLOCKS)
+    return fail(WISE_ERR_UNSUPPORTED, "max_blocks must be in [1, %d] (got %d)", WISE_MAX_BLOCKS,
+                s->max_blocks);
   if (s->tiles_per_item < 0 || s->tiles_per_item > 16 ||
       (s->tiles_per_item & (s->tiles_per_item - 1)) != 0)
     return fail(WISE_ERR_INVALID_ARG, "tiles_per_item must be 0, 1, 2, 4, 8 or 16");

@@ -27,6 +27,8 @@
 
 namespace wise {
 
+constexpr int kMaxW = WISE_MAX_BLOCKS / 32;  // mask words of a (row, KV head), at most
+
 __device__ __forceinline__ void group_sync(int id, int threads) {
   if (threads == 32) {
     __syncwarp();
@@ -166,7 +168,7 @@ template <int N>
 __device__ __forceinline__ void group_sums_u32(const uint32_t (&v)[N], uint32_t (&out)[N],
                                                int lane, int wsub, int wph, uint32_t* buf,
                                                int& parity, int bar_id) {
-  uint32_t* b = buf + (parity & 1) * 8 * N;
+  uint32_t* b = buf + (parity & 1) * wph * N;
 #pragma unroll
   for (int n = 0; n < N; ++n) {
     const uint32_t w = __reduce_add_sync(kFull, v[n]);
@@ -192,7 +194,7 @@ __device__ __forceinline__ void group_sums_u32(const uint32_t (&v)[N], uint32_t 
 // every sum fits in 32 bits), and v is the largest float bit pattern whose
 // blocks of mass >= v sum to eta or more, found two bits at a time from the
 // top (three group sums a step).  The truncation moves a sum by less than
-// 1024 * 2^-31 = 4.8e-7, so the cutoff can differ from an exact prefix sum
+// 4096 * 2^-31 = 1.9e-6, so the cutoff can differ from an exact prefix sum
 // only where the cumulative mass lies that close to eta.  Block i = wsub * 32E
 // + lane * E + e stays in index order, so the kept blocks become mask words by
 // shuffles (each word written once, no atomics).
@@ -290,8 +292,9 @@ __device__ __forceinline__ void group_select_threshold(const float2 (&st)[E], in
 //   select  npad = 32 * E * W keys (npad >= max_blocks, a power of
 //           two; blocks past the row's n_b are padding) are sorted mostly in
 //           registers (see group_bitonic_sort).
-// W = 4 warps a head for up to 512 keys, 8 beyond (same-box A/B: 4 warps
-// made the 4K finish 18.7 -> 12.6 us, 8 warps stay best at 1024 keys).
+// W = 4 warps a head for up to 512 keys, 8 for 1024, 16 for 2048 and 4096
+// (rows past 32K tokens; same-box A/B: 4 warps made the 4K finish 18.7 ->
+// 12.6 us, 8 warps stay best at 1024 keys).
 
 template <typename T, int E, int W, bool kBuild>
 __global__ void __launch_bounds__(W * 32)
@@ -300,9 +303,10 @@ __global__ void __launch_bounds__(W * 32)
                   T* __restrict__ out, float* __restrict__ lse) {
   constexpr int wph = W;
   extern __shared__ __align__(16) uint8_t fsm[];
-  __shared__ uint32_t smask[32];
-  __shared__ uint32_t fwords[32];  // the mask the call leaves (list 1 is built from it)
+  __shared__ uint32_t smask[kMaxW];
+  __shared__ uint32_t fwords[kMaxW];  // the mask the call leaves (list 1 is built from it)
   __shared__ List1Smem l1sm;
+  static_assert(E * W <= kMaxW, "smask holds a word for every 32 padded keys");
   const int G = kp.G, D = kp.D;
   const int gs = wph * 32;
   const int th = threadIdx.x;
@@ -459,10 +463,10 @@ __global__ void __launch_bounds__(W * 32)
   }
 
   // ---- eta selection for this query head, then the group's OR
-  if (th < 32) smask[th] = 0u;
+  for (int i = th; i < kp.W; i += gs) smask[i] = 0u;
   __syncthreads();
   if constexpr (32 * E * W >= 512) {
-    // 512 or 1024 keys: the threshold search (the bitonic sort of 1024 keys
+    // 512 keys or more: the threshold search (the bitonic sort of 1024 keys
     // took 10 us of a 19 us finish at 32K, %globaltimer stamps per CTA).
     group_select_threshold<E>(st, nb, lse2, kp.eta, lane, wsub, wph,
                               reinterpret_cast<uint32_t*>(xbuf), reinterpret_cast<int*>(scratch),
@@ -569,7 +573,9 @@ __global__ void __launch_bounds__(256)
 // Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
 // short kernel (one warp per query head); longer ones a CTA of W warps per
 // query head, clustered by KV head (E = npad / (32 W) keys a thread).
-static int finish_warps(const KParams& kp) { return kp.max_blocks <= 512 ? 4 : 8; }
+static int finish_warps(const KParams& kp) {
+  return kp.max_blocks <= 512 ? 4 : kp.max_blocks <= 1024 ? 8 : 16;
+}
 
 static int finish_npad(const KParams& kp) {
   int n = 32 * finish_warps(kp);
@@ -620,11 +626,10 @@ static cudaError_t launch_finish_b(const KParams& kp, const int8_t* modes,
       default: return launch_long<T, 4, 4, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
     }
   }
-  switch (e) {  // npad = 1024 with 8 warps: e = 4
-    case 1: return launch_long<T, 1, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
-    case 2: return launch_long<T, 2, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
-    default: return launch_long<T, 4, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
-  }
+  if (w == 8) return launch_long<T, 4, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+  // npad 2048 or 4096 with 16 warps: e = 4 or 8
+  if (e == 4) return launch_long<T, 4, 16, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+  return launch_long<T, 8, 16, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
 }
 
 template <typename T>

@@ -234,6 +234,7 @@ FLAG_SPARSE_LIST = 8
 FLAG_DENSE_LIST = 16
 FLAG_INPUTS_READY = 32
 DENSE_LIST_MAX_ROWS = 256
+MAX_BLOCKS = 4096  # WISE_MAX_BLOCKS: largest max_blocks (rows of up to 128K tokens)
 
 
 def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,

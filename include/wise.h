@@ -118,6 +118,10 @@ enum {
   WISE_BAD_SLOT = 16            /* a row slot below -1 or past num_slots     */
 };
 
+/* Largest max_blocks: 4096 blocks of 32 tokens, rows of up to 128K tokens
+ * (a (row, KV head) mask of 128 words). */
+#define WISE_MAX_BLOCKS 4096
+
 typedef struct {
   int32_t num_rows;          /* R >= 0 (0: every call is a no-op)              */
   int32_t num_q_heads;       /* Hq >= 1                                         */
@@ -127,8 +131,9 @@ typedef struct {
   int32_t tile_tokens;       /* block size B; must be 32                        */
   int32_t max_pages_per_row; /* page_table row stride, >= 1                     */
   int32_t num_pages;         /* pages in the K/V pools, >= 1                    */
-  int32_t max_blocks;        /* mask capacity per (row, KV head), 1..1024;
-                                a row's capacity is min(max_blocks * 32,
+  int32_t max_blocks;        /* mask capacity per (row, KV head),
+                                1..WISE_MAX_BLOCKS; a row's capacity
+                                is min(max_blocks * 32,
                                 max_pages_per_row * page_size) tokens          */
   int32_t tiles_per_item;    /* blocks per split range T: 1, 2, 4, 8 or 16;
                                 0 means 8, or 16 when max_blocks > 64 and

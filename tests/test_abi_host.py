@@ -61,7 +61,7 @@ def test_workspace_layout_is_aligned_and_sized(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 96, 2), ("num_kv_heads", 3, 1), ("num_q_heads", 24, 2), ("page_size", 12, 2),
     ("page_size", 8, 2),
-    ("tile_tokens", 64, 2), ("max_blocks", 2048, 2), ("max_blocks", 0, 2), ("dtype", 7, 1),
+    ("tile_tokens", 64, 2), ("max_blocks", 4097, 2), ("max_blocks", 0, 2), ("dtype", 7, 1),
     ("eta", 0.0, 1), ("eta", float("nan"), 1), ("scale", -1.0, 1), ("num_rows", -1, 1),
     ("num_pages", 0, 1), ("tiles_per_item", 17, 1), ("tiles_per_item", 3, 1)])
 def test_shape_checks(lib, field, value, status):
@@ -208,6 +208,21 @@ def test_noalloc_status_rejects_a_null_pointer(lib):
     assert b"host_status" in lib.wise_last_error()
 
 
+def test_max_blocks_limit(lib):
+    """WISE_MAX_BLOCKS (rows of up to 128K tokens): the header, the binding and
+    the shape check agree."""
+    text = open(HEADER).read()
+    assert re.search(r"#define WISE_MAX_BLOCKS (\d+)", text).group(1) == str(W.MAX_BLOCKS)
+    ok = _shape(num_rows=2, num_q_heads=8, num_kv_heads=2, max_blocks=W.MAX_BLOCKS,
+                max_pages_per_row=2 * W.MAX_BLOCKS)
+    assert W.wise_workspace_bytes(ok) > 0
+    bad = _shape(num_rows=2, num_q_heads=8, num_kv_heads=2, max_blocks=W.MAX_BLOCKS + 1,
+                 max_pages_per_row=2 * W.MAX_BLOCKS + 2)
+    n = ctypes.c_size_t(0)
+    assert lib.wise_workspace_bytes(ctypes.byref(bad), ctypes.byref(n)) == 2  # WISE_ERR_UNSUPPORTED
+    assert b"max_blocks" in lib.wise_last_error()
+
+
 def test_default_split_size(lib):
     # short rows: 8 blocks a range
     s = _shape(num_rows=64, num_q_heads=16, num_kv_heads=16, max_blocks=32, max_pages_per_row=64)
@@ -218,6 +233,9 @@ def test_default_split_size(lib):
     # a small batch of long rows keeps 8 (enough items for every consumer)
     s = _shape(num_rows=2, num_q_heads=32, num_kv_heads=8, max_blocks=1024, max_pages_per_row=2048)
     assert W.wise_workspace_layout(s)["max_items"] == 2 * 8 * 128
+    # the longest rows (4096 blocks, 128K tokens)
+    s = _shape(num_rows=2, num_q_heads=8, num_kv_heads=2, max_blocks=4096, max_pages_per_row=8192)
+    assert W.wise_workspace_layout(s)["max_items"] == 2 * 2 * 512
     # an explicit split size wins
     s = _shape(num_rows=2, num_q_heads=32, num_kv_heads=8, max_blocks=1024, max_pages_per_row=2048,
                tiles_per_item=16)
