@@ -90,13 +90,13 @@ def parse():
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--sparse-scaling", action="store_true",
                    help="time one sparse call (64 rows, 16 heads MHA, D=128) at contexts "
-                        "1K-32K with 8 selected tiles per (row, head), and at 8K with 1-256 "
+                        "1K-128K with 8 selected tiles per (row, head), and at 8K with 1-256 "
                         "selected tiles; prints one JSON line with the table")
     p.add_argument("--point", default=None, metavar="CONTEXT:TILES",
                    help="with --sparse-scaling: time only this point (e.g. 8192:1)")
     p.add_argument("--gqa", action="store_true",
                    help="with --sparse-scaling: 32 query / 8 KV heads (the tensor-core path), "
-                        "16 rows, contexts 4K-32K")
+                        "16 rows, contexts 4K-128K")
     p.add_argument("--shared-blocks", action="store_true",
                    help="with --sparse-scaling: every head of a row selects the same blocks")
     p.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -1280,12 +1280,14 @@ def sparse_scaling_main(args):
     """Sparse-mode time against the selected tiles and against the context.
 
     Each point is one sparse call over 64 rows (--rows) x 16 heads (MHA, D=128, bf16):
-    compaction, partial pass and finish, timed with CUDA events on the
-    launching stream (mean of 30 calls, the L2 flushed by a 512 MiB write
+    the work list built from the mask (wise_build_sparse_list), partial pass
+    and finish on it, and for contrast the same call on a compaction
+    (compaction, partial pass, finish); each launch timed with CUDA events on
+    the launching stream (mean of 30 calls, the L2 flushed by a 512 MiB write
     before each).  Sweep 1 holds 8 selected tiles per (row, head) and grows the
-    context 1K -> 32K; sweep 2 holds the context at 8K and grows the selected
-    tiles 1 -> 256 (every block).  The dense call at each context is timed the
-    same way for contrast."""
+    context 1K -> 128K (the K/V pool then holds 69 GB); sweep 2 holds the
+    context at 8K and grows the selected tiles 1 -> 256 (every block).  The
+    dense call at each context is timed the same way for contrast."""
     import numpy as np
     import torch
     import block_sparse_paged_split_gb300 as W
@@ -1299,11 +1301,11 @@ def sparse_scaling_main(args):
     if args.gqa:
         # Grouped-query heads (the tensor-core consumer): 32 query / 8 KV heads.
         R, H, Hq, D, reps = args.rows or 16, 8, 32, 128, 30
-        points = ([(L, 16, True) for L in (4096, 8192, 16384, 32768)] +
+        points = ([(L, 16, True) for L in (4096, 8192, 16384, 32768, 65536, 131072)] +
                   [(32768, k, False) for k in (1, 4, 64, 256, 1024)])
     else:
         R, H, Hq, D, reps = args.rows or 64, 16, 16, 128, 30
-        points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768)] +
+        points = ([(L, 8, True) for L in (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)] +
                   [(8192, k, False) for k in (1, 2, 4, 16, 32, 64, 128, 256)])
     peak, peak_kind = peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
@@ -1326,16 +1328,27 @@ def sparse_scaling_main(args):
         args_common = (d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                        d["page_table"].data_ptr(), d["seq_lens"].data_ptr())
 
-        def call(modes_t, sup):
+        def call(modes_t, sup, on_list):
             m = modes_t.data_ptr()
             t = []
-            for fn, a in ((lib.wise_compact_tiles, (S, m, args_common[4], sup.data_ptr(),
-                                                    ws.data_ptr(), ws.numel(), st)),
-                          (lib.wise_decode_partial, (S,) + args_common + (m, ws.data_ptr(),
-                                                                          ws.numel(), st)),
-                          (lib.wise_decode_finish, (S, m, args_common[4], ws.data_ptr(), ws.numel(),
-                                                    sup.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                                    st))):
+            if on_list:  # every row sparse: list 1 from the mask, both passes on it
+                L1 = ctypes.c_uint32(W.FLAG_SPARSE_LIST)
+                launches = ((lib.wise_build_sparse_list, (S, args_common[4], sup.data_ptr(),
+                                                          ws.data_ptr(), ws.numel(), st)),
+                            (lib.wise_decode_partial_ex, (S,) + args_common + (None, ws.data_ptr(),
+                                                                               ws.numel(), L1, st)),
+                            (lib.wise_decode_finish_ex, (S, None, args_common[4], ws.data_ptr(),
+                                                         ws.numel(), L1, None, out.data_ptr(),
+                                                         lse.data_ptr(), st)))
+            else:
+                launches = ((lib.wise_compact_tiles, (S, m, args_common[4], sup.data_ptr(),
+                                                      ws.data_ptr(), ws.numel(), st)),
+                            (lib.wise_decode_partial, (S,) + args_common + (m, ws.data_ptr(),
+                                                                            ws.numel(), st)),
+                            (lib.wise_decode_finish, (S, m, args_common[4], ws.data_ptr(),
+                                                      ws.numel(), sup.data_ptr(), out.data_ptr(),
+                                                      lse.data_ptr(), st)))
+            for fn, a in launches:
                 e = torch.cuda.Event(enable_timing=True)
                 e.record(stream)
                 t.append(e)
@@ -1347,11 +1360,11 @@ def sparse_scaling_main(args):
             t.append(e)
             return t
 
-        def timed(modes_t, sup):
+        def timed(modes_t, sup, on_list=False):
             calls, comp, parts, fin = [], [], [], []
             for i in range(reps + 3):
                 flush.fill_(i & 0xFF)
-                t = call(modes_t, sup)
+                t = call(modes_t, sup, on_list)
                 torch.cuda.synchronize()
                 if i >= 3:
                     calls.append(t[0].elapsed_time(t[3]) * 1e3)
@@ -1364,15 +1377,20 @@ def sparse_scaling_main(args):
                     statistics.fmean(fin))
 
         sparse = torch.full((R,), W.MODE_SPARSE, dtype=torch.int8, device="cuda")
-        call_us, part_us, comp_us, fin_us = timed(sparse, d["support"])
+        call_us, part_us, build_us, fin_us = timed(sparse, d["support"], on_list=True)
+        c_call_us, c_part_us, c_comp_us, c_fin_us = timed(sparse, d["support"])
         tiles = R * H * min(k, d["max_blocks"])
         sel_bytes = tiles * 32 * D * 2 * 2
         row = {"context": L, "selected_tiles_per_head": min(k, d["max_blocks"]),
-               "sparse_call_us": round(call_us, 2), "sparse_partial_us": round(part_us, 2),
-               "sparse_compact_us": round(comp_us, 2), "sparse_finish_us": round(fin_us, 2),
+               "sparse_call_us": round(call_us, 2), "sparse_build_us": round(build_us, 2),
+               "sparse_partial_us": round(part_us, 2), "sparse_finish_us": round(fin_us, 2),
                "selected_kv_bytes": sel_bytes,
                "partial_gbs": round(sel_bytes / (part_us * 1e-6) / 1e9, 1),
-               "partial_frac": round(sel_bytes / (part_us * 1e-6) / 1e9 / peak, 3)}
+               "partial_frac": round(sel_bytes / (part_us * 1e-6) / 1e9 / peak, 3),
+               "call_frac": round(sel_bytes / (call_us * 1e-6) / 1e9 / peak, 3),
+               "compaction_call_us": round(c_call_us, 2), "compaction_us": round(c_comp_us, 2),
+               "compaction_partial_us": round(c_part_us, 2),
+               "compaction_finish_us": round(c_fin_us, 2)}
         if with_dense:
             dense = torch.zeros((R,), dtype=torch.int8, device="cuda")
             dense_call, dense_part, _, _ = timed(dense, torch.zeros_like(d["support"]))

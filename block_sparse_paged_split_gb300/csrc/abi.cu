@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "list1.cuh"
 
 namespace wise {
 namespace {
@@ -344,6 +345,36 @@ wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
   if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
   const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
   return wise_compact_tiles_m(shape, modes, seq_lens, &m, workspace, workspace_bytes, stream);
+}
+
+wise_status wise_build_sparse_list_m(const wise_shape* shape, const int32_t* seq_lens,
+                                     const wise_mask* mask, void* workspace,
+                                     size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  WsView ws;
+  if ((st = make_view(shape, workspace, workspace_bytes, &ws)) != WISE_OK) return st;
+  if (shape->num_rows > 0 && !seq_lens) return fail(WISE_ERR_INVALID_ARG, "seq_lens is NULL");
+  MaskView mv;
+  if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
+  if (!mv.words) return fail(WISE_ERR_INVALID_ARG, "the list is built from the support mask");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // A new call: status word and queue counters back to 0, list 1's bucket
+  // counters too (the build appends to them).
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, s);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+  e = launch_build_sparse_list(make_params(shape), seq_lens, mv, ws, s);
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "sparse list launch");
+}
+
+wise_status wise_build_sparse_list(const wise_shape* shape, const int32_t* seq_lens,
+                                   const uint32_t* support, void* workspace,
+                                   size_t workspace_bytes, wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
+  const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
+  return wise_build_sparse_list_m(shape, seq_lens, &m, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -11,6 +11,7 @@
 // row's own mode, length and mask, so a row's result does not depend on the
 // rest of the batch.
 #include "internal.h"
+#include "list1.cuh"
 
 namespace wise {
 
@@ -246,6 +247,44 @@ __global__ void __cluster_dims__(kCompactCluster, 1, 1) __launch_bounds__(kCompa
 cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                            const MaskView& mv, const WsView& ws, cudaStream_t stream) {
   return launch_pdl(compact_kernel, dim3(kCompactCluster), dim3(kCompactThreads), 0, stream, modes,
+                    seq_lens, mv, ws, kp);
+}
+
+// ------------------------------------------------------------------ list 1 from a mask
+// The work list of an all-sparse call built from the mask alone: one CTA per
+// (row, KV head) copies the pair's mask words to shared memory and appends the
+// pair's items to list 1 (compact slots, one bucket per tile count: the list
+// a finish with WISE_FLAG_BUILD_SPARSE_LIST writes).  The work is the pair's
+// W words and its selected ranges, so the call's cost follows the selection,
+// where compaction visits every block range of every row.
+constexpr int kBuildThreads = 128;
+
+__global__ void __launch_bounds__(kBuildThreads)
+    build_sparse_list_kernel(const int32_t* __restrict__ seq_lens, const MaskView mv,
+                             const WsView ws, const KParams kp) {
+  __shared__ uint32_t words[WISE_MAX_BLOCKS / 32];
+  __shared__ List1Smem sm;
+  const int rg = blockIdx.x;
+  const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
+  grid_dependency_wait();  // the lengths and the mask may come from the kernel before
+  const int raw = seq_lens[r];
+  const int L = clamp_len(raw, kp.cap_tokens);
+  const uint32_t* mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // null: the row has no mask
+  if (threadIdx.x == 0 && g == 0 && raw > kp.cap_tokens)
+    flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
+  if (L == 0 || mw == nullptr) {  // nothing to attend: no item
+    if (threadIdx.x == 0) list1_empty_pair(ws, kp, rg);
+    return;
+  }
+  for (int i = threadIdx.x; i < kp.W; i += blockDim.x) words[i] = mw[i];
+  __syncthreads();
+  list1_build_pair(ws, kp, rg, L, words, sm);
+}
+
+cudaError_t launch_build_sparse_list(const KParams& kp, const int32_t* seq_lens,
+                                     const MaskView& mv, const WsView& ws, cudaStream_t stream) {
+  if (kp.R == 0) return cudaSuccess;
+  return launch_pdl(build_sparse_list_kernel, dim3(kp.R * kp.Hkv), dim3(kBuildThreads), 0, stream,
                     seq_lens, mv, ws, kp);
 }
 

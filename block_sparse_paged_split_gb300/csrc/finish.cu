@@ -617,6 +617,15 @@ static cudaError_t launch_finish_b(const KParams& kp, const int8_t* modes,
   if (can_fold_finish(kp))
     return launch_pdl(finish_short_kernel<T, kBuild>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0,
                       stream, modes, seq_lens, ws, kp, mv, static_cast<T*>(out), lse);
+  if (kp.list1) {
+    // Every row sparse: no selection, so no sort keys -- the warps only take
+    // the pair's split slots (at most S_max).  Sized by the row length (16
+    // warps and 4096 keys at 128K) the CTAs held 82 registers x 512 threads,
+    // one CTA an SM, and the finish of a 64-row sparse call grew from 8 to
+    // 30 us with the context at a fixed selection.
+    if (kp.S_max <= 32) return launch_long<T, 1, 4, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+    return launch_long<T, 1, 8, kBuild>(kp, modes, seq_lens, ws, mv, out, lse, stream);
+  }
   const int w = finish_warps(kp);
   const int e = finish_npad(kp) / (32 * w);
   if (w == 4) {

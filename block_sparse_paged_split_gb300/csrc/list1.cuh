@@ -50,8 +50,8 @@ __device__ __forceinline__ void list1_empty_pair(const WsView& ws, const KParams
 // Every thread of the CTA calls this (blockDim.x a multiple of 32): the items
 // of (row, KV head) rg, whose row holds L tokens and whose final mask words
 // are mw (shared memory), appended to list 1, and the pair's head info.
-__device__ __noinline__ void list1_build_pair(const WsView& ws, const KParams& kp, int rg,
-                                                 int L, const uint32_t* mw, List1Smem& sm) {
+static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KParams& kp, int rg,
+                                                        int L, const uint32_t* mw, List1Smem& sm) {
   const int th = threadIdx.x, nt = blockDim.x;
   const int lane = th & 31, warp = th >> 5, nw = nt >> 5;
   const int T = kp.T;
@@ -112,5 +112,13 @@ __device__ __noinline__ void list1_build_pair(const WsView& ws, const KParams& k
     carry += tot;
   }
 }
+
+// List 1 straight from a mask, for an all-sparse call whose mask no finish of
+// this workspace has just left (wise_build_sparse_list): one CTA per (row, KV
+// head) reads the pair's words and runs list1_build_pair on them.  Its
+// counters must be 0 when the kernel starts (the caller resets the
+// workspace header first).  Defined in compact.cu.
+cudaError_t launch_build_sparse_list(const KParams& kp, const int32_t* seq_lens,
+                                     const MaskView& mv, const WsView& ws, cudaStream_t stream);
 
 }  // namespace wise

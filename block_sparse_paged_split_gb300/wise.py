@@ -121,6 +121,8 @@ def library() -> ctypes.CDLL:
             "wise_selftest_wait_timeout": [P, P],
             "wise_noalloc_status": [ctypes.POINTER(ctypes.c_int32), P],
             "wise_compact_tiles_m": [S, P, P, ctypes.POINTER(wise_mask), P, SZ, P],
+            "wise_build_sparse_list": [S, P, P, P, SZ, P],
+            "wise_build_sparse_list_m": [S, P, ctypes.POINTER(wise_mask), P, SZ, P],
             "wise_decode_finish_m": [S, P, P, P, SZ, U32, ctypes.POINTER(wise_mask), P, P, P],
             "wise_decode_m": [S, P, P, P, P, P, P, ctypes.POINTER(wise_mask), P, P, P, SZ, P],
             "wise_validate_m": [S, P, P, P, ctypes.POINTER(wise_mask), P, P],
@@ -204,6 +206,15 @@ def alloc_workspace(shape: wise_shape, device=None) -> torch.Tensor:
 def wise_compact_tiles(shape, modes, seq_lens, support, workspace, stream=None) -> None:
     _check(library().wise_compact_tiles(
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(support, torch.int32, "support"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
+def wise_build_sparse_list(shape, seq_lens, support, workspace, stream=None) -> None:
+    """List 1 for a call in which every row is sparse, from the mask alone
+    (then wise_decode_partial_ex / wise_decode_finish_ex with FLAG_SPARSE_LIST)."""
+    _check(library().wise_build_sparse_list(
+        ctypes.byref(shape), _ptr(seq_lens, torch.int32, "seq_lens"),
         _ptr(support, torch.int32, "support"), _ptr(workspace, torch.uint8, "workspace"),
         workspace.numel(), _stream(stream)))
 
@@ -310,6 +321,12 @@ def wise_compact_tiles_m(shape, modes, seq_lens, mask: wise_mask, workspace, str
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
         ctypes.byref(mask), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _stream(stream)))
+
+
+def wise_build_sparse_list_m(shape, seq_lens, mask: wise_mask, workspace, stream=None) -> None:
+    _check(library().wise_build_sparse_list_m(
+        ctypes.byref(shape), _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.byref(mask),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def wise_decode_finish_m(shape, modes, seq_lens, workspace, mask: wise_mask, out, lse, flags=0,

@@ -25,7 +25,8 @@
  *
  * One call of the path, on one CUDA stream:
  *     wise_compact_tiles -> wise_decode_partial -> wise_decode_finish
- * (wise_decode runs all three).  wise_support_union ORs masks kept per depth.
+ * (wise_decode runs all three); a call in which every row is sparse may take
+ * its work list from wise_build_sparse_list instead of the compaction.  wise_support_union ORs masks kept per depth.
  * Variants from the pages' FlashAttention decode path, built for comparison:
  * wise_support_head_union (head-union masks) and wise_block_mass (block
  * masses from the LSE by a second read of K); wise_decode_partial_finish
@@ -237,6 +238,23 @@ wise_status wise_compact_tiles(const wise_shape *shape, const int8_t *modes,
                                void *workspace, size_t workspace_bytes,
                                wise_stream_t stream);
 
+/* The work list of a call in which every row is sparse, built from the mask
+ * alone [WISE PR, "What changes": sparse rows are compacted first]: list 1
+ * of the workspace, as a finish with WISE_FLAG_BUILD_SPARSE_LIST writes it
+ * (per (row, KV head): its k-th block range holding a selected tile is item
+ * k, a bitmap of the selected blocks of that range; items bucketed by tile
+ * count), for a partial pass and finish with WISE_FLAG_SPARSE_LIST.  Where
+ * compaction visits every block range of every row, this reads each (row,
+ * KV head)'s W mask words and writes one record per selected range, so the
+ * sparse call's cost follows its selection, not its rows' lengths.  Resets
+ * the workspace header (status word, counters), then writes list 1 and its
+ * head info; padding rows and masks selecting nothing get no item, and a
+ * length above the row's capacity is clamped and flagged.  support must not
+ * be NULL. */
+wise_status wise_build_sparse_list(const wise_shape *shape, const int32_t *seq_lens,
+                                   const uint32_t *support, void *workspace,
+                                   size_t workspace_bytes, wise_stream_t stream);
+
 /* Split partial pass [WISE PR, "What changes": split-KV paged decode with
  * per-row modes].  For every work item written by wise_compact_tiles and
  * every query head of its KV head: online softmax over the item's tiles,
@@ -290,11 +308,13 @@ enum {
    * masks selecting nothing get no item.  support must not be NULL, and the
    * call's partial pass must not be on list 1 (that pass, or a compaction,
    * empties list 1 for this finish to fill).  List 1 stays valid until the
-   * next partial pass that is not on it, or the next compaction. */
+   * next partial pass that is not on it, the next compaction or the next
+   * wise_build_sparse_list. */
   WISE_FLAG_BUILD_SPARSE_LIST = 4u,
   /* Partial pass and finish: every row is sparse and the work list is list 1
    * (written by an earlier finish with WISE_FLAG_BUILD_SPARSE_LIST over the
-   * same rows and lengths); modes is ignored and may be NULL.  Both passes of
+   * same rows and lengths, or by wise_build_sparse_list); modes is ignored
+   * and may be NULL.  Both passes of
    * the call take the flag.  Not with wise_decode_partial_finish. */
   WISE_FLAG_SPARSE_LIST = 8u,
   /* Partial pass and finish: every row attends every block below its length
@@ -370,7 +390,8 @@ wise_status wise_decode_partial_finish(const wise_shape *shape, const void *q,
 /* The calls that read or write the mask, with the mask addressed through a
  * wise_mask (per-request slots and a layer of a mask pool) instead of a
  * [num_rows, num_kv_heads, W] array; otherwise as wise_compact_tiles,
- * wise_decode_finish_ex, wise_decode and wise_validate.  `mask` is a HOST
+ * wise_build_sparse_list, wise_decode_finish_ex, wise_decode and
+ * wise_validate (a row without a mask slot gets no item in list 1).  `mask` is a HOST
  * pointer to the descriptor (its words and row_slot are device pointers);
  * mask->words may be NULL where the flat call's support may be NULL.  The
  * compaction reads each row's slot with its mode and length. */
@@ -378,6 +399,9 @@ wise_status wise_compact_tiles_m(const wise_shape *shape, const int8_t *modes,
                                  const int32_t *seq_lens, const wise_mask *mask,
                                  void *workspace, size_t workspace_bytes,
                                  wise_stream_t stream);
+wise_status wise_build_sparse_list_m(const wise_shape *shape, const int32_t *seq_lens,
+                                     const wise_mask *mask, void *workspace,
+                                     size_t workspace_bytes, wise_stream_t stream);
 wise_status wise_decode_finish_m(const wise_shape *shape, const int8_t *modes,
                                  const int32_t *seq_lens, void *workspace,
                                  size_t workspace_bytes, uint32_t flags,

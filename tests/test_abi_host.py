@@ -208,6 +208,24 @@ def test_noalloc_status_rejects_a_null_pointer(lib):
     assert b"host_status" in lib.wise_last_error()
 
 
+def test_build_sparse_list_checks(lib):
+    """wise_build_sparse_list: the mask and the lengths are required, the
+    workspace is checked; all before anything is enqueued."""
+    P = ctypes.c_void_p
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    assert lib.wise_build_sparse_list(ctypes.byref(s), P(16), None, P(4096), n, None) == 1
+    assert b"support" in lib.wise_last_error()
+    assert lib.wise_build_sparse_list(ctypes.byref(s), None, P(16), P(4096), n, None) == 1
+    assert lib.wise_build_sparse_list(ctypes.byref(s), P(16), P(16), P(4096), n - 1, None) == 3
+    assert lib.wise_build_sparse_list(ctypes.byref(s), P(16), P(16), P(4100), n, None) == 3
+    assert lib.wise_build_sparse_list(ctypes.byref(s), P(16), P(18), P(4096), n, None) == 1
+    m = W.wise.wise_mask(None, None, 0, 0)
+    assert lib.wise_build_sparse_list_m(ctypes.byref(s), P(16), ctypes.byref(m), P(4096), n,
+                                        None) == 1
+    assert lib.wise_build_sparse_list_m(ctypes.byref(s), P(16), None, P(4096), n, None) == 1
+
+
 def test_max_blocks_limit(lib):
     """WISE_MAX_BLOCKS (rows of up to 128K tokens): the header, the binding and
     the shape check agree."""

@@ -78,8 +78,9 @@ def test_gpu_arm_line():
 @pytest.mark.gpu
 def test_sparse_scaling_point():
     """One point of the sparse-scaling measurement (8 rows, 4K context, 8
-    selected tiles per head): per-kernel times that add up to the call, and
-    selected bytes equal to rows x heads x tiles x 32 tokens x 512 B."""
+    selected tiles per head): per-kernel times that add up to the call, on the
+    list built from the mask and on a compaction, and selected bytes equal to
+    rows x heads x tiles x 32 tokens x 512 B."""
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--sparse-scaling",
                           "--point", "4096:8", "--rows", "8"],
                          capture_output=True, text=True, timeout=600, cwd=ROOT)
@@ -88,9 +89,11 @@ def test_sparse_scaling_point():
     (pt,) = out["sparse_scaling"]
     assert pt["context"] == 4096 and pt["selected_tiles_per_head"] == 8 and out["rows"] == 8
     assert pt["selected_kv_bytes"] == 8 * 16 * 8 * 32 * 512
-    parts = pt["sparse_compact_us"] + pt["sparse_partial_us"] + pt["sparse_finish_us"]
+    parts = pt["sparse_build_us"] + pt["sparse_partial_us"] + pt["sparse_finish_us"]
     assert 0 < parts <= pt["sparse_call_us"] * 1.01
-    assert 0 < pt["partial_frac"] < 1.5
+    parts = pt["compaction_us"] + pt["compaction_partial_us"] + pt["compaction_finish_us"]
+    assert 0 < parts <= pt["compaction_call_us"] * 1.01
+    assert 0 < pt["partial_frac"] < 1.5 and 0 < pt["call_frac"] <= pt["partial_frac"]
 
 
 @pytest.mark.gpu

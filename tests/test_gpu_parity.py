@@ -548,7 +548,7 @@ def test_seq_len_above_capacity_is_clamped_and_flagged():
 
 
 # Long rows take the multi-warp finish kernel: one CTA of W warps per query
-# head (4 up to 512 blocks, 8 beyond), the KV head's query heads as one
+# head (4 up to 512 blocks, 8 up to 1024, 16 beyond), the KV head's query heads as one
 # thread-block cluster; its sort keeps E = (padded block count) / (32 W) keys
 # per thread.  One case per layout and cluster size.
 LONG_CASES = [
