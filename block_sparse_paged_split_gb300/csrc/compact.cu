@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kBuildThreads)
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   grid_dependency_wait();  // the lengths and the mask may come from the kernel before
+  grid_dependents_launch();  // the partial pass may start its prologue now
   const int raw = seq_lens[r];
   const int L = clamp_len(raw, kp.cap_tokens);
   const uint32_t* mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // null: the row has no mask
