@@ -86,6 +86,9 @@ def parse():
     p.add_argument("--no-sparse-list", action="store_true",
                    help="sparse depths get their own compaction instead of the work list the "
                         "previous depth's finish builds")
+    p.add_argument("--mixed-list", action="store_true",
+                   help="depths that mix sparse rows with others take their work list from "
+                        "wise_build_list (run with WISE_FLAG_LIST_MODES) instead of a compaction")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--sparse-scaling", action="store_true",
@@ -349,7 +352,7 @@ class Pipeline:
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
                  lse_discover: bool = False, overlap: bool = False, share=None,
                  sparse_list: bool = True, device_inputs: bool = False, dense_list: bool = True,
-                 early_lists: bool = False):
+                 early_lists: bool = False, mixed_list: bool = False):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -440,14 +443,28 @@ class Pipeline:
         # with the sparse list the step launches no compaction at all.
         self.dense_list = (dense_list and w.num_rows <= W.DENSE_LIST_MAX_ROWS and
                            not (fold or overlap or head_union or lse_discover))
+        # mixed_list=True: a depth that mixes sparse rows with others (and is
+        # not itself building or on list 1) gets its work list from
+        # wise_build_list for its modes instead of a compaction.
+        self.mixed_list = mixed_list and not (fold or overlap or head_union or lse_discover)
         # A list-derived pass needs the workspace's queue counters at 0.
         W.wise_workspace_reset(self.shape, self.ws)
 
         def calls(modes_t, t, compact=True, early=False, build=False, on_list=False, dense=False,
-                  list_ready=False, alt=False):
+                  list_ready=False, alt=False, list_modes=False):
             d = self.depth[t]
             m = modes_t.data_ptr()
             c = []
+            if list_modes:
+                f = W.FLAG_SPARSE_LIST | W.FLAG_LIST_MODES
+                c.append(("build_list", lib.wise_build_list, (S, m, sl, sup, ws, nws, st)))
+                c.append(("partial", lib.wise_decode_partial_ex,
+                          (S, d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                           pt, sl, m, ws, nws, f, st)))
+                c.append(("finish", lib.wise_decode_finish_ex,
+                          (S, m, sl, ws, nws, f, sup, self.out[t].data_ptr(),
+                           self.lse[t].data_ptr(), st)))
+                return c
             # alt: consecutive depths take the workspace's two slot sets in
             # turn, so a depth on the dense list, or on a list built before
             # the previous finish, starts while that finish still runs
@@ -593,6 +610,11 @@ class Pipeline:
                                              build=build, on_list=on_list, dense=dense,
                                              list_ready=list_ready, alt=self.early_lists)))
                 list0 = build and not dense
+                continue
+            if self.mixed_list and any(int(x) == W.MODE_SPARSE for x in dm[t]):
+                self.wise_step.append((t, depth_name(dm[t]),
+                                       calls(self.modes[t], t, list_modes=True)))
+                listed = False  # list 1 now holds this depth's list, not an all-sparse one
                 continue
             list0 = True
             c = calls(self.modes[t], t, compact=not reuse, early=reuse)
@@ -982,7 +1004,7 @@ def sweep_workload(name, args, steps, peak):
     w = make_workload(name, **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
                     device_inputs=True, dense_list=not args.no_dense_list,
-                    early_lists=args.early)
+                    early_lists=args.early, mixed_list=args.mixed_list)
     for _ in range(3):
         pipe.run(pipe.wise_step)
         pipe.run(pipe.dense_step)
@@ -1033,7 +1055,7 @@ def eta_point(name, eta, args, steps):
     w = make_workload(name, eta=eta)
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
                     device_inputs=True, dense_list=not args.no_dense_list,
-                    early_lists=args.early)
+                    early_lists=args.early, mixed_list=args.mixed_list)
     for _ in range(3):
         pipe.run(pipe.wise_step)
     torch.cuda.synchronize()
@@ -1080,7 +1102,7 @@ def main_ours(args):
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
                     lse_discover=args.lse_discover, overlap=args.overlap,
                     sparse_list=not args.no_sparse_list, dense_list=not args.no_dense_list,
-                    early_lists=args.early)
+                    early_lists=args.early, mixed_list=args.mixed_list)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -1163,7 +1185,7 @@ def main_ours(args):
                       head_union=args.head_union, lse_discover=args.lse_discover,
                       overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list,
                       dense_list=not args.no_dense_list,
-                    early_lists=args.early)
+                    early_lists=args.early, mixed_list=args.mixed_list)
     graph_b = pipe_b.graph(pipe_b.wise_step)
     e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
     e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)
@@ -1216,7 +1238,9 @@ def main_ours(args):
                                   "row lengths (no compaction launch)" if pipe.dense_list else "")
                                + (", consecutive depths on alternate slot sets, a depth on the "
                                   "dense list or a ready list starting beside the previous finish"
-                                  if pipe.early_lists else ""),
+                                  if pipe.early_lists else "")
+                               + (", mixed depths on a work list built from their modes and masks "
+                                  "(no compaction launch)" if pipe.mixed_list else ""),
                    "rows_per_step": rows_per_step, "parallelism": f"replicas x{world} (rows independent)",
                    "l2": f"inputs larger than L2: "
                          f"{w.num_depths * pipe.kv_bytes(np.zeros(w.num_rows, np.int8)) / 1e9:.2f} GB "

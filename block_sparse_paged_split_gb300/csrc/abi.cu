@@ -347,9 +347,9 @@ wise_status wise_compact_tiles(const wise_shape* shape, const int8_t* modes,
   return wise_compact_tiles_m(shape, modes, seq_lens, &m, workspace, workspace_bytes, stream);
 }
 
-wise_status wise_build_sparse_list_m(const wise_shape* shape, const int32_t* seq_lens,
-                                     const wise_mask* mask, void* workspace,
-                                     size_t workspace_bytes, wise_stream_t stream) {
+wise_status wise_build_list_m(const wise_shape* shape, const int8_t* modes,
+                              const int32_t* seq_lens, const wise_mask* mask, void* workspace,
+                              size_t workspace_bytes, wise_stream_t stream) {
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   WsView ws;
@@ -357,14 +357,32 @@ wise_status wise_build_sparse_list_m(const wise_shape* shape, const int32_t* seq
   if (shape->num_rows > 0 && !seq_lens) return fail(WISE_ERR_INVALID_ARG, "seq_lens is NULL");
   MaskView mv;
   if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
-  if (!mv.words) return fail(WISE_ERR_INVALID_ARG, "the list is built from the support mask");
+  if (!modes && !mv.words)
+    return fail(WISE_ERR_INVALID_ARG, "an all-sparse list is built from the support mask");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // A new call: status word and queue counters back to 0, list 1's bucket
   // counters too (the build appends to them).
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
-  e = launch_build_sparse_list(make_params(shape), seq_lens, mv, ws, s);
-  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "sparse list launch");
+  e = launch_build_list(make_params(shape), modes, seq_lens, mv, ws, s);
+  return e == cudaSuccess ? WISE_OK : cuda_fail(e, "list build launch");
+}
+
+wise_status wise_build_list(const wise_shape* shape, const int8_t* modes, const int32_t* seq_lens,
+                            const uint32_t* support, void* workspace, size_t workspace_bytes,
+                            wise_stream_t stream) {
+  wise_status st = check_shape(shape);
+  if (st != WISE_OK) return st;
+  if (shape->num_rows > 0 && !modes) return fail(WISE_ERR_INVALID_ARG, "modes is NULL");
+  if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
+  const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
+  return wise_build_list_m(shape, modes, seq_lens, &m, workspace, workspace_bytes, stream);
+}
+
+wise_status wise_build_sparse_list_m(const wise_shape* shape, const int32_t* seq_lens,
+                                     const wise_mask* mask, void* workspace,
+                                     size_t workspace_bytes, wise_stream_t stream) {
+  return wise_build_list_m(shape, nullptr, seq_lens, mask, workspace, workspace_bytes, stream);
 }
 
 wise_status wise_build_sparse_list(const wise_shape* shape, const int32_t* seq_lens,
@@ -374,7 +392,7 @@ wise_status wise_build_sparse_list(const wise_shape* shape, const int32_t* seq_l
   if (st != WISE_OK) return st;
   if (support && !aligned(support, 4)) return fail(WISE_ERR_INVALID_ARG, "support misaligned");
   const wise_mask m{const_cast<uint32_t*>(support), nullptr, 0, 0};
-  return wise_build_sparse_list_m(shape, seq_lens, &m, workspace, workspace_bytes, stream);
+  return wise_build_list_m(shape, nullptr, seq_lens, &m, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
@@ -389,8 +407,10 @@ wise_status partial_pass(const wise_shape* shape, const void* q, const void* k_c
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_EARLY_START | WISE_FLAG_SPARSE_LIST |
-                          WISE_FLAG_DENSE_LIST | WISE_FLAG_INPUTS_READY))
+                          WISE_FLAG_DENSE_LIST | WISE_FLAG_INPUTS_READY | WISE_FLAG_LIST_MODES))
     return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((flags & WISE_FLAG_LIST_MODES) && !(flags & WISE_FLAG_SPARSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_LIST_MODES goes with WISE_FLAG_SPARSE_LIST");
   if ((flags & (WISE_FLAG_SPARSE_LIST | WISE_FLAG_DENSE_LIST)) && fa.out)
     return fail(WISE_ERR_INVALID_ARG, "the folded finish takes neither list flag");
   if ((flags & WISE_FLAG_SPARSE_LIST) && (flags & WISE_FLAG_DENSE_LIST))
@@ -478,8 +498,10 @@ wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
   wise_status st = check_shape(shape);
   if (st != WISE_OK) return st;
   if (flags & ~(uint32_t)(WISE_FLAG_SLOT_SET_1 | WISE_FLAG_BUILD_SPARSE_LIST | WISE_FLAG_SPARSE_LIST |
-                          WISE_FLAG_DENSE_LIST))
+                          WISE_FLAG_DENSE_LIST | WISE_FLAG_LIST_MODES))
     return fail(WISE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((flags & WISE_FLAG_LIST_MODES) && !(flags & WISE_FLAG_SPARSE_LIST))
+    return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_LIST_MODES goes with WISE_FLAG_SPARSE_LIST");
   if ((flags & WISE_FLAG_SPARSE_LIST) && (flags & WISE_FLAG_DENSE_LIST))
     return fail(WISE_ERR_INVALID_ARG, "WISE_FLAG_SPARSE_LIST and WISE_FLAG_DENSE_LIST exclude each other");
   if ((flags & WISE_FLAG_DENSE_LIST) && shape->num_rows > WISE_DENSE_LIST_MAX_ROWS)
@@ -489,7 +511,8 @@ wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
   if ((st = make_view(shape, workspace, workspace_bytes, &ws, (flags & WISE_FLAG_SLOT_SET_1) ? 1 : 0)) != WISE_OK)
     return st;
   if (shape->num_rows == 0) return WISE_OK;
-  if ((!modes && !(flags & WISE_FLAG_SPARSE_LIST)) || !seq_lens || !out || !lse)
+  const bool list_modes = (flags & WISE_FLAG_LIST_MODES) != 0;
+  if ((!modes && (list_modes || !(flags & WISE_FLAG_SPARSE_LIST))) || !seq_lens || !out || !lse)
     return fail(WISE_ERR_INVALID_ARG, "a required pointer is NULL");
   MaskView mv;
   if ((st = mask_view(shape, mask, &mv)) != WISE_OK) return st;
@@ -504,7 +527,10 @@ wise_status wise_decode_finish_m(const wise_shape* shape, const int8_t* modes,
   kp.build = (flags & WISE_FLAG_BUILD_SPARSE_LIST) ? 1 : 0;
   kp.list1 = (flags & WISE_FLAG_SPARSE_LIST) ? 1 : 0;
   kp.dense_list = (flags & WISE_FLAG_DENSE_LIST) ? 1 : 0;
-  cudaError_t e = launch_finish(shape->dtype, kp, modes, seq_lens, ws, mv, out, lse,
+  // On list 1 the finish sees the modes only when the list was built for
+  // them; without them every row is sparse.
+  const int8_t* kmodes = (kp.list1 && !list_modes) ? nullptr : modes;
+  cudaError_t e = launch_finish(shape->dtype, kp, kmodes, seq_lens, ws, mv, out, lse,
                                 reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : cuda_fail(e, "finish launch");
 }

@@ -250,42 +250,51 @@ cudaError_t launch_compact(const KParams& kp, const int8_t* modes, const int32_t
                     seq_lens, mv, ws, kp);
 }
 
-// ------------------------------------------------------------------ list 1 from a mask
-// The work list of an all-sparse call built from the mask alone: one CTA per
-// (row, KV head) copies the pair's mask words to shared memory and appends the
-// pair's items to list 1 (compact slots, one bucket per tile count: the list
-// a finish with WISE_FLAG_BUILD_SPARSE_LIST writes).  The work is the pair's
-// W words and its selected ranges, so the call's cost follows the selection,
-// where compaction visits every block range of every row.
+// ------------------------------------------------------------------ list 1 from the modes and masks
+// The work list of a call built from its rows' modes, lengths and masks alone:
+// one CTA per (row, KV head) appends the pair's items to list 1 (compact
+// slots, one bucket per tile count: the list a finish with
+// WISE_FLAG_BUILD_SPARSE_LIST writes) -- a sparse row's selected ranges, from
+// its mask words copied to shared memory, or every range of a dense or
+// discover row.  modes null: every row sparse.  The work is the pair's W words
+// and its ranges with a tile to attend, so an all-sparse call's cost follows
+// the selection, where compaction visits every block range of every row.
 constexpr int kBuildThreads = 128;
 
 __global__ void __launch_bounds__(kBuildThreads)
-    build_sparse_list_kernel(const int32_t* __restrict__ seq_lens, const MaskView mv,
-                             const WsView ws, const KParams kp) {
+    build_list_kernel(const int8_t* __restrict__ modes, const int32_t* __restrict__ seq_lens,
+                      const MaskView mv, const WsView ws, const KParams kp) {
   __shared__ uint32_t words[WISE_MAX_BLOCKS / 32];
   __shared__ List1Smem sm;
   const int rg = blockIdx.x;
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
-  grid_dependency_wait();  // the lengths and the mask may come from the kernel before
+  grid_dependency_wait();  // the inputs and the mask may come from the kernel before
   grid_dependents_launch();  // the partial pass may start its prologue now
   const int raw = seq_lens[r];
   const int L = clamp_len(raw, kp.cap_tokens);
-  const uint32_t* mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // null: the row has no mask
+  const int mode = modes ? (int)modes[r] : (int)WISE_MODE_SPARSE;
+  const bool sparse = mode == WISE_MODE_SPARSE;
+  const uint32_t* mw = sparse ? mask_of(mv, mask_slot(mv, r), g, kp.W) : nullptr;
   if (threadIdx.x == 0 && g == 0 && raw > kp.cap_tokens)
     flag_error(ws.status, WISE_DEVERR_SEQ_LEN_CLAMPED);
-  if (L == 0 || mw == nullptr) {  // nothing to attend: no item
+  if (L == 0 || (sparse && mw == nullptr)) {  // nothing to attend: no item
     if (threadIdx.x == 0) list1_empty_pair(ws, kp, rg);
     return;
   }
-  for (int i = threadIdx.x; i < kp.W; i += blockDim.x) words[i] = mw[i];
-  __syncthreads();
-  list1_build_pair(ws, kp, rg, L, words, sm);
+  if (sparse) {
+    for (int i = threadIdx.x; i < kp.W; i += blockDim.x) words[i] = mw[i];
+    __syncthreads();
+  }
+  const int flags = sparse ? kItemSparse
+                           : (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION
+                                  ? kItemDiscover : 0);
+  list1_build_pair(ws, kp, rg, L, words, !sparse, flags, sm);
 }
 
-cudaError_t launch_build_sparse_list(const KParams& kp, const int32_t* seq_lens,
-                                     const MaskView& mv, const WsView& ws, cudaStream_t stream) {
+cudaError_t launch_build_list(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
+                              const MaskView& mv, const WsView& ws, cudaStream_t stream) {
   if (kp.R == 0) return cudaSuccess;
-  return launch_pdl(build_sparse_list_kernel, dim3(kp.R * kp.Hkv), dim3(kBuildThreads), 0, stream,
+  return launch_pdl(build_list_kernel, dim3(kp.R * kp.Hkv), dim3(kBuildThreads), 0, stream, modes,
                     seq_lens, mv, ws, kp);
 }
 

@@ -321,7 +321,9 @@ __global__ void __launch_bounds__(W * 32)
   const int r = rg / kp.Hkv, g = rg - r * kp.Hkv;
   const int h = g * G + hgrp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
-  const int mode = kp.list1 ? (int)WISE_MODE_SPARSE : (int)modes[r];
+  // On list 1 every row is sparse, unless the list was built for the call's
+  // modes (wise_build_list; the modes are then passed).
+  const int mode = (kp.list1 && !modes) ? (int)WISE_MODE_SPARSE : (int)modes[r];
   const int nb = (L + kTile - 1) / kTile;
   uint32_t* const mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // the pair's mask, or null
   const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(W * 32)
     if (kBuild && hgrp == 0) {
       if (th < kp.W) fwords[th] = old_word;
       __syncthreads();
-      list1_build_pair(ws, kp, rg, L, fwords, l1sm);
+      list1_build_pair(ws, kp, rg, L, fwords, false, kItemSparse, l1sm);
     }
     return;
   }
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(W * 32)
   }
   cluster_arrive();  // no CTA leaves while the group's first CTA may still read it
   cluster_wait();
-  if (kBuild && hgrp == 0) list1_build_pair(ws, kp, rg, L, fwords, l1sm);
+  if (kBuild && hgrp == 0) list1_build_pair(ws, kp, rg, L, fwords, false, kItemSparse, l1sm);
 }
 
 // ------------------------------------------------------------------ short rows
@@ -509,7 +511,9 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h = g * kp.G + warp;
   const int L = clamp_len(seq_lens[r], kp.cap_tokens);
-  const int mode = kp.list1 ? (int)WISE_MODE_SPARSE : (int)modes[r];
+  // On list 1 every row is sparse, unless the list was built for the call's
+  // modes (wise_build_list; the modes are then passed).
+  const int mode = (kp.list1 && !modes) ? (int)WISE_MODE_SPARSE : (int)modes[r];
   const int nb = (L + kTile - 1) / kTile;
   uint32_t* const mw = mask_of(mv, mask_slot(mv, r), g, kp.W);  // the pair's mask, or null
   const bool disc = (mode == WISE_MODE_DISCOVER || mode == WISE_MODE_DISCOVER_UNION) && mw != nullptr;
@@ -567,7 +571,7 @@ __global__ void __launch_bounds__(256)
   }
   if (!kBuild) return;
   __syncthreads();
-  list1_build_pair(ws, kp, rg, L, fwords, l1sm);
+  list1_build_pair(ws, kp, rg, L, fwords, false, kItemSparse, l1sm);
 }
 
 // Rows of at most 64 blocks and 8 split slots (can_fold_finish) take the
@@ -617,7 +621,7 @@ static cudaError_t launch_finish_b(const KParams& kp, const int8_t* modes,
   if (can_fold_finish(kp))
     return launch_pdl(finish_short_kernel<T, kBuild>, dim3(kp.R * kp.Hkv), dim3(32 * kp.G), 0,
                       stream, modes, seq_lens, ws, kp, mv, static_cast<T*>(out), lse);
-  if (kp.list1) {
+  if (kp.list1 && !modes) {
     // Every row sparse: no selection, so no sort keys -- the warps only take
     // the pair's split slots (at most S_max).  Sized by the row length (16
     // warps and 4096 keys at 128K) the CTAs held 82 registers x 512 threads,

@@ -47,11 +47,22 @@ __device__ __forceinline__ void list1_empty_pair(const WsView& ws, const KParams
   ws.head_info_1[rg] = make_int4(rg * kp.S_max, 0, 0, 0);
 }
 
+// Every blocks of range s below nb (a row that attends all its blocks).
+__device__ __forceinline__ uint32_t list1_range_full(int s, int T, int nb) {
+  const int lo = s * T;
+  if (lo >= nb) return 0u;
+  const int n = min(T, nb - lo);
+  return n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+}
+
 // Every thread of the CTA calls this (blockDim.x a multiple of 32): the items
-// of (row, KV head) rg, whose row holds L tokens and whose final mask words
-// are mw (shared memory), appended to list 1, and the pair's head info.
+// of (row, KV head) rg, whose row holds L tokens, appended to list 1, and the
+// pair's head info.  full: every block of the row (a dense or discover row);
+// otherwise the blocks selected in the mask words mw (shared memory).  flags:
+// the row's mode flags for the records (kItemSparse, kItemDiscover).
 static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KParams& kp, int rg,
-                                                        int L, const uint32_t* mw, List1Smem& sm) {
+                                                        int L, const uint32_t* mw, bool full,
+                                                        int flags, List1Smem& sm) {
   const int th = threadIdx.x, nt = blockDim.x;
   const int lane = th & 31, warp = th >> 5, nw = nt >> 5;
   const int T = kp.T;
@@ -63,7 +74,7 @@ static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KPa
   }
   __syncthreads();
   for (int s = th; s < nr; s += nt) {
-    const int n = __popc(list1_range_bits(mw, s, T, nb));
+    const int n = __popc(full ? list1_range_full(s, T, nb) : list1_range_bits(mw, s, T, nb));
     if (n) atomicAdd(&sm.hist[n - 1], 1);
   }
   __syncthreads();
@@ -85,7 +96,8 @@ static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KPa
   int carry = 0;
   for (int base = 0; base < nr; base += nt) {
     const int s = base + th;
-    const uint32_t bits = s < nr ? list1_range_bits(mw, s, T, nb) : 0u;
+    const uint32_t bits =
+        s >= nr ? 0u : (full ? list1_range_full(s, T, nb) : list1_range_bits(mw, s, T, nb));
     const int n = __popc(bits);
     const unsigned bal = __ballot_sync(kFull, n > 0);
     if (lane == 0) sm.wcnt[warp] = __popc(bal);
@@ -105,7 +117,7 @@ static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KPa
       // call came out of order and the item is dropped.
       if (pos >= 0 && pos < ws.max_items)
         ws.items_1[(size_t)(n - 1) * ws.max_items + pos] =
-            make_int4(rg, s | (k << 16), (int)(bits | ((uint32_t)n << 16)), L | kItemSparse);
+            make_int4(rg, s | (k << 16), (int)(bits | ((uint32_t)n << 16)), L | flags);
       else
         flag_error(ws.status, WISE_DEVERR_BAD_WORK_LIST);
     }
@@ -113,12 +125,12 @@ static __device__ __noinline__ void list1_build_pair(const WsView& ws, const KPa
   }
 }
 
-// List 1 straight from a mask, for an all-sparse call whose mask no finish of
-// this workspace has just left (wise_build_sparse_list): one CTA per (row, KV
-// head) reads the pair's words and runs list1_build_pair on them.  Its
-// counters must be 0 when the kernel starts (the caller resets the
+// List 1 straight from the rows' modes, lengths and masks (wise_build_list;
+// modes null: every row sparse, wise_build_sparse_list): one CTA per (row, KV
+// head) runs list1_build_pair on the pair's mask words or its whole length.
+// Its counters must be 0 when the kernel starts (the caller resets the
 // workspace header first).  Defined in compact.cu.
-cudaError_t launch_build_sparse_list(const KParams& kp, const int32_t* seq_lens,
-                                     const MaskView& mv, const WsView& ws, cudaStream_t stream);
+cudaError_t launch_build_list(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
+                              const MaskView& mv, const WsView& ws, cudaStream_t stream);
 
 }  // namespace wise

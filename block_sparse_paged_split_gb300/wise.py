@@ -123,6 +123,8 @@ def library() -> ctypes.CDLL:
             "wise_compact_tiles_m": [S, P, P, ctypes.POINTER(wise_mask), P, SZ, P],
             "wise_build_sparse_list": [S, P, P, P, SZ, P],
             "wise_build_sparse_list_m": [S, P, ctypes.POINTER(wise_mask), P, SZ, P],
+            "wise_build_list": [S, P, P, P, P, SZ, P],
+            "wise_build_list_m": [S, P, P, ctypes.POINTER(wise_mask), P, SZ, P],
             "wise_decode_finish_m": [S, P, P, P, SZ, U32, ctypes.POINTER(wise_mask), P, P, P],
             "wise_decode_m": [S, P, P, P, P, P, P, ctypes.POINTER(wise_mask), P, P, P, SZ, P],
             "wise_validate_m": [S, P, P, P, ctypes.POINTER(wise_mask), P, P],
@@ -219,6 +221,16 @@ def wise_build_sparse_list(shape, seq_lens, support, workspace, stream=None) -> 
         workspace.numel(), _stream(stream)))
 
 
+def wise_build_list(shape, modes, seq_lens, support, workspace, stream=None) -> None:
+    """List 1 for a call of any modes (then wise_decode_partial_ex /
+    wise_decode_finish_ex with FLAG_SPARSE_LIST | FLAG_LIST_MODES and the same
+    modes); support may be None."""
+    _check(library().wise_build_list(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(support, torch.int32, "support"), _ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
 def wise_decode_partial(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                         stream=None) -> None:
     e = _elem(shape)
@@ -244,6 +256,7 @@ FLAG_BUILD_SPARSE_LIST = 4
 FLAG_SPARSE_LIST = 8
 FLAG_DENSE_LIST = 16
 FLAG_INPUTS_READY = 32
+FLAG_LIST_MODES = 64
 DENSE_LIST_MAX_ROWS = 256
 MAX_BLOCKS = 4096  # WISE_MAX_BLOCKS: largest max_blocks (rows of up to 128K tokens)
 
@@ -251,7 +264,7 @@ MAX_BLOCKS = 4096  # WISE_MAX_BLOCKS: largest max_blocks (rows of up to 128K tok
 def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, modes, workspace,
                            flags=0, stream=None) -> None:
     """flags: FLAG_SLOT_SET_1, FLAG_EARLY_START, FLAG_SPARSE_LIST (modes may
-    then be None), FLAG_DENSE_LIST, FLAG_INPUTS_READY."""
+    then be None), FLAG_DENSE_LIST, FLAG_INPUTS_READY, FLAG_LIST_MODES."""
     e = _elem(shape)
     _check(library().wise_decode_partial_ex(
         ctypes.byref(shape), _ptr(q, e, "q"), _ptr(k_cache, e, "k_cache"), _ptr(v_cache, e, "v_cache"),
@@ -263,7 +276,8 @@ def wise_decode_partial_ex(shape, q, k_cache, v_cache, page_table, seq_lens, mod
 def wise_decode_finish_ex(shape, modes, seq_lens, workspace, support, out, lse, flags=0,
                           stream=None) -> None:
     """flags: FLAG_SLOT_SET_1, FLAG_BUILD_SPARSE_LIST, FLAG_SPARSE_LIST (modes
-    may then be None), FLAG_DENSE_LIST."""
+    may then be None), FLAG_DENSE_LIST, FLAG_LIST_MODES (with FLAG_SPARSE_LIST:
+    the list came from wise_build_list for these modes)."""
     e = _elem(shape)
     _check(library().wise_decode_finish_ex(
         ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
@@ -327,6 +341,13 @@ def wise_build_sparse_list_m(shape, seq_lens, mask: wise_mask, workspace, stream
     _check(library().wise_build_sparse_list_m(
         ctypes.byref(shape), _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.byref(mask),
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def wise_build_list_m(shape, modes, seq_lens, mask: wise_mask, workspace, stream=None) -> None:
+    _check(library().wise_build_list_m(
+        ctypes.byref(shape), _ptr(modes, torch.int8, "modes"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.byref(mask), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
 
 
 def wise_decode_finish_m(shape, modes, seq_lens, workspace, mask: wise_mask, out, lse, flags=0,

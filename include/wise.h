@@ -25,8 +25,9 @@
  *
  * One call of the path, on one CUDA stream:
  *     wise_compact_tiles -> wise_decode_partial -> wise_decode_finish
- * (wise_decode runs all three); a call in which every row is sparse may take
- * its work list from wise_build_sparse_list instead of the compaction.  wise_support_union ORs masks kept per depth.
+ * (wise_decode runs all three); a call may take its work list from
+ * wise_build_list (wise_build_sparse_list when every row is sparse) instead
+ * of the compaction.  wise_support_union ORs masks kept per depth.
  * Variants from the pages' FlashAttention decode path, built for comparison:
  * wise_support_head_union (head-union masks) and wise_block_mass (block
  * masses from the LSE by a second read of K); wise_decode_partial_finish
@@ -255,6 +256,19 @@ wise_status wise_build_sparse_list(const wise_shape *shape, const int32_t *seq_l
                                    const uint32_t *support, void *workspace,
                                    size_t workspace_bytes, wise_stream_t stream);
 
+/* The work list of a call of any modes, built from the rows' modes, lengths
+ * and masks as wise_build_sparse_list builds an all-sparse one: each sparse
+ * row's selected ranges, every block range of a dense or discover row (with
+ * the discover flag, so the partial pass records tile statistics); padding
+ * rows and sparse rows without a selected block get no item.  The call then
+ * runs its partial pass and finish with WISE_FLAG_SPARSE_LIST |
+ * WISE_FLAG_LIST_MODES and the same modes: a mixed batch, or a batch past
+ * WISE_DENSE_LIST_MAX_ROWS, without wise_compact_tiles.  modes must not be
+ * NULL; support may be NULL (sparse rows then get no item). */
+wise_status wise_build_list(const wise_shape *shape, const int8_t *modes,
+                            const int32_t *seq_lens, const uint32_t *support, void *workspace,
+                            size_t workspace_bytes, wise_stream_t stream);
+
 /* Split partial pass [WISE PR, "What changes": split-KV paged decode with
  * per-row modes].  For every work item written by wise_compact_tiles and
  * every query head of its KV head: online softmax over the item's tiles,
@@ -314,8 +328,9 @@ enum {
   /* Partial pass and finish: every row is sparse and the work list is list 1
    * (written by an earlier finish with WISE_FLAG_BUILD_SPARSE_LIST over the
    * same rows and lengths, or by wise_build_sparse_list); modes is ignored
-   * and may be NULL.  Both passes of
-   * the call take the flag.  Not with wise_decode_partial_finish. */
+   * and may be NULL (see WISE_FLAG_LIST_MODES for a list of any modes).
+   * Both passes of the call take the flag.  Not with
+   * wise_decode_partial_finish. */
   WISE_FLAG_SPARSE_LIST = 8u,
   /* Partial pass and finish: every row attends every block below its length
    * (sparse rows too), discover and discover-union rows (by modes) also
@@ -340,7 +355,13 @@ enum {
    * every read waits for the previous kernel (a programmatic dependent
    * launch sees that kernel's writes only past its dependency wait).  Other
    * passes accept and ignore it. */
-  WISE_FLAG_INPUTS_READY = 32u
+  WISE_FLAG_INPUTS_READY = 32u,
+  /* With WISE_FLAG_SPARSE_LIST: list 1 was built by wise_build_list for the
+   * modes this call passes, so the rows keep them -- the finish merges every
+   * row and, for discover rows, selects and writes (DISCOVER) or ORs
+   * (DISCOVER_UNION) the mask; modes must not be NULL.  The partial pass
+   * accepts and ignores it (the items carry their rows' flags). */
+  WISE_FLAG_LIST_MODES = 64u
 };
 
 /* Rows a call with WISE_FLAG_DENSE_LIST takes (its table lives in the
@@ -390,8 +411,9 @@ wise_status wise_decode_partial_finish(const wise_shape *shape, const void *q,
 /* The calls that read or write the mask, with the mask addressed through a
  * wise_mask (per-request slots and a layer of a mask pool) instead of a
  * [num_rows, num_kv_heads, W] array; otherwise as wise_compact_tiles,
- * wise_build_sparse_list, wise_decode_finish_ex, wise_decode and
- * wise_validate (a row without a mask slot gets no item in list 1).  `mask` is a HOST
+ * wise_build_sparse_list, wise_build_list, wise_decode_finish_ex,
+ * wise_decode and wise_validate (a sparse row without a mask slot gets no
+ * item in list 1).  `mask` is a HOST
  * pointer to the descriptor (its words and row_slot are device pointers);
  * mask->words may be NULL where the flat call's support may be NULL.  The
  * compaction reads each row's slot with its mode and length. */
@@ -402,6 +424,9 @@ wise_status wise_compact_tiles_m(const wise_shape *shape, const int8_t *modes,
 wise_status wise_build_sparse_list_m(const wise_shape *shape, const int32_t *seq_lens,
                                      const wise_mask *mask, void *workspace,
                                      size_t workspace_bytes, wise_stream_t stream);
+wise_status wise_build_list_m(const wise_shape *shape, const int8_t *modes,
+                              const int32_t *seq_lens, const wise_mask *mask, void *workspace,
+                              size_t workspace_bytes, wise_stream_t stream);
 wise_status wise_decode_finish_m(const wise_shape *shape, const int8_t *modes,
                                  const int32_t *seq_lens, void *workspace,
                                  size_t workspace_bytes, uint32_t flags,

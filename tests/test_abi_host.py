@@ -226,6 +226,29 @@ def test_build_sparse_list_checks(lib):
     assert lib.wise_build_sparse_list_m(ctypes.byref(s), P(16), None, P(4096), n, None) == 1
 
 
+def test_build_list_and_list_modes_checks(lib):
+    """wise_build_list needs the modes (the mask may be NULL: sparse rows then
+    get no item); WISE_FLAG_LIST_MODES goes with WISE_FLAG_SPARSE_LIST, and
+    its finish needs the modes."""
+    P = ctypes.c_void_p
+    s = _shape()
+    n = W.wise_workspace_bytes(s)
+    assert lib.wise_build_list(ctypes.byref(s), None, P(16), P(16), P(4096), n, None) == 1
+    assert b"modes" in lib.wise_last_error()
+    assert lib.wise_build_list(ctypes.byref(s), P(16), None, P(16), P(4096), n, None) == 1
+    assert lib.wise_build_list(ctypes.byref(s), P(16), P(16), P(16), P(4096), n - 1, None) == 3
+    LM = ctypes.c_uint32(W.FLAG_LIST_MODES)
+    assert lib.wise_decode_partial_ex(ctypes.byref(s), P(16), P(16), P(16), P(16), P(16), P(16),
+                                      P(4096), n, LM, None) == 1
+    assert b"WISE_FLAG_SPARSE_LIST" in lib.wise_last_error()
+    assert lib.wise_decode_finish_ex(ctypes.byref(s), P(16), P(16), P(4096), n, LM, None, P(16),
+                                     P(16), None) == 1
+    both = ctypes.c_uint32(W.FLAG_LIST_MODES | W.FLAG_SPARSE_LIST)
+    assert lib.wise_decode_finish_ex(ctypes.byref(s), None, P(16), P(4096), n, both, None, P(16),
+                                     P(16), None) == 1
+    assert W.FLAG_LIST_MODES == 64
+
+
 def test_max_blocks_limit(lib):
     """WISE_MAX_BLOCKS (rows of up to 128K tokens): the header, the binding and
     the shape check agree."""

@@ -1,5 +1,6 @@
 """wise_build_sparse_list: list 1 of an all-sparse call built from the mask
-alone (no compaction, no finish before it).  Its items equal those a finish
+alone (no compaction, no finish before it); wise_build_list: the same for a
+call of any modes (run with WISE_FLAG_LIST_MODES).  Its items equal those a finish
 with WISE_FLAG_BUILD_SPARSE_LIST writes for the same mask, they partition the
 oracle's compacted tile lists, the sparse call on them equals the compaction's
 call bit for bit where the finish merges the same slots in the same order
@@ -13,7 +14,7 @@ import torch
 import block_sparse_paged_split_gb300 as W
 from block_sparse_paged_split_gb300.workload import custom_workload
 from oracle import wise_oracle as O
-from tests.gpu_harness import (Batch, compare_outputs, dev_support, gpu_call, item_fields,
+from tests.gpu_harness import (Batch, compare_masks, compare_outputs, dev_support, gpu_call, item_fields,
                                item_invariant_fails, list1_schedule, np_support, oracle_call,
                                shape_for, words)
 
@@ -209,3 +210,98 @@ def test_built_list_clamps_and_flags_long_lengths():
     v = _views(shape, ws)
     assert int(v["status"][0]) & W.wise.DEVERR_SEQ_LEN_CLAMPED
     assert int(v["head_info_1"][0, 0, 2]) == -(-cap // 32)  # every block below the capacity
+
+
+# ---------------------------------------------------------------- any modes
+MIXED = np.array([1, 2, 0, 3, 1, 2, 3, 3], np.int8)  # discover, union, dense, sparse
+
+
+def _mixed_on_built_list(b, shape, modes_np, sup, depth=0, ws=None):
+    """wise_build_list, then the partial pass and finish on list 1 with the
+    rows' modes (WISE_FLAG_SPARSE_LIST | WISE_FLAG_LIST_MODES)."""
+    w = b.w
+    d = b.dev(depth)
+    ws = W.alloc_workspace(shape) if ws is None else ws
+    modes = torch.from_numpy(modes_np).cuda()
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.num_rows, w.num_q_heads), dtype=torch.float32, device="cuda")
+    f = W.FLAG_SPARSE_LIST | W.FLAG_LIST_MODES
+    W.wise_build_list(shape, modes, b.seq_lens, sup, ws)
+    W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
+                             modes, ws, f)
+    W.wise_decode_finish_ex(shape, modes, b.seq_lens, ws, sup, out, lse, f)
+    torch.cuda.synchronize()
+    return out, lse, ws
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
+def test_mixed_call_on_built_list_equals_compaction(Hq, Hkv, D, dtype):
+    """Rows of every mode in one call: on the list built for the modes it
+    equals the compaction's call bit for bit (outputs, LSEs and the mask the
+    discover rows leave), its items partition the oracle's lists for the same
+    modes, and it agrees with the oracle."""
+    w = _wl(Hq, Hkv, D, dtype)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    T = W.wise._tiles_per_item(shape)
+    sup_np = _random_mask(w, 0.3, seed=83)
+    g = gpu_call(b, 0, MIXED, sup_np)
+    sup = dev_support(sup_np)
+    ws = None
+    for _ in range(2):  # the second call reuses the workspace
+        sup.copy_(dev_support(sup_np))
+        out, lse, ws = _mixed_on_built_list(b, shape, MIXED, sup, ws=ws)
+        assert torch.equal(out.cpu(), g["out_raw"]) and np.array_equal(lse.cpu().numpy(), g["lse"])
+        assert np.array_equal(np_support(sup), g["support"])
+        v = _views(shape, ws)
+        assert int(v["status"][0]) == 0
+    ref = O.compact_tiles(sup_np, MIXED, w.seq_lens, 32)
+    fails = item_invariant_fails(list1_schedule(v, T), v["head_info_1"].numpy(), ref["lists"], T,
+                                 -(-shape.max_blocks // T), w.seq_lens, MIXED, Hkv, compact_slots=True)
+    assert not fails, fails[:5]
+    o = oracle_call(b, 0, MIXED, sup_np)
+    assert not compare_outputs(w, {"out": out.double().cpu().numpy(), "lse": lse.cpu().numpy()}, o)
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens", [(2, 2, np.array([20000, 3000, 0, 700, 17000], np.int32)),
+                                         (8, 2, np.array([40000, 33, 9000, 0, 131072], np.int32))])
+def test_mixed_long_rows_on_built_list(Hq, Hkv, lens):
+    """Long rows of every mode (the clustered finish selects on list 1): the
+    outputs and the masks against the oracle on the same input mask."""
+    w = _wl(Hq, Hkv, 128, "bf16", lens=lens)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    modes_np = np.array([1, 3, 2, 3, 0], np.int8)[:R]
+    sup_np = _random_mask(w, 0.05, seed=89)
+    sup = dev_support(sup_np)
+    out, lse, ws = _mixed_on_built_list(b, shape, modes_np, sup)
+    assert int(_views(shape, ws)["status"][0]) == 0
+    g = {"out": out.double().cpu().numpy(), "lse": lse.cpu().numpy(), "support": np_support(sup)}
+    o = oracle_call(b, 0, modes_np, sup_np)
+    fails = compare_outputs(w, g, o)
+    fails += compare_masks(w, g["support"], o, modes_np, support_in=sup_np)["fails"]
+    assert not fails, fails[:5]
+
+
+def test_large_mixed_batch_on_built_list():
+    """300 rows (past the dense list's limit) of every mode, no compaction:
+    sampled rows against the oracle."""
+    rng = np.random.default_rng(97)
+    lens = rng.integers(0, 1500, size=300).astype(np.int32)
+    w = _wl(4, 2, 128, "bf16", lens=lens)
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    modes_np = rng.integers(0, 4, size=R).astype(np.int8)
+    sup_np = _random_mask(w, 0.2, seed=101)
+    sup = dev_support(sup_np)
+    out, lse, ws = _mixed_on_built_list(b, shape, modes_np, sup)
+    assert int(_views(shape, ws)["status"][0]) == 0
+    rows = np.unique(np.concatenate([[0, R - 1], rng.choice(R, size=22, replace=False)]))
+    g = {"out": out.double().cpu().numpy(), "lse": lse.cpu().numpy(), "support": np_support(sup)}
+    o = oracle_call(b, 0, modes_np, sup_np, rows=rows)
+    fails = compare_outputs(w, g, o, rows=rows)
+    fails += compare_masks(w, g["support"], o, modes_np, rows=rows, support_in=sup_np)["fails"]
+    assert not fails, fails[:5]
