@@ -71,14 +71,14 @@ def _status(pipe):
     return int(W.workspace_views(pipe.shape, pipe.ws)["status"].item())
 
 
-def _check_step(name, rows=None, device_inputs=False, early=False):
+def _check_step(name, rows=None, device_inputs=False, early=False, mixed_list=False):
     w = make_workload(name)
-    pipe = bench.Pipeline(w, device_inputs=device_inputs, early_lists=early)
+    pipe = bench.Pipeline(w, device_inputs=device_inputs, early_lists=early, mixed_list=mixed_list)
     for _ in range(2):  # the step as the benchmark replays it, on a used workspace
         pipe.run(pipe.wise_step)
     torch.cuda.synchronize()
     assert not any(c[0] == "compact" for _, m, calls in pipe.wise_step for c in calls
-                   if "mixed" not in m), "a compaction launch in a compaction-free step"
+                   if mixed_list or "mixed" not in m), "a compaction launch in a compaction-free step"
     snaps = _depthwise(pipe, pipe.wise_step)
     assert _status(pipe) == 0
     # one graph replay of the whole step gives the same bits
@@ -142,6 +142,13 @@ def test_bench_step_mixed_8k_sampled():
     sparse rows), the first three rows of each mode."""
     report = _check_step("mixed_8k", rows="by_mode", device_inputs=True)
     assert sum(c + m + g for _, c, m, g in report) > 0  # discover rows were among them
+
+
+def test_bench_step_mixed_8k_on_a_built_list():
+    """The same mixed call with `bench.py --mixed-list`: its work list built
+    from the rows' modes and masks (wise_build_list), no compaction."""
+    report = _check_step("mixed_8k", rows="by_mode", device_inputs=True, mixed_list=True)
+    assert sum(c + m + g for _, c, m, g in report) > 0
 
 
 def test_bench_step_gqa_32k_sampled():
