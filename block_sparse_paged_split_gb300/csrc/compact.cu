@@ -294,7 +294,10 @@ __global__ void __launch_bounds__(kBuildThreads)
 cudaError_t launch_build_list(const KParams& kp, const int8_t* modes, const int32_t* seq_lens,
                               const MaskView& mv, const WsView& ws, cudaStream_t stream) {
   if (kp.R == 0) return cudaSuccess;
-  return launch_pdl(build_list_kernel, dim3(kp.R * kp.Hkv), dim3(kBuildThreads), 0, stream, modes,
+  // A pair's ranges in one pass of the CTA's threads: one warp (its barriers
+  // are then a warp's) up to 32 ranges, four warps beyond.
+  const int threads = kp.S_max <= 32 ? 32 : kBuildThreads;
+  return launch_pdl(build_list_kernel, dim3(kp.R * kp.Hkv), dim3(threads), 0, stream, modes,
                     seq_lens, mv, ws, kp);
 }
 
