@@ -305,3 +305,51 @@ def test_large_mixed_batch_on_built_list():
     fails = compare_outputs(w, g, o, rows=rows)
     fails += compare_masks(w, g["support"], o, modes_np, rows=rows, support_in=sup_np)["fails"]
     assert not fails, fails[:5]
+
+
+def test_mixed_list_on_a_slot_pool():
+    """A call of every mode on a list built from a slot pool
+    (wise_build_list_m, then the finish through the same descriptor): equal,
+    bit for bit, to the same call on the gathered masks, and the discover
+    rows write their selections into their own slots only."""
+    w = _wl(4, 4, 128, "bf16")
+    b = Batch(w)
+    R = w.num_rows
+    shape = shape_for(w)
+    slots, layers, layer = 11, 3, 1
+    rng = np.random.default_rng(103)
+    bits = rng.random((slots, layers, 4, words(w) * 32)) < 0.3
+    pool_np = np.packbits(bits, axis=-1, bitorder="little").view(np.uint32).reshape(
+        slots, layers, 4, -1).copy()
+    row_slot = rng.permutation(slots)[:R].astype(np.int32)
+    row_slot[6] = -1  # a sparse row (MIXED[6] == 3) without a mask
+    modes = torch.from_numpy(MIXED).cuda()
+    f = W.FLAG_SPARSE_LIST | W.FLAG_LIST_MODES
+    d = b.dev(0)
+    # on the pool
+    pool = dev_support(pool_np)
+    mask = W.make_mask(pool, torch.from_numpy(row_slot).cuda(), layer)
+    ws = W.alloc_workspace(shape)
+    out_a = torch.empty_like(d["q"])
+    lse_a = torch.empty((R, 4), dtype=torch.float32, device="cuda")
+    W.wise_build_list_m(shape, modes, b.seq_lens, mask, ws)
+    W.wise_decode_partial_ex(shape, d["q"], d["k_cache"], d["v_cache"], b.page_table, b.seq_lens,
+                             modes, ws, f)
+    W.wise_decode_finish_m(shape, modes, b.seq_lens, ws, mask, out_a, lse_a, f)
+    # on the gathered masks
+    gathered = O.gather_slot_masks(pool_np, row_slot, layer)
+    sup = dev_support(gathered)
+    out_b, lse_b, _ = _mixed_on_built_list(b, shape, MIXED, sup)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    after = np_support(pool)
+    g_after = np_support(sup)
+    for r, sl in enumerate(row_slot):
+        if sl >= 0:
+            assert np.array_equal(after[sl, layer], g_after[r]), r
+    touched = {(int(sl), layer) for sl in row_slot if sl >= 0}
+    for sl in range(slots):
+        for ly in range(layers):
+            if (sl, ly) not in touched:
+                assert np.array_equal(after[sl, ly], pool_np[sl, ly]), (sl, ly)
+    assert torch.all(out_a[6] == 0) and torch.all(torch.isneginf(lse_a[6]))
