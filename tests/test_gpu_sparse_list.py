@@ -178,9 +178,9 @@ def test_built_list_from_a_slot_pool():
     row_slot = rng.permutation(slots)[:R].astype(np.int32)
     row_slot[3] = -1
     pool = dev_support(pool_np)
+    slots_t = torch.from_numpy(row_slot).cuda()  # the descriptor holds its address
     ws_a = W.alloc_workspace(shape)
-    W.wise_build_sparse_list_m(shape, b.seq_lens,
-                               W.make_mask(pool, torch.from_numpy(row_slot).cuda(), layer), ws_a)
+    W.wise_build_sparse_list_m(shape, b.seq_lens, W.make_mask(pool, slots_t, layer), ws_a)
     out, lse = _sparse_on_list(b, shape, ws_a)
     gathered = O.gather_slot_masks(pool_np, row_slot, layer)
     ws_b = W.alloc_workspace(shape)
@@ -328,7 +328,8 @@ def test_mixed_list_on_a_slot_pool():
     d = b.dev(0)
     # on the pool
     pool = dev_support(pool_np)
-    mask = W.make_mask(pool, torch.from_numpy(row_slot).cuda(), layer)
+    slots_t = torch.from_numpy(row_slot).cuda()  # alive while the descriptor is used
+    mask = W.make_mask(pool, slots_t, layer)
     ws = W.alloc_workspace(shape)
     out_a = torch.empty_like(d["q"])
     lse_a = torch.empty((R, 4), dtype=torch.float32, device="cuda")
