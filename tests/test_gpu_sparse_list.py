@@ -24,11 +24,12 @@ RAGGED = np.array([1, 31, 32, 33, 300, 517, 0, 1024], np.int32)
 CASES = [(4, 4, 128, "bf16"), (8, 2, 128, "bf16"), (4, 1, 64, "bf16"), (4, 2, 128, "f32")]
 
 
-def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=61):
+def _wl(Hq, Hkv, D, dtype, lens=RAGGED, seed=61, page_size=16):
     R = len(lens)
     return custom_workload("sparse_list", R=R, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, depths=2,
                            n_planted=3, seq_lens=lens, pool_factor=2, seed=seed,
-                           depth_modes=[np.full(R, W.MODE_SPARSE, np.int8)] * 2)
+                           depth_modes=[np.full(R, W.MODE_SPARSE, np.int8)] * 2,
+                           page_size=page_size)
 
 
 def _random_mask(w, density, seed):
@@ -234,13 +235,15 @@ def _mixed_on_built_list(b, shape, modes_np, sup, depth=0, ws=None):
     return out, lse, ws
 
 
-@pytest.mark.parametrize("Hq,Hkv,D,dtype", CASES)
-def test_mixed_call_on_built_list_equals_compaction(Hq, Hkv, D, dtype):
+@pytest.mark.parametrize("Hq,Hkv,D,dtype,page_size", [c + (16,) for c in CASES] +
+                         [(8, 1, 128, "bf16", 16), (4, 4, 128, "bf16", 32), (8, 2, 64, "f32", 32)])
+def test_mixed_call_on_built_list_equals_compaction(Hq, Hkv, D, dtype, page_size):
     """Rows of every mode in one call: on the list built for the modes it
     equals the compaction's call bit for bit (outputs, LSEs and the mask the
     discover rows leave), its items partition the oracle's lists for the same
-    modes, and it agrees with the oracle."""
-    w = _wl(Hq, Hkv, D, dtype)
+    modes, and it agrees with the oracle.  Eight query heads a KV head, and
+    pages of 32 tokens (one page a tile) too."""
+    w = _wl(Hq, Hkv, D, dtype, page_size=page_size)
     b = Batch(w)
     R = w.num_rows
     shape = shape_for(w)
