@@ -5,18 +5,24 @@ One step = one decode step of one layer over the Ouro-1.4B-shaped batch
 (64 rows x 1024 tokens, 16 heads MHA, head dim 128, bf16, page 16, B=32)
 through its four recurrent depths, each with its own K/V pool:
 
-    depth 0  discover         compact + partial + finish
-    depth 1  union-discover   partial + finish (the same work list as depth 0)
-    depth 2  sparse           compact + partial + finish
-    depth 3  sparse           partial + finish (the mask is depth 2's)
+    depth 0  discover         partial + finish, on the work list the partial
+                              pass derives from the row lengths (dense list)
+    depth 1  union-discover   the same; its finish also writes the sparse
+                              depths' work list (list 1)
+    depth 2  sparse           partial + finish on list 1
+    depth 3  sparse           partial + finish on list 1 (read before the
+                              dependency wait)
 
-(`--fold`: the finish folded into the partial pass, for rows of at most 64
-blocks.)  `value` is decode attention rows per second over the whole step
-(4 x 64 row-calls per step).  Every kernel launch in the timed region is
-bracketed by CUDA events on the launching stream, which gives the per-mode
-times and the roofline of the dominant kernel (the split partial pass).  The same K steps
-are also timed in dense mode (the baseline the method is compared with).
-Inputs per step are 2.1 GB of K/V (larger than the 129 MB L2).
+No depth launches a compaction; a depth that mixes sparse rows with others
+(the mixed 8K batch) takes a work list built for its modes (wise_build_list).
+`value` is decode attention rows per second over the whole step (4 x 64
+row-calls per step), timed over CUDA-graph replays of the step.  The same K
+steps launched eagerly, every launch bracketed by CUDA events on the
+launching stream, give the per-mode times and the roofline of the dominant
+kernel (the split partial pass); `e2e` adds each step's host copies.  The
+dense baseline runs the same launches with every row dense.  Inputs per step
+are 2.1 GB of K/V (larger than the 129 MB L2).  The other workloads (4K,
+mixed 8K, GQA 32K) follow in `modes_by_workload`.
 
 `--impl reference` times the CPU oracle (the definition the kernels are
 checked against) on a bounded sample of the same workload.
@@ -86,9 +92,10 @@ def parse():
     p.add_argument("--no-sparse-list", action="store_true",
                    help="sparse depths get their own compaction instead of the work list the "
                         "previous depth's finish builds")
-    p.add_argument("--mixed-list", action="store_true",
-                   help="depths that mix sparse rows with others take their work list from "
-                        "wise_build_list (run with WISE_FLAG_LIST_MODES) instead of a compaction")
+    p.add_argument("--no-mixed-list", action="store_true",
+                   help="depths that mix sparse rows with others get a compaction instead of "
+                        "the work list wise_build_list builds for their modes (measured: the "
+                        "same step time at 8K; the built list stays flat past it)")
     p.add_argument("--fold", action="store_true",
                    help="fold the finish into the partial pass (rows of at most 64 blocks)")
     p.add_argument("--sparse-scaling", action="store_true",
@@ -352,7 +359,7 @@ class Pipeline:
     def __init__(self, w, tiles_per_item: int = 0, fold: bool = False, head_union: bool = False,
                  lse_discover: bool = False, overlap: bool = False, share=None,
                  sparse_list: bool = True, device_inputs: bool = False, dense_list: bool = True,
-                 early_lists: bool = False, mixed_list: bool = False):
+                 early_lists: bool = False, mixed_list: bool = True):
         import numpy as np
         import torch
         import block_sparse_paged_split_gb300 as W
@@ -1004,7 +1011,7 @@ def sweep_workload(name, args, steps, peak):
     w = make_workload(name, **eta_kw(args.eta))
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
                     device_inputs=True, dense_list=not args.no_dense_list,
-                    early_lists=args.early, mixed_list=args.mixed_list)
+                    early_lists=args.early, mixed_list=not args.no_mixed_list)
     for _ in range(3):
         pipe.run(pipe.wise_step)
         pipe.run(pipe.dense_step)
@@ -1055,7 +1062,7 @@ def eta_point(name, eta, args, steps):
     w = make_workload(name, eta=eta)
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, sparse_list=not args.no_sparse_list,
                     device_inputs=True, dense_list=not args.no_dense_list,
-                    early_lists=args.early, mixed_list=args.mixed_list)
+                    early_lists=args.early, mixed_list=not args.no_mixed_list)
     for _ in range(3):
         pipe.run(pipe.wise_step)
     torch.cuda.synchronize()
@@ -1102,7 +1109,7 @@ def main_ours(args):
     pipe = Pipeline(w, tiles_per_item=args.tiles_per_item, fold=args.fold, head_union=args.head_union,
                     lse_discover=args.lse_discover, overlap=args.overlap,
                     sparse_list=not args.no_sparse_list, dense_list=not args.no_dense_list,
-                    early_lists=args.early, mixed_list=args.mixed_list)
+                    early_lists=args.early, mixed_list=not args.no_mixed_list)
 
     for _ in range(max(args.warmup, 3)):
         pipe.run(pipe.wise_step)
@@ -1185,7 +1192,7 @@ def main_ours(args):
                       head_union=args.head_union, lse_discover=args.lse_discover,
                       overlap=args.overlap, share=pipe, sparse_list=not args.no_sparse_list,
                       dense_list=not args.no_dense_list,
-                    early_lists=args.early, mixed_list=args.mixed_list)
+                    early_lists=args.early, mixed_list=not args.no_mixed_list)
     graph_b = pipe_b.graph(pipe_b.wise_step)
     e2e_ms, h2d, d2h = e2e_pipelined([pipe, pipe_b], [graph, graph_b], args.steps)
     e2e_serial_ms, _, _ = e2e_region(pipe, args.steps, graph)

@@ -67,12 +67,18 @@ def test_gpu_arm_line():
     dens = [p["support_density_blocks"] for p in pts]
     assert all(0 < d <= 1 for d in dens) and dens == sorted(dens)
     assert all(p["step_ms"] > 0 and p["dense_step_ms"] > 0 for p in pts)
-    # no depth of the headline step launches a compaction: the sparse depths
-    # run on the list the union depth built, the others on the dense list
+    # no depth of any workload's step launches a compaction: the sparse
+    # depths run on the list the union depth built, the dense and discover
+    # depths on the dense list, the mixed call on a list built for its modes
     assert "no compaction launch" in out["config"]["workload"]
     for mode, row in out["modes"].items():
         if mode.startswith("depth"):
             assert "compact" not in row["kernels_us"], mode
+    for name, res in sweep.items():
+        for mode, row in res["modes"].items():
+            if mode.startswith("depth"):
+                assert "compact" not in row["kernels_us"], (name, mode)
+    assert "build_list" in sweep["mixed_8k"]["modes"]["depth0_mixed"]["kernels_us"]
 
 
 @pytest.mark.gpu

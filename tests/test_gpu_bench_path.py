@@ -3,9 +3,10 @@
 bench.py's `Pipeline` builds the WISE step the headline times: discover and
 union-discover on work lists derived from the row lengths, the union depth's
 finish writing the sparse depths' work list, the second sparse depth reading
-its list before the dependency wait, no compaction launch (mixed batches keep
-theirs).  Here that same step runs depth by depth (each depth's output and the
-mask it leaves snapshotted) and as one replay of its CUDA graph (bitwise equal
+its list before the dependency wait, no compaction launch (a mixed batch's
+list is built for its modes).  Here that same step runs depth by depth (each
+depth's output and the mask it leaves snapshotted) and as one replay of its
+CUDA graph (bitwise equal
 to the depth-by-depth run), and every depth is checked against the oracle on
 the inputs the step actually used: every row at 1K, sampled rows beyond (the
 oracle computes them one by one from the rows' own pages, gathered from the
@@ -71,7 +72,7 @@ def _status(pipe):
     return int(W.workspace_views(pipe.shape, pipe.ws)["status"].item())
 
 
-def _check_step(name, rows=None, device_inputs=False, early=False, mixed_list=False):
+def _check_step(name, rows=None, device_inputs=False, early=False, mixed_list=True):
     w = make_workload(name)
     pipe = bench.Pipeline(w, device_inputs=device_inputs, early_lists=early, mixed_list=mixed_list)
     for _ in range(2):  # the step as the benchmark replays it, on a used workspace
@@ -138,16 +139,16 @@ def test_bench_step_4k_sampled():
 
 
 def test_bench_step_mixed_8k_sampled():
-    """32 ragged rows up to 8K in one mixed call (compaction kept for the
-    sparse rows), the first three rows of each mode."""
+    """32 ragged rows up to 8K in one mixed call on the work list built for
+    its modes and masks (no compaction), the first three rows of each mode."""
     report = _check_step("mixed_8k", rows="by_mode", device_inputs=True)
     assert sum(c + m + g for _, c, m, g in report) > 0  # discover rows were among them
 
 
-def test_bench_step_mixed_8k_on_a_built_list():
-    """The same mixed call with `bench.py --mixed-list`: its work list built
-    from the rows' modes and masks (wise_build_list), no compaction."""
-    report = _check_step("mixed_8k", rows="by_mode", device_inputs=True, mixed_list=True)
+def test_bench_step_mixed_8k_on_a_compaction():
+    """The same mixed call with `bench.py --no-mixed-list`: a compaction
+    instead of the work list built for the modes."""
+    report = _check_step("mixed_8k", rows="by_mode", device_inputs=True, mixed_list=False)
     assert sum(c + m + g for _, c, m, g in report) > 0
 
 
